@@ -1,0 +1,170 @@
+"""Oracle for block-sparse GQA attention: a plain fp64 CPU statement of the method.
+
+TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code with
+the CUDA library (``block_sparse_gqa_gb300``) and neither imports the other.
+
+The arithmetic lives in ``msa_oracle.c`` (compiled with gcc, no fast-math); this
+module only builds it and marshals numpy arrays.  See that file's header for the
+passages each function follows and the readings taken where the pages are silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "msa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+FMT_BF16, FMT_E4M3, FMT_F64 = 0, 1, 2
+DISPATCH_KV_OUTER, DISPATCH_Q_OUTER = 1, 2
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile msa_oracle.c into liboracle.so next to it (IEEE double, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fno-fast-math",
+                               "-ffp-contract=off", "-o", tmp, _SRC, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_attn_fwd.restype = i32
+        lib.oracle_attn_fwd.argtypes = [P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32,
+                                        f64, f64, f64, f64, P, i32, P, P, i32]
+        lib.oracle_schedule.restype = i32
+        lib.oracle_schedule.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
+        lib.oracle_worklist.restype = ctypes.c_long
+        lib.oracle_worklist.argtypes = [P, P, i32, i32, P, ctypes.c_long]
+        lib.oracle_lse_merge.restype = None
+        lib.oracle_lse_merge.argtypes = [i32, i32, P, P, P, P]
+        lib.oracle_bf16_decode.restype = f64
+        lib.oracle_bf16_decode.argtypes = [ctypes.c_uint16]
+        lib.oracle_e4m3_decode.restype = f64
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_dispatch.restype = i32
+        lib.oracle_dispatch.argtypes = [ctypes.c_int32, i32]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _fmt_of(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return FMT_BF16
+    if a.dtype == np.uint8:
+        return FMT_E4M3
+    if a.dtype == np.float64:
+        return FMT_F64
+    raise TypeError(f"oracle inputs are bf16 bits (uint16), e4m3 bytes (uint8) or float64, got {a.dtype}")
+
+
+def attn_fwd(Q, K, V, indices, *, Lkv, block=128, scale, q_descale=1.0, k_descale=1.0,
+             v_descale=1.0, qids=None, nthreads=None):
+    """O [nq,Hq,D] and LSE [nq,Hq] (float64) for the queries ``qids`` (default: all).
+
+    Q [N,Hq,D], K/V [Lkv,Hkv,D] as bf16 bit patterns (uint16), e4m3 bytes (uint8) or
+    float64; indices [N,Hkv,topK] int32.  Returns (O, LSE, status) with status 1 when
+    an invalid block id (>= nblocks or < -1) was seen and ignored.
+    """
+    lib = _load()
+    Q = np.ascontiguousarray(Q); K = np.ascontiguousarray(K); V = np.ascontiguousarray(V)
+    fmt = _fmt_of(Q)
+    if _fmt_of(K) != fmt or _fmt_of(V) != fmt:
+        raise TypeError("Q, K and V must share one storage format")
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    N, Hq, D = Q.shape
+    Hkv = K.shape[1]
+    topK = indices.shape[2]
+    assert K.shape == (Lkv, Hkv, D) and V.shape == K.shape and indices.shape == (N, Hkv, topK)
+    if qids is None:
+        qids = np.arange(N, dtype=np.int32)
+    qids = np.ascontiguousarray(qids, dtype=np.int32)
+    nq = len(qids)
+    O = np.zeros((nq, Hq, D), np.float64)
+    LSE = np.zeros((nq, Hq), np.float64)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    st = lib.oracle_attn_fwd(_ptr(Q), _ptr(K), _ptr(V), fmt, _ptr(indices), N, Lkv, Hq, Hkv, D,
+                             topK, block, float(scale), float(q_descale), float(k_descale),
+                             float(v_descale), _ptr(qids), nq, _ptr(O), _ptr(LSE), int(nthreads))
+    if st < 0:
+        raise ValueError("oracle_attn_fwd rejected its arguments")
+    return O, LSE, st
+
+
+def schedule(indices, *, Lkv, block=128):
+    """Reverse index of the lists: dict with counts, offsets, qlist, slot, cmap, E, nsb, status."""
+    lib = _load()
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    N, Hkv, topK = indices.shape
+    nblocks = Lkv // block
+    R = Hkv * nblocks
+    cap = max(N * Hkv * topK, 1)
+    counts = np.zeros(R, np.int32)
+    offsets = np.zeros(R + 1, np.int32)
+    qlist = np.zeros(cap, np.int32)
+    slot = np.zeros(cap, np.int32)
+    cmap = np.zeros((N, Hkv, topK), np.int32)
+    E = ctypes.c_int64(0)
+    nsb = ctypes.c_int32(0)
+    st = lib.oracle_schedule(_ptr(indices), N, Lkv, Hkv, topK, block, _ptr(counts), _ptr(offsets),
+                             _ptr(qlist), _ptr(slot), _ptr(cmap), ctypes.byref(E), ctypes.byref(nsb))
+    E = int(E.value)
+    return dict(counts=counts, offsets=offsets, qlist=qlist[:E].copy(), slot=slot[:E].copy(),
+                cmap=cmap, E=E, nsb=int(nsb.value), status=int(st))
+
+
+def worklist(counts, offsets, tile_rows=8):
+    """Tiles (row, first, count) of at most tile_rows entries, in row order."""
+    lib = _load()
+    counts = np.ascontiguousarray(counts, dtype=np.int32)
+    offsets = np.ascontiguousarray(offsets, dtype=np.int32)
+    R = len(counts)
+    cap = int(sum((int(c) + tile_rows - 1) // tile_rows for c in counts)) + 1
+    tiles = np.zeros((cap, 3), np.int32)
+    T = lib.oracle_worklist(_ptr(counts), _ptr(offsets), R, tile_rows, _ptr(tiles), cap)
+    assert T >= 0
+    return tiles[:T].copy()
+
+
+def lse_merge(O_parts, lse_parts):
+    """Merge n partial (O_k [n,D], lse_k [n]) results of one (query, head)."""
+    lib = _load()
+    O_parts = np.ascontiguousarray(O_parts, dtype=np.float64)
+    lse_parts = np.ascontiguousarray(lse_parts, dtype=np.float64)
+    n, D = O_parts.shape
+    O = np.zeros(D, np.float64)
+    lse = ctypes.c_double(0.0)
+    lib.oracle_lse_merge(n, D, _ptr(O_parts), _ptr(lse_parts), _ptr(O), ctypes.byref(lse))
+    return O, lse.value
+
+
+def bf16_decode(bits: int) -> float:
+    return _load().oracle_bf16_decode(int(bits))
+
+
+def e4m3_decode(byte: int) -> float:
+    return _load().oracle_e4m3_decode(int(byte))
+
+
+def dispatch(nsb: int, N: int) -> int:
+    """1 = KV-outer, 2 = Q-outer (crossover nsb/N < 2.85)."""
+    return _load().oracle_dispatch(int(nsb), int(N))

@@ -1,0 +1,311 @@
+/*
+ * Oracle for block-sparse GQA attention (forward main branch).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously-correct CPU
+ * statement of what the GPU path computes.  Only the test suite, the smoke check
+ * and the CPU-baseline leg of the benchmark may load it.  It shares no code, header
+ * or table with the CUDA library, and the CUDA library never calls it.
+ *
+ * Arithmetic is IEEE double throughout (compiled without fast-math); exp/log are
+ * libm's.  Inputs are decoded exactly from their storage format (bf16 bit patterns,
+ * OCP FP8 E4M3 bytes, or doubles) before any arithmetic.
+ *
+ * Sources (page title, section):
+ *  - "Kernel optimization for MiniMax M3 on NVIDIA Blackwell" (Fireworks), opening
+ *    section: KV sequence cut into 128-token blocks; each GQA group of a query
+ *    selects topK blocks; exact attention over only the selected blocks.
+ *  - "Sparse Attention" (dinara-dl), Chapter 1: the softmax of a query is normalised
+ *    over the keys of all its selected blocks together; unselected keys get weight 0.
+ *  - "Flash-MSA" post: the local block of every token is always attended, sliding-
+ *    window style (causal inside the block); selection is per GQA (proxy) head.
+ *  - "Sparse Attention", Chapter 5, "Reverse index": for each block, the list of
+ *    queries that chose it, plus the block's place in each query's list.
+ *  - "Sparse Attention", Chapter 5, "Partial outputs and Combine": partials are merged
+ *    with weights computed from their log-sum-exp values.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - queries occupy the last N positions of the KV sequence: pos(i) = Lkv - N + i;
+ *  - key j is visible to query i iff j <= pos(i) (diagonal included);
+ *  - block ids per list: -1 is padding; a repeated id counts once (union); an id
+ *    beyond the query's own block contributes nothing; an id >= nblocks or < -1 is
+ *    invalid: it is ignored and reported through the status return;
+ *  - head h belongs to group h / (Hq/Hkv);
+ *  - LSE is the natural log of sum_j exp(s_j); an empty key set gives O = 0 and
+ *    LSE = -inf;
+ *  - schedule rows are r = g * nblocks + b; each row lists its queries ascending,
+ *    with the slot (list position) of the first occurrence of b in the query's list.
+ *
+ * Pins: every function here is checked by the CPU test suite against results fixed
+ * independently of this file (dense causal attention, explicit single-block softmax,
+ * closed forms, brute-force masks, invariances, the worked example of the reverse
+ * index).  The work-list split rule and the dispatch threshold constant are
+ * builder-defined; their restatement here is parity unpinned.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_IN_BF16 = 0, ORC_IN_E4M3 = 1, ORC_IN_F64 = 2 };
+
+/* bf16 is the upper 16 bits of an IEEE binary32: widening is exact. */
+double oracle_bf16_decode(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* OCP 8-bit floating point specification, E4M3: 1 sign bit, 4 exponent bits
+ * (bias 7), 3 mantissa bits; no infinities; S.1111.111 is NaN; exponent field 0
+ * encodes subnormals m/8 * 2^-6. */
+double oracle_e4m3_decode(uint8_t byte) {
+  int sign = (byte >> 7) & 1;
+  int e = (byte >> 3) & 0xF;
+  int m = byte & 0x7;
+  double v;
+  if (e == 0xF && m == 0x7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+static double load_elem(const void* base, int fmt, size_t idx) {
+  switch (fmt) {
+    case ORC_IN_BF16: return oracle_bf16_decode(((const uint16_t*)base)[idx]);
+    case ORC_IN_E4M3: return oracle_e4m3_decode(((const uint8_t*)base)[idx]);
+    default: return ((const double*)base)[idx];
+  }
+}
+
+typedef struct {
+  const void *Q, *K, *V;
+  int fmt;
+  const int32_t* indices;
+  int N, Lkv, Hq, Hkv, D, topK, block;
+  double scale, q_descale, k_descale, v_descale;
+  const int32_t* qids; /* which queries to evaluate (row i of the output = qids[i]) */
+  int nq;
+  double *O, *LSE; /* [nq, Hq, D], [nq, Hq] */
+  int next;        /* work counter */
+  pthread_mutex_t mu;
+  int bad;         /* invalid index seen */
+} attn_job;
+
+/* One (query, head): gather the keys of the selected blocks, mask causally,
+ * softmax over their union, weighted sum of V. */
+static void attn_one(attn_job* J, int row, int h, double* q, double* s, int* keys) {
+  const int i = J->qids[row];
+  const int G = J->Hq / J->Hkv;
+  const int g = h / G;
+  const int nblocks = J->Lkv / J->block;
+  const long pos = (long)J->Lkv - J->N + i;
+  const long lb = pos / J->block;
+  const int D = J->D;
+  double* O = J->O + ((size_t)row * J->Hq + h) * D;
+
+  for (int d = 0; d < D; ++d)
+    q[d] = load_elem(J->Q, J->fmt, ((size_t)i * J->Hq + h) * D + d) * J->q_descale;
+
+  /* the set S of selected blocks: first occurrence of each id, pads and
+   * future blocks excluded */
+  const int32_t* lst = J->indices + ((size_t)i * J->Hkv + g) * J->topK;
+  int nkeys = 0;
+  for (int k = 0; k < J->topK; ++k) {
+    int b = lst[k];
+    if (b < -1 || b >= nblocks) { J->bad = 1; continue; }
+    if (b == -1 || b > lb) continue;
+    int dup = 0;
+    for (int k2 = 0; k2 < k; ++k2) if (lst[k2] == b) { dup = 1; break; }
+    if (dup) continue;
+    for (int t = 0; t < J->block; ++t) {
+      long j = (long)b * J->block + t;
+      if (j <= pos) keys[nkeys++] = (int)j;
+    }
+  }
+  if (nkeys == 0) {
+    for (int d = 0; d < D; ++d) O[d] = 0.0;
+    J->LSE[(size_t)row * J->Hq + h] = -INFINITY;
+    return;
+  }
+  double m = -INFINITY;
+  for (int t = 0; t < nkeys; ++t) {
+    size_t kb = ((size_t)keys[t] * J->Hkv + g) * D;
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d) acc += q[d] * (load_elem(J->K, J->fmt, kb + d) * J->k_descale);
+    s[t] = J->scale * acc;
+    if (s[t] > m) m = s[t];
+  }
+  double l = 0.0;
+  for (int t = 0; t < nkeys; ++t) { s[t] = exp(s[t] - m); l += s[t]; }
+  for (int d = 0; d < D; ++d) O[d] = 0.0;
+  for (int t = 0; t < nkeys; ++t) {
+    size_t vb = ((size_t)keys[t] * J->Hkv + g) * D;
+    double w = s[t] / l;
+    for (int d = 0; d < D; ++d) O[d] += w * (load_elem(J->V, J->fmt, vb + d) * J->v_descale);
+  }
+  J->LSE[(size_t)row * J->Hq + h] = m + log(l);
+}
+
+static void* attn_worker(void* arg) {
+  attn_job* J = (attn_job*)arg;
+  int maxkeys = J->topK * J->block;
+  double* q = (double*)malloc(sizeof(double) * J->D);
+  double* s = (double*)malloc(sizeof(double) * maxkeys);
+  int* keys = (int*)malloc(sizeof(int) * maxkeys);
+  for (;;) {
+    pthread_mutex_lock(&J->mu);
+    int row = J->next++;
+    pthread_mutex_unlock(&J->mu);
+    if (row >= J->nq) break;
+    for (int h = 0; h < J->Hq; ++h) attn_one(J, row, h, q, s, keys);
+  }
+  free(q); free(s); free(keys);
+  return NULL;
+}
+
+/* Forward attention for the queries listed in qids (all N when qids == NULL).
+ * Layouts: Q [N,Hq,D], K and V [Lkv,Hkv,D], indices [N,Hkv,topK] int32.
+ * Outputs: O [nq,Hq,D] double, LSE [nq,Hq] double.
+ * Returns 0, 1 if an invalid block id was seen, or -1 on bad arguments. */
+int oracle_attn_fwd(const void* Q, const void* K, const void* V, int fmt,
+                    const int32_t* indices, int N, int Lkv, int Hq, int Hkv, int D,
+                    int topK, int block, double scale, double q_descale,
+                    double k_descale, double v_descale, const int32_t* qids, int nq,
+                    double* O, double* LSE, int nthreads) {
+  if (!Q || !K || !V || !indices || !O || !LSE) return -1;
+  if (N < 0 || Lkv <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || topK <= 0 || block <= 0) return -1;
+  if (Hq % Hkv != 0 || Lkv % block != 0 || N > Lkv) return -1;
+  int32_t* all = NULL;
+  if (!qids) {
+    all = (int32_t*)malloc(sizeof(int32_t) * (N > 0 ? N : 1));
+    for (int i = 0; i < N; ++i) all[i] = i;
+    qids = all;
+    nq = N;
+  }
+  for (int r = 0; r < nq; ++r)
+    if (qids[r] < 0 || qids[r] >= N) { free(all); return -1; }
+  attn_job J;
+  memset(&J, 0, sizeof J);
+  J.Q = Q; J.K = K; J.V = V; J.fmt = fmt; J.indices = indices;
+  J.N = N; J.Lkv = Lkv; J.Hq = Hq; J.Hkv = Hkv; J.D = D; J.topK = topK; J.block = block;
+  J.scale = scale; J.q_descale = q_descale; J.k_descale = k_descale; J.v_descale = v_descale;
+  J.qids = qids; J.nq = nq; J.O = O; J.LSE = LSE;
+  pthread_mutex_init(&J.mu, NULL);
+  if (nthreads < 1) nthreads = 1;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
+  for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, attn_worker, &J);
+  for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+  free(th);
+  pthread_mutex_destroy(&J.mu);
+  free(all);
+  return J.bad ? 1 : 0;
+}
+
+/* Reverse index ("Sparse Attention", Chapter 5): for every row r = g*nblocks + b,
+ * the queries i (ascending) whose group-g list contains b with b <= lb(i), and the
+ * slot k of the first occurrence of b in that list.  Also the combine map
+ * cmap[i,g,k] = CSR position of the entry made from list slot k, or -1.
+ *
+ * counts[R], offsets[R+1], qlist[E], slot[E], cmap[N*Hkv*topK]; R = Hkv*nblocks.
+ * *E_out = number of entries, *nsb_out = rows with at least one entry.
+ * qlist and slot must hold N*Hkv*topK entries.  Returns 0, 1 on invalid ids. */
+int oracle_schedule(const int32_t* indices, int N, int Lkv, int Hkv, int topK, int block,
+                    int32_t* counts, int32_t* offsets, int32_t* qlist, int32_t* slot,
+                    int32_t* cmap, int64_t* E_out, int32_t* nsb_out) {
+  const int nblocks = Lkv / block;
+  const int R = Hkv * nblocks;
+  int bad = 0;
+  /* pass 1: which list slots are entries */
+  size_t L = (size_t)N * Hkv * topK;
+  for (size_t t = 0; t < L; ++t) cmap[t] = -1;
+  for (int r = 0; r < R; ++r) counts[r] = 0;
+  for (int i = 0; i < N; ++i) {
+    long lb = ((long)Lkv - N + i) / block;
+    for (int g = 0; g < Hkv; ++g) {
+      const int32_t* lst = indices + ((size_t)i * Hkv + g) * topK;
+      for (int k = 0; k < topK; ++k) {
+        int b = lst[k];
+        if (b < -1 || b >= nblocks) { bad = 1; continue; }
+        if (b == -1 || b > lb) continue;
+        int dup = 0;
+        for (int k2 = 0; k2 < k; ++k2) if (lst[k2] == b) { dup = 1; break; }
+        if (dup) continue;
+        counts[g * nblocks + b] += 1;
+        cmap[((size_t)i * Hkv + g) * topK + k] = 0; /* marked; position filled below */
+      }
+    }
+  }
+  offsets[0] = 0;
+  int32_t nsb = 0;
+  for (int r = 0; r < R; ++r) {
+    offsets[r + 1] = offsets[r] + counts[r];
+    if (counts[r] > 0) ++nsb;
+  }
+  /* pass 2: fill each row in ascending query order */
+  int32_t* fill = (int32_t*)calloc((size_t)R, sizeof(int32_t));
+  for (int i = 0; i < N; ++i)
+    for (int g = 0; g < Hkv; ++g)
+      for (int k = 0; k < topK; ++k) {
+        size_t t = ((size_t)i * Hkv + g) * topK + k;
+        if (cmap[t] < 0) continue;
+        int b = indices[t];
+        int r = g * nblocks + b;
+        int p = offsets[r] + fill[r]++;
+        qlist[p] = i;
+        slot[p] = k;
+        cmap[t] = p;
+      }
+  free(fill);
+  *E_out = offsets[R];
+  *nsb_out = nsb;
+  return bad;
+}
+
+/* Work list: each row's entries cut, in order, into tiles of at most tile_rows
+ * entries; tiles listed in row order.  tiles[3*t] = row, [3*t+1] = first CSR
+ * position, [3*t+2] = count.  Returns the number of tiles (or -1 if cap is too
+ * small).  Builder-defined split rule: parity unpinned by the pages. */
+long oracle_worklist(const int32_t* counts, const int32_t* offsets, int R, int tile_rows,
+                     int32_t* tiles, long cap) {
+  long T = 0;
+  for (int r = 0; r < R; ++r)
+    for (int f = 0; f < counts[r]; f += tile_rows) {
+      if (T >= cap) return -1;
+      tiles[3 * T] = r;
+      tiles[3 * T + 1] = offsets[r] + f;
+      tiles[3 * T + 2] = counts[r] - f < tile_rows ? counts[r] - f : tile_rows;
+      ++T;
+    }
+  return T;
+}
+
+/* Log-sum-exp merge of n partial results of one (query, head) ("Sparse Attention",
+ * Chapter 5, "Partial outputs and Combine"): part k holds O_k (its own softmax-
+ * normalised output over a disjoint key subset) and lse_k.  The merged LSE is
+ * log sum_k exp(lse_k) and O = sum_k exp(lse_k - LSE) O_k. */
+void oracle_lse_merge(int n, int D, const double* O_parts, const double* lse_parts,
+                      double* O_out, double* lse_out) {
+  double M = -INFINITY;
+  for (int k = 0; k < n; ++k) if (lse_parts[k] > M) M = lse_parts[k];
+  for (int d = 0; d < D; ++d) O_out[d] = 0.0;
+  if (M == -INFINITY) { *lse_out = -INFINITY; return; }
+  double S = 0.0;
+  for (int k = 0; k < n; ++k) S += exp(lse_parts[k] - M);
+  double LSE = M + log(S);
+  for (int k = 0; k < n; ++k) {
+    double w = exp(lse_parts[k] - LSE);
+    for (int d = 0; d < D; ++d) O_out[d] += w * O_parts[(size_t)k * D + d];
+  }
+  *lse_out = LSE;
+}
+
+/* Crossover ("Kernel optimization for MiniMax M3", Q-outer vs KV-outer section):
+ * KV-outer when nsb / N < 2.85, i.e. 100*nsb < 285*N in exact integers.
+ * Returns 1 for KV-outer, 2 for Q-outer. */
+int oracle_dispatch(int32_t nsb, int N) {
+  return ((int64_t)nsb * 100 < (int64_t)N * 285) ? 1 : 2;
+}

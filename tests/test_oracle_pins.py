@@ -1,0 +1,341 @@
+"""Pins for the oracle: each checks it against something other than itself.
+
+Sources: "Sparse Attention" (dinara-dl) Ch. 1 (softmax over the union of selected
+blocks), Ch. 2 (worked example [2, 5, 8]), Ch. 5 (reverse index; LSE-weighted
+combine); "Flash-MSA" (local block always attended, causally); "Kernel optimization
+for MiniMax M3" (block 128, GQA groups, crossover nsb/N < 2.85).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rnd(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+def dense_causal(Q, K, V, Lkv, scale):
+    """Textbook causal GQA attention as full matrices (bottom-right aligned)."""
+    N, Hq, D = Q.shape
+    Hkv = K.shape[1]
+    G = Hq // Hkv
+    Kx = np.repeat(K, G, axis=1)
+    Vx = np.repeat(V, G, axis=1)
+    S = np.einsum("nhd,jhd->hnj", Q, Kx) * scale
+    pos = Lkv - N + np.arange(N)
+    mask = np.arange(Lkv)[None, :] <= pos[:, None]
+    S = np.where(mask[None], S, -np.inf)
+    m = S.max(-1, keepdims=True)
+    P = np.exp(S - m)
+    l = P.sum(-1, keepdims=True)
+    O = np.einsum("hnj,jhd->nhd", P / l, Vx)
+    return O, (m + np.log(l))[..., 0].T
+
+
+def masked_bruteforce(Q, K, V, indices, Lkv, block, scale):
+    """Dense 0/1 mask built from the lists with Python sets, then a masked softmax."""
+    N, Hq, D = Q.shape
+    Hkv = K.shape[1]
+    G = Hq // Hkv
+    nb = Lkv // block
+    O = np.zeros((N, Hq, D))
+    LSE = np.full((N, Hq), -np.inf)
+    for i in range(N):
+        pos = Lkv - N + i
+        for h in range(Hq):
+            g = h // G
+            chosen = {int(b) for b in indices[i, g] if 0 <= b < nb}
+            keys = [j for j in range(Lkv) if (j // block) in chosen and j <= pos]
+            if not keys:
+                continue
+            s = np.array([scale * float(Q[i, h] @ K[j, g]) for j in keys])
+            w = np.exp(s - s.max())
+            O[i, h] = (w / w.sum()) @ V[keys, g]
+            LSE[i, h] = s.max() + math.log(w.sum())
+    return O, LSE
+
+
+def full_lists(N, Lkv, Hkv, block, topK=None):
+    """Lists lb(i), lb(i)-1, ..., 0 (local block first), cut to topK and -1 padded."""
+    nb = Lkv // block
+    topK = topK or nb
+    idx = np.full((N, Hkv, topK), -1, np.int32)
+    for i in range(N):
+        lb = (Lkv - N + i) // block
+        n = min(lb + 1, topK)
+        for g in range(Hkv):
+            idx[i, g, :n] = np.arange(lb + 1)[::-1][:n]
+    return idx
+
+
+@pytest.mark.parametrize("N,Lkv", [(256, 256), (96, 256)])
+def test_dense_equivalence(N, Lkv):
+    """Lists holding every block 0..lb(i) reduce to dense causal GQA attention."""
+    rng = np.random.default_rng(1)
+    Hq, Hkv, D, block = 4, 2, 16, 32
+    Q, K, V = rnd(rng, N, Hq, D), rnd(rng, Lkv, Hkv, D), rnd(rng, Lkv, Hkv, D)
+    scale = 1 / math.sqrt(D)
+    idx = full_lists(N, Lkv, Hkv, block)
+    O, LSE, st = oracle.attn_fwd(Q, K, V, idx, Lkv=Lkv, block=block, scale=scale)
+    Od, LSEd = dense_causal(Q, K, V, Lkv, scale)
+    assert st == 0
+    np.testing.assert_allclose(O, Od, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(LSE, LSEd, rtol=0, atol=1e-12)
+
+
+def test_topk1_local_block_only():
+    """topK = 1: an explicit causal softmax over keys 128*lb(i) .. pos(i)."""
+    rng = np.random.default_rng(2)
+    N = Lkv = 256
+    Hq, Hkv, D, block = 2, 1, 8, 128
+    Q, K, V = rnd(rng, N, Hq, D), rnd(rng, Lkv, Hkv, D), rnd(rng, Lkv, Hkv, D)
+    scale = 0.37
+    idx = np.array([[[i // block]] for i in range(N)], np.int32)
+    O, LSE, _ = oracle.attn_fwd(Q, K, V, idx, Lkv=Lkv, block=block, scale=scale)
+    for i in [0, 1, 77, 127, 128, 129, 200, 255]:
+        for h in range(Hq):
+            lo = 128 * (i // 128)
+            s = np.array([scale * np.dot(Q[i, h], K[j, 0]) for j in range(lo, i + 1)])
+            e = np.exp(s - s.max())
+            ref = sum(e[t] * V[lo + t, 0] for t in range(len(e))) / e.sum()
+            assert np.max(np.abs(O[i, h] - ref)) < 1e-12
+            assert abs(LSE[i, h] - (s.max() + math.log(e.sum()))) < 1e-12
+
+
+def test_bruteforce_random_lists():
+    """Random lists with pads, duplicates and future blocks vs a set-built dense mask."""
+    rng = np.random.default_rng(3)
+    N, Lkv, Hq, Hkv, D, block, topK = 40, 64, 6, 3, 8, 8, 5
+    nb = Lkv // block
+    Q, K, V = rnd(rng, N, Hq, D), rnd(rng, Lkv, Hkv, D), rnd(rng, Lkv, Hkv, D)
+    idx = rng.integers(-1, nb, size=(N, Hkv, topK)).astype(np.int32)
+    scale = 0.25
+    O, LSE, st = oracle.attn_fwd(Q, K, V, idx, Lkv=Lkv, block=block, scale=scale)
+    Ob, LSEb = masked_bruteforce(Q, K, V, idx, Lkv, block, scale)
+    assert st == 0
+    np.testing.assert_allclose(O, Ob, atol=1e-12)
+    np.testing.assert_array_equal(np.isinf(LSE), np.isinf(LSEb))
+    fin = np.isfinite(LSEb)
+    np.testing.assert_allclose(LSE[fin], LSEb[fin], atol=1e-12)
+    assert np.all(O[~fin] == 0.0)
+
+
+def test_order_duplicate_pad_invariance():
+    """Shuffling lists, appending duplicates and -1 pads changes neither O/LSE nor the CSR."""
+    rng = np.random.default_rng(4)
+    N = Lkv = 512
+    Hq, Hkv, D, block, topK = 4, 2, 16, 64, 4
+    Q, K, V = rnd(rng, N, Hq, D), rnd(rng, Lkv, Hkv, D), rnd(rng, Lkv, Hkv, D)
+    idx = np.full((N, Hkv, topK), -1, np.int32)
+    for i in range(N):
+        lb = i // block
+        for g in range(Hkv):
+            picks = rng.permutation(lb)[: topK - 1] if lb else []
+            idx[i, g, 0] = lb
+            idx[i, g, 1 : 1 + len(picks)] = picks
+    shuf = idx.copy()
+    for i in range(N):
+        for g in range(Hkv):
+            rng.shuffle(shuf[i, g])
+    extra = np.concatenate([shuf, shuf[:, :, :2], np.full((N, Hkv, 3), -1, np.int32)], axis=2)
+    O1, L1, _ = oracle.attn_fwd(Q, K, V, idx, Lkv=Lkv, block=block, scale=0.3)
+    O2, L2, _ = oracle.attn_fwd(Q, K, V, extra, Lkv=Lkv, block=block, scale=0.3)
+    np.testing.assert_allclose(O1, O2, atol=1e-13)
+    np.testing.assert_allclose(L1, L2, atol=1e-13)
+    s1 = oracle.schedule(idx, Lkv=Lkv, block=block)
+    s2 = oracle.schedule(extra, Lkv=Lkv, block=block)
+    for k in ("counts", "offsets", "qlist"):
+        np.testing.assert_array_equal(s1[k], s2[k])
+    assert s1["nsb"] == s2["nsb"] and s1["E"] == s2["E"]
+
+
+def test_closed_forms():
+    rng = np.random.default_rng(5)
+    N = Lkv = 384
+    Hq, Hkv, D, block = 4, 2, 8, 128
+    idx = full_lists(N, Lkv, Hkv, block, topK=3)
+    K = rnd(rng, Lkv, Hkv, D)
+    # V constant -> O equals the constant
+    c = 1.75
+    Q = rnd(rng, N, Hq, D)
+    O, _, _ = oracle.attn_fwd(Q, K, np.full((Lkv, Hkv, D), c), idx, Lkv=Lkv, block=block, scale=0.5)
+    assert np.max(np.abs(O - c)) < 1e-14
+    # Q zero -> O is the mean of the visible V rows, LSE = log |J| = log(pos + 1)
+    V = rnd(rng, Lkv, Hkv, D)
+    O, LSE, _ = oracle.attn_fwd(np.zeros((N, Hq, D)), K, V, idx, Lkv=Lkv, block=block, scale=0.5)
+    G = Hq // Hkv
+    for i in [0, 5, 130, 383]:
+        for h in range(Hq):
+            ref = V[: i + 1, h // G].mean(axis=0)
+            assert np.max(np.abs(O[i, h] - ref)) < 1e-13
+            assert abs(LSE[i, h] - math.log(i + 1)) < 1e-13
+    # query at pos = 128 b with only its local block: O = V[pos], LSE = scale * q.k[pos]
+    only_local = np.array([[[i // block] + [-1] * 2] * Hkv for i in range(N)], np.int32)
+    O, LSE, _ = oracle.attn_fwd(Q, K, V, only_local, Lkv=Lkv, block=block, scale=0.5)
+    for i in (0, 128, 256):
+        for h in range(Hq):
+            g = h // G
+            assert np.array_equal(O[i, h], V[i, g])
+            assert abs(LSE[i, h] - 0.5 * float(Q[i, h] @ K[i, g])) < 1e-13
+
+
+def test_merge_identity():
+    """Per-part softmax results merged by LSE weighting equal the whole (P3 Ch. 5 combine)."""
+    rng = np.random.default_rng(6)
+    N = Lkv = 512
+    Hq, Hkv, D, block = 2, 1, 16, 64
+    Q, K, V = rnd(rng, N, Hq, D) * 3, rnd(rng, Lkv, Hkv, D), rnd(rng, Lkv, Hkv, D)
+    i = 450  # lb = 7
+    whole = np.full((N, 1, 8), -1, np.int32)
+    whole[i, 0] = [7, 0, 3, 5, 1, 6, 2, 4]
+    Ow, Lw, _ = oracle.attn_fwd(Q, K, V, whole, Lkv=Lkv, block=block, scale=0.4, qids=[i])
+    parts = [[7, 3], [0], [5, 1, 6], [2, 4]]
+    Op, Lp = [], []
+    for p in parts:
+        lst = np.full((N, 1, 8), -1, np.int32)
+        lst[i, 0, : len(p)] = p
+        o, l, _ = oracle.attn_fwd(Q, K, V, lst, Lkv=Lkv, block=block, scale=0.4, qids=[i])
+        Op.append(o[0]); Lp.append(l[0])
+    for h in range(Hq):
+        O, L = oracle.lse_merge(np.stack([o[h] for o in Op]), np.array([l[h] for l in Lp]))
+        assert np.max(np.abs(O - Ow[0, h])) < 1e-12
+        assert abs(L - Lw[0, h]) < 1e-12
+    # a plain average is not the merge
+    avg = np.mean([o[0] for o in Op], axis=0)
+    assert np.max(np.abs(avg - Ow[0, 0])) > 1e-3
+
+
+def test_worked_example_reverse_index():
+    with open(os.path.join(GOLDEN, "worked_example_reverse_index.json")) as f:
+        ex = json.load(f)
+    N, Hkv, topK = ex["N"], ex["Hkv"], ex["topK"]
+    idx = np.full((N, Hkv, topK), -1, np.int32)
+    idx[ex["query"], 0] = ex["list"]
+    s = oracle.schedule(idx, Lkv=ex["Lkv"], block=ex["block"])
+    nonempty = [r for r in range(len(s["counts"])) if s["counts"][r] > 0]
+    assert nonempty == ex["expected_rows"]
+    for r, k in zip(ex["expected_rows"], ex["expected_slots"]):
+        p = s["offsets"][r]
+        assert s["qlist"][p] == ex["query"] and s["slot"][p] == k
+        assert s["cmap"][ex["query"], 0, k] == p
+    assert s["E"] == 3 and s["nsb"] == 3
+
+
+def brute_schedule(idx, Lkv, block):
+    N, Hkv, topK = idx.shape
+    nb = Lkv // block
+    rows = []
+    for g in range(Hkv):
+        for b in range(nb):
+            ent = []
+            for i in range(N):
+                lb = (Lkv - N + i) // block
+                lst = [int(x) for x in idx[i, g]]
+                if b <= lb and b in lst:
+                    ent.append((i, lst.index(b)))
+            rows.append(ent)
+    return rows
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_schedule_bruteforce_and_invariants(seed):
+    rng = np.random.default_rng(10 + seed)
+    N, Lkv, Hkv, topK, block = 50, 80, 2, 6, 8
+    nb = Lkv // block
+    idx = rng.integers(-1, nb, size=(N, Hkv, topK)).astype(np.int32)
+    s = oracle.schedule(idx, Lkv=Lkv, block=block)
+    rows = brute_schedule(idx, Lkv, block)
+    assert [len(r) for r in rows] == list(s["counts"])
+    for r, ent in enumerate(rows):
+        a, b = s["offsets"][r], s["offsets"][r + 1]
+        assert list(zip(s["qlist"][a:b], s["slot"][a:b])) == ent
+    E = s["E"]
+    assert s["counts"].sum() == E == s["offsets"][-1]
+    assert s["nsb"] == int((s["counts"] > 0).sum())
+    cm = s["cmap"].reshape(-1)
+    valid = cm[cm >= 0]
+    assert sorted(valid.tolist()) == list(range(E))  # bijection onto [0, E)
+    assert (s["cmap"] >= 0).sum(axis=2).max() <= topK
+    for p in range(E):  # cmap inverts (qlist, slot)
+        i, k = s["qlist"][p], s["slot"][p]
+        r = np.searchsorted(s["offsets"], p, side="right") - 1
+        g = r // nb
+        assert s["cmap"][i, g, k] == p
+    assert s["status"] == 0
+
+
+def test_schedule_invalid_ids_flagged():
+    idx = np.array([[[0, 9, -2]]], np.int32)  # nblocks = 2
+    s = oracle.schedule(idx, Lkv=16, block=8)
+    assert s["status"] == 1 and s["E"] == 1
+
+
+def test_worklist_covers_rows():
+    counts = np.array([0, 3, 17, 8, 1], np.int32)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    t = oracle.worklist(counts, offsets, 8)
+    assert t.tolist() == [[1, 0, 3], [2, 3, 8], [2, 11, 8], [2, 19, 1], [3, 20, 8], [4, 28, 1]]
+
+
+def test_dispatch_threshold():
+    assert oracle.dispatch(56, 20) == 1 and oracle.dispatch(57, 20) == 2  # 57/20 = 2.85 exactly
+    assert oracle.dispatch(256, 8192) == 1 and oracle.dispatch(9980, 256) == 2
+
+
+def test_e4m3_decoder_matches_library_cast():
+    """The spec-written E4M3 decoder agrees with torch's float8_e4m3fn on all 256 codes."""
+    b = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    lib = b.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = np.array([oracle.e4m3_decode(i) for i in range(256)])
+    nan = np.isnan(lib)
+    assert np.array_equal(nan, np.isnan(ours)) and nan.sum() == 2
+    assert np.array_equal(lib[~nan], ours[~nan])
+    assert oracle.e4m3_decode(0x7E) == 448.0 and oracle.e4m3_decode(0x01) == 2.0 ** -9
+
+
+def test_bf16_decoder_matches_library_cast():
+    rng = np.random.default_rng(7)
+    x = torch.from_numpy(rng.standard_normal(1000).astype(np.float32)).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    assert all(oracle.bf16_decode(int(u)) == float(v) for u, v in zip(bits, x.to(torch.float64)))
+
+
+def test_fp8_path_equals_decoded_f64():
+    """e4m3 bytes + descales give the same result as their decoded values in float64."""
+    rng = np.random.default_rng(8)
+    N = Lkv = 256
+    Hq, Hkv, D, block = 4, 2, 16, 64
+    qb = torch.from_numpy(rng.standard_normal((N, Hq, D)).astype(np.float32)).to(torch.float8_e4m3fn)
+    kb = torch.from_numpy(rng.standard_normal((Lkv, Hkv, D)).astype(np.float32)).to(torch.float8_e4m3fn)
+    vb = torch.from_numpy(rng.standard_normal((Lkv, Hkv, D)).astype(np.float32)).to(torch.float8_e4m3fn)
+    idx = full_lists(N, Lkv, Hkv, block, topK=3)
+    dq, dk, dv = 0.5, 0.25, 2.0
+    O8, L8, _ = oracle.attn_fwd(qb.view(torch.uint8).numpy(), kb.view(torch.uint8).numpy(),
+                                vb.view(torch.uint8).numpy(), idx, Lkv=Lkv, block=block,
+                                scale=0.3, q_descale=dq, k_descale=dk, v_descale=dv)
+    Qf, Kf, Vf = (t.to(torch.float64).numpy() for t in (qb, kb, vb))
+    O, L, _ = oracle.attn_fwd(Qf * dq, Kf * dk, Vf * dv, idx, Lkv=Lkv, block=block, scale=0.3)
+    np.testing.assert_allclose(O8, O, atol=1e-12)
+    np.testing.assert_allclose(L8, L, atol=1e-12)
+
+
+def test_bf16_path_equals_decoded_f64():
+    rng = np.random.default_rng(9)
+    N = Lkv = 256
+    Hq, Hkv, D, block = 4, 1, 16, 64
+    ts = [torch.from_numpy(rng.standard_normal(s).astype(np.float32)).to(torch.bfloat16)
+          for s in ((N, Hq, D), (Lkv, Hkv, D), (Lkv, Hkv, D))]
+    bits = [t.view(torch.int16).numpy().view(np.uint16) for t in ts]
+    idx = full_lists(N, Lkv, Hkv, block, topK=2)
+    Ob, Lb, _ = oracle.attn_fwd(*bits, idx, Lkv=Lkv, block=block, scale=0.3)
+    O, L, _ = oracle.attn_fwd(*(t.to(torch.float64).numpy() for t in ts), idx, Lkv=Lkv,
+                              block=block, scale=0.3)
+    assert np.array_equal(Ob, O) and np.array_equal(Lb, L)
