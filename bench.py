@@ -1,0 +1,377 @@
+#!/usr/bin/env python3
+"""Benchmark: block-sparse GQA attention forward (schedule + attention + combine).
+
+One step = one pass of the whole forward over one batch of synthetic input: the
+reverse index and work list (msa_build_schedule) and the attention with its combine
+(msa_sparse_attn_fwd), on the MiniMax M3 shape (N = Lkv = 8192, Hq 64, Hkv 4,
+D 128, block 128, topK 16) by default.  Inputs are resident in HBM when the timed
+region starts; L2 is flushed (a 256 MiB write) before every timed step, outside the
+step's events.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the oracle (plain fp64 C on the host cores) on a bounded
+sample of the same workload: the pages ship no code, so the oracle is the only
+reference implementation there is.  Under torchrun (N > 1) every rank runs its own
+independent M3 problem (weak scaling, no collective on the data path); rank 0
+prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn fwd useful TFLOP/s and % HBM roofline, M3 shape top16, 1 GB300"
+KERNELS_PER_STEP = 11  # mark, rowscan, scan_rows, seg_reduce, seg_top, seg_down, scatter, tiles, kv_outer, combine, q_outer
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="m3", choices=["tiny", "m3", "long", "lowreuse"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("attn_kv_outer.cu", "ptx.cuh", "msa_internal.h"):
+        with open(os.path.join(ROOT, "block_sparse_gqa_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """dram read+write bytes per launch of the KV-outer kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", f"kv_outer_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_hash:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != kernel_source_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def max_over_ranks(pg, value, device):
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def time_oracle(wl, seconds, seed=0):
+    """Run the oracle on a seeded query sample sized for ~`seconds` of CPU time.
+    Returns (TFLOP/s of useful work, sample description, threads)."""
+    import numpy as np
+    import oracle
+    import workloads
+    cfg = wl.cfg
+    threads = os.cpu_count() or 1
+    Qn, Kn, Vn = wl.np_inputs()
+    idx = wl.indices.numpy()
+    rng = np.random.default_rng(seed)
+
+    def run(nq):
+        qids = np.sort(rng.choice(cfg.N, size=nq, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.attn_fwd(Qn, Kn, Vn, idx, Lkv=cfg.Lkv, scale=cfg.scale, q_descale=wl.q_descale,
+                        k_descale=wl.k_descale, v_descale=wl.v_descale, qids=qids, nthreads=threads)
+        return time.perf_counter() - t0
+
+    probe_n = min(16, cfg.N)
+    tp = run(probe_n)
+    nq = int(min(cfg.N, max(probe_n, probe_n * seconds / max(tp, 1e-6))))
+    t = run(nq)
+    flops = 4.0 * nq * cfg.Hq * cfg.topK * 128 * cfg.D
+    sample = f"{nq} of {cfg.N} queries (seeded uniform sample), all {cfg.Hq} heads, {cfg.name} lists"
+    return flops / t / 1e12, sample, threads, t
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, world, rank):
+    import workloads
+    if rank != 0:
+        return
+    wl = workloads.make_workload(args.workload)
+    cfg = wl.cfg
+    per_step = max(1.0, min(6.0, 150.0 / max(args.steps + args.warmup, 1)))
+    vals, times = [], []
+    for k in range(args.warmup + args.steps):
+        v, sample, threads, t = time_oracle(wl, per_step, seed=k)
+        if k >= args.warmup:
+            vals.append(v)
+            times.append(t)
+    value = statistics.median(vals)
+    ms = 1e3 * cfg.nominal_flops() / (value * 1e12)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: N={cfg.N} Lkv={cfg.Lkv} Hq={cfg.Hq} Hkv={cfg.Hkv} D={cfg.D} "
+                               f"block=128 topK={cfg.topK}", "reference": "oracle (plain fp64 C, host cores)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample + "; ms_per_step extrapolates the full workload"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local, pg):
+    import torch
+
+    import block_sparse_gqa_gb300 as msa
+    import workloads
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --impl ours needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = workloads.CONFIGS[args.workload]
+    wl = workloads.make_workload(cfg, seed=cfg.seed + 1000 * rank)
+    stream = torch.cuda.current_stream()
+
+    idx_d = wl.indices.to(dev)
+    Q, K, V = (t.to(dev) for t in (wl.Q, wl.K, wl.V))
+    O = torch.empty((cfg.N, cfg.Hq, cfg.D), dtype=torch.bfloat16, device=dev)
+    LSE = torch.empty((cfg.N, cfg.Hq), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    sched = msa.build_schedule(idx_d, cfg.nblocks)
+
+    def new_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)  # materialise the CUDA event handle
+        return evs
+
+    def step(stage):
+        msa.build_schedule(idx_d, cfg.nblocks, schedule=sched)
+        msa.sparse_attn_fwd(Q, K, V, sched, scale=cfg.scale, O=O, LSE=LSE,
+                            stage_events=[e.cuda_event for e in stage] if stage else None)
+
+    for _ in range(args.warmup):
+        step(None)
+    torch.cuda.synchronize()
+    info = sched.query()
+    assert info["status"] == 0, info
+    if info["path"] != 1:
+        raise SystemExit(f"workload {cfg.name} dispatches to the Q-outer path; the roofline below is for KV-outer")
+
+    starts, ends = new_events(args.steps), new_events(args.steps)
+    stages = [new_events(3) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier(pg)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    for k in range(args.steps):
+        flush.zero_()
+        starts[k].record(stream)
+        step(stages[k])
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    clock_info = clocks.stop()
+
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    attn_ms = [st[0].elapsed_time(st[1]) for st in stages]
+    comb_ms = [st[1].elapsed_time(st[2]) for st in stages]
+    sched_ms = [s.elapsed_time(st[0]) for s, st in zip(starts, stages)]
+    total_ms = max_over_ranks(pg, sum(step_ms), dev)
+    ms_per_step = total_ms / args.steps
+    value = world * cfg.nominal_flops() / (ms_per_step * 1e-3) / 1e12
+
+    # algorithmic bytes ("Roofline"): attention kernel and whole step
+    E, nsb, T = info["entries"], info["nsb"], info["ntiles"]
+    G, D = cfg.G, cfg.D
+    q_bytes = cfg.N * cfg.Hq * D * 2
+    kv_bytes = nsb * 2 * 128 * D * 2
+    part_bytes = E * G * (2 * D + 4)
+    meta_attn = E * 4 + T * 16
+    attn_bytes = q_bytes + kv_bytes + part_bytes + meta_attn
+    comb_bytes = part_bytes + cfg.N * cfg.Hkv * cfg.topK * 4 + cfg.N * cfg.Hq * (2 * D + 4)
+    step_bytes = attn_bytes + comb_bytes + cfg.N * cfg.Hkv * cfg.topK * 4 * 3
+    peak, peak_kind = load_peaks()
+    attn_mean = statistics.mean(attn_ms)
+    achieved = attn_bytes / (attn_mean * 1e-3) / 1e9
+    traffic = recorded_traffic(cfg.name)
+
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.pin_memory()
+        hQ, hK, hV, hI = (pin(t) for t in (wl.Q, wl.K, wl.V, wl.indices))
+        hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+        hL = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
+        dQ, dK, dV, dI = (torch.empty_like(t, device=dev) for t in (wl.Q, wl.K, wl.V, wl.indices))
+        dO, dL = torch.empty_like(O), torch.empty_like(LSE)
+        e_sched = None
+
+        def e2e_step():
+            nonlocal e_sched
+            dQ.copy_(hQ, non_blocking=True); dK.copy_(hK, non_blocking=True)
+            dV.copy_(hV, non_blocking=True); dI.copy_(hI, non_blocking=True)
+            e_sched = msa.build_schedule(dI, cfg.nblocks, schedule=e_sched)
+            msa.sparse_attn_fwd(dQ, dK, dV, e_sched, scale=cfg.scale, O=dO, LSE=dL)
+            hO.copy_(dO, non_blocking=True); hL.copy_(dL, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        es, ee = new_events(args.steps), new_events(args.steps)
+        barrier(pg)
+        for k in range(args.steps):
+            flush.zero_()
+            es[k].record(stream)
+            e2e_step()
+            ee[k].record(stream)
+        torch.cuda.synchronize()
+        e_total = max_over_ranks(pg, sum(s.elapsed_time(e) for s, e in zip(es, ee)), dev)
+        e_ms = e_total / args.steps
+        h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV, hI))
+        d2h = hO.numel() * hO.element_size() + hL.numel() * hL.element_size()
+        e2e = {"value": world * cfg.nominal_flops() / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        e_sched.close()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample, threads, _ = time_oracle(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample}
+
+    sched.close()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/K/V, uniform block picks)",
+        "config": {"workload": f"{cfg.name}: N={cfg.N} Lkv={cfg.Lkv} Hq={cfg.Hq} Hkv={cfg.Hkv} D={cfg.D} block=128 "
+                               f"topK={cfg.topK}, causal, own block + {cfg.topK - 1} uniform earlier blocks",
+                   "l2": "flushed (256 MiB write) before every timed step, outside the step events",
+                   "parallelism": f"independent problem per GPU x{world}", "path": "kv_outer",
+                   "entries": E, "nsb": nsb, "tiles": T},
+        "roofline": {"kernel": "kv_outer_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes": attn_bytes, "peak_source": f"{peak_kind} MEASURED_PEAKS.json hbm_gbs"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s", "launch_ms": attn_mean},
+        "path_roofline": {"bytes_per_step": step_bytes, "achieved_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+                          "frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak},
+        "stage_ms": {"schedule": statistics.mean(sched_ms), "attention": attn_mean,
+                     "combine": statistics.mean(comb_ms)},
+        "selected_pair_tflops": world * 4.0 * 128 * D * G * E / (ms_per_step * 1e-3) / 1e12,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clock_info,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        # rank 0 alone times the oracle; other ranks exit without work or collectives
+        rank = int(os.environ.get("RANK", "0"))
+        if rank == 0:
+            run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), rank)
+        return
+    world, rank, local, pg = dist_setup(args)
+    run_ours(args, world, rank, local, pg)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,295 @@
+// C ABI of libmsa (declared in include/msa.h): argument checks, workspace
+// ownership, tensor-map encoding and the launch sequence.  No call here
+// synchronises the host except msa_schedule_query / msa_schedule_export /
+// msa_schedule_destroy, and nothing aborts, traps or prints.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "msa_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+
+msa_status_t from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return MSA_OK;
+  g_last_cuda = static_cast<int>(e);
+  cudaGetLastError();  // clear a sticky-free error so the next call starts clean
+  return e == cudaErrorMemoryAllocation ? MSA_ERR_OOM : MSA_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Carves the schedule's device arrays out of one allocation.
+struct Carver {
+  size_t off = 0;
+  char* base = nullptr;
+  template <class T>
+  T* take(size_t count) {
+    const size_t o = off;
+    off = align_up(off + count * sizeof(T), 256);
+    return base ? reinterpret_cast<T*>(base + o) : nullptr;
+  }
+};
+
+void carve(msa_schedule* s, char* base) {
+  Carver c;
+  c.base = base;
+  msa::SchedDev& d = s->d;
+  d.mask = c.take<uint32_t>(static_cast<size_t>(s->R) * s->C);
+  d.rowbase = c.take<int32_t>(static_cast<size_t>(s->R) * (s->C + 1));
+  d.counts = c.take<int32_t>(s->R);
+  d.offsets = c.take<int32_t>(static_cast<size_t>(s->R) + 1);
+  d.qlist = c.take<int32_t>(s->cap_entries);
+  d.slot = c.take<int32_t>(s->cap_entries);
+  d.cmap = c.take<int32_t>(s->cap_entries);
+  d.blist = c.take<int32_t>(s->cap_entries);
+  d.tiles = c.take<int4>(s->cap_tiles);
+  d.window_tiles = c.take<int32_t>(static_cast<size_t>(s->nW) + 1);
+  d.segoff = c.take<int32_t>(static_cast<size_t>(s->nseg) + 1);
+  d.seg_sums = c.take<int32_t>(static_cast<size_t>(s->nseg_blocks) + 1);
+  d.hdr = c.take<msa::SchedHeader>(1);
+  s->dev_bytes = c.off;
+}
+
+msa_status_t schedule_create(int N, int Hkv, int topK, int nblocks, msa_schedule** out) {
+  msa_schedule* s = new (std::nothrow) msa_schedule();
+  if (!s) return MSA_ERR_OOM;
+  std::memset(s, 0, sizeof(*s));
+  s->N = N;
+  s->Hkv = Hkv;
+  s->topK = topK;
+  s->nblocks = nblocks;
+  s->R = Hkv * nblocks;
+  s->C = (N + msa::kChunk - 1) / msa::kChunk;
+  s->nW = (N + msa::kWindow - 1) / msa::kWindow;
+  s->cap_entries = static_cast<int64_t>(N) * Hkv * topK;
+  s->nseg = static_cast<int64_t>(s->nW) * s->R;
+  s->nseg_blocks = (s->nseg + msa::kSegScanBlock - 1) / msa::kSegScanBlock;
+  const int64_t nonempty = s->nseg < s->cap_entries ? s->nseg : s->cap_entries;
+  s->cap_tiles = s->cap_entries / msa::kTileQ + nonempty + 1;
+  carve(s, nullptr);
+  cudaError_t e = cudaMalloc(&s->dev_base, s->dev_bytes);
+  if (e != cudaSuccess) {
+    delete s;
+    return from_cuda(e);
+  }
+  carve(s, static_cast<char*>(s->dev_base));
+  *out = s;
+  return MSA_OK;
+}
+
+msa_status_t ensure_partials(msa_schedule* s, int G) {
+  if (s->partial && s->partial_G == G) return MSA_OK;
+  if (s->partial) {
+    cudaFree(s->partial);
+    s->partial = nullptr;
+    s->plse = nullptr;
+  }
+  const size_t rows = static_cast<size_t>(s->cap_entries) * G;
+  const size_t bytes = align_up(rows * msa::kHeadDim * 2, 256) + rows * sizeof(float);
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) return from_cuda(e);
+  s->partial = p;
+  s->plse = reinterpret_cast<float*>(static_cast<char*>(p) + align_up(rows * msa::kHeadDim * 2, 256));
+  s->partial_G = G;
+  return MSA_OK;
+}
+
+}  // namespace
+
+namespace msa {
+bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz) {
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode) return false;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+  CUresult r = g_encode(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd, gs, bx, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+}  // namespace msa
+
+extern "C" {
+
+void msa_fwd_opts_init(msa_fwd_opts_t* opts) {
+  if (!opts) return;
+  std::memset(opts, 0, sizeof(*opts));
+  opts->path = MSA_PATH_AUTO;
+  opts->q_descale = opts->k_descale = opts->v_descale = 1.f;
+}
+
+msa_status_t msa_build_schedule(const int32_t* indices, int N, int Hkv, int topK, int nblocks, cudaStream_t stream,
+                                msa_schedule_t* inout) {
+  if (!indices || !inout) return MSA_ERR_INVALID_ARG;
+  if (N < 1 || Hkv < 1 || topK < 1 || nblocks < 1) return MSA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(nblocks) * msa::kBlock > INT32_MAX) return MSA_ERR_CAPACITY;
+  if (static_cast<int64_t>(N) > static_cast<int64_t>(nblocks) * msa::kBlock) return MSA_ERR_INVALID_ARG;
+  if (topK > 64) return MSA_ERR_UNSUPPORTED;
+  const int64_t rows16 = static_cast<int64_t>(N) * Hkv * topK * msa::kGroup;
+  if (rows16 > INT32_MAX || static_cast<int64_t>(Hkv) * nblocks > INT32_MAX) return MSA_ERR_CAPACITY;
+  msa_schedule* s = *inout;
+  if (s) {
+    if (s->N != N || s->Hkv != Hkv || s->topK != topK || s->nblocks != nblocks) return MSA_ERR_INVALID_ARG;
+  } else {
+    msa_status_t st = schedule_create(N, Hkv, topK, nblocks, &s);
+    if (st != MSA_OK) return st;
+  }
+  cudaError_t e = msa::enqueue_schedule(s, indices, stream);
+  s->last_stream = stream;
+  if (!*inout) {
+    if (e != cudaSuccess) {
+      cudaFree(s->dev_base);
+      delete s;
+      return from_cuda(e);
+    }
+    *inout = s;
+  }
+  return from_cuda(e);
+}
+
+msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, msa_schedule_t s, void* O,
+                                 float* LSE, float scale, const msa_fwd_opts_t* opts) {
+  msa_fwd_opts_t def;
+  if (!opts) {
+    msa_fwd_opts_init(&def);
+    opts = &def;
+  }
+  if (!s || !Q.ptr || !K.ptr || !V.ptr || !O) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(Q.ptr) || !aligned16(K.ptr) || !aligned16(V.ptr) || !aligned16(O)) return MSA_ERR_INVALID_ARG;
+  if (Q.n != s->N || K.n != static_cast<int64_t>(s->nblocks) * msa::kBlock || V.n != K.n) return MSA_ERR_INVALID_ARG;
+  if (K.h != s->Hkv || V.h != s->Hkv || Q.h < 1 || Q.h % K.h != 0) return MSA_ERR_INVALID_ARG;
+  if (Q.d != K.d || K.d != V.d) return MSA_ERR_INVALID_ARG;
+  if (Q.dtype != K.dtype || K.dtype != V.dtype) return MSA_ERR_UNSUPPORTED;
+  if (Q.d != msa::kHeadDim || Q.h / K.h != msa::kGroup) return MSA_ERR_UNSUPPORTED;
+  if (Q.dtype != MSA_BF16) return MSA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return MSA_ERR_INVALID_ARG;
+  if (opts->path != MSA_PATH_AUTO && opts->path != MSA_PATH_KV_OUTER && opts->path != MSA_PATH_Q_OUTER)
+    return MSA_ERR_INVALID_ARG;
+  msa_status_t st = ensure_partials(s, msa::kGroup);
+  if (st != MSA_OK) return st;
+  const int force = opts->path == MSA_PATH_AUTO ? 0 : static_cast<int>(opts->path);
+  const cudaStream_t stream = opts->stream;
+  int ctas = opts->num_ctas > 0 ? opts->num_ctas : device_sms();
+  if (ctas < 1) return MSA_ERR_CUDA;
+  const int Hq = static_cast<int>(Q.h);
+  cudaError_t e;
+  if (opts->stage_events[0] && (e = cudaEventRecord(opts->stage_events[0], stream))) return from_cuda(e);
+  msa::KvOuterArgs a{s, Q.ptr, K.ptr, V.ptr, Hq, s->nblocks * msa::kBlock, scale, force, ctas};
+  if ((e = msa::launch_kv_outer(a, stream))) return from_cuda(e);
+  if (opts->stage_events[1] && (e = cudaEventRecord(opts->stage_events[1], stream))) return from_cuda(e);
+  if ((e = msa::launch_combine(s, Hq, O, LSE, force, stream))) return from_cuda(e);
+  if ((e = msa::launch_q_outer(s, Q.ptr, K.ptr, V.ptr, Hq, scale, O, LSE, force, stream))) return from_cuda(e);
+  if (opts->stage_events[2] && (e = cudaEventRecord(opts->stage_events[2], stream))) return from_cuda(e);
+  s->last_stream = stream;
+  return MSA_OK;
+}
+
+msa_status_t msa_schedule_destroy(msa_schedule_t s) {
+  if (!s) return MSA_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize(s->last_stream);
+  if (s->partial) cudaFree(s->partial);
+  if (s->dev_base) cudaFree(s->dev_base);
+  delete s;
+  return from_cuda(e);
+}
+
+msa_status_t msa_schedule_query(msa_schedule_t s, msa_schedule_info_t* info) {
+  if (!s || !info) return MSA_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize(s->last_stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  msa::SchedHeader h;
+  e = cudaMemcpy(&h, s->d.hdr, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return from_cuda(e);
+  info->entries = h.entries;
+  info->nsb = h.nsb;
+  info->ntiles = h.ntiles;
+  info->path = h.path;
+  info->status = h.status;
+  info->rows = s->R;
+  info->windows = s->nW;
+  if (h.status & msa::kStatusTimeout) return MSA_ERR_TIMEOUT;
+  if (h.status & msa::kStatusBadIndex) return MSA_ERR_BAD_INDEX;
+  return MSA_OK;
+}
+
+msa_status_t msa_schedule_export(msa_schedule_t s, int32_t* counts, int32_t* offsets, int32_t* qlist, int32_t* slot,
+                                 int32_t* cmap, int32_t* tiles, int32_t* window_tiles) {
+  if (!s) return MSA_ERR_INVALID_ARG;
+  msa_schedule_info_t info;
+  msa_status_t st = msa_schedule_query(s, &info);
+  if (st != MSA_OK && st != MSA_ERR_BAD_INDEX) return st;
+  struct Item {
+    void* dst;
+    const void* src;
+    size_t bytes;
+  } items[] = {
+      {counts, s->d.counts, sizeof(int32_t) * s->R},
+      {offsets, s->d.offsets, sizeof(int32_t) * (static_cast<size_t>(s->R) + 1)},
+      {qlist, s->d.qlist, sizeof(int32_t) * static_cast<size_t>(info.entries)},
+      {slot, s->d.slot, sizeof(int32_t) * static_cast<size_t>(info.entries)},
+      {cmap, s->d.cmap, sizeof(int32_t) * static_cast<size_t>(s->cap_entries)},
+      {tiles, s->d.tiles, sizeof(int4) * static_cast<size_t>(info.ntiles)},
+      {window_tiles, s->d.window_tiles, sizeof(int32_t) * (static_cast<size_t>(s->nW) + 1)},
+  };
+  for (const Item& it : items) {
+    if (!it.dst || it.bytes == 0) continue;
+    cudaError_t e = cudaMemcpy(it.dst, it.src, it.bytes, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return st;
+}
+
+const char* msa_status_string(msa_status_t st) {
+  switch (st) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_INVALID_ARG: return "invalid argument";
+    case MSA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MSA_ERR_CUDA: return "CUDA runtime error";
+    case MSA_ERR_OOM: return "device allocation failed";
+    case MSA_ERR_BAD_INDEX: return "block id out of range in indices (ignored)";
+    case MSA_ERR_TIMEOUT: return "bounded device wait expired";
+    case MSA_ERR_CAPACITY: return "size exceeds a fixed capacity";
+  }
+  return "unknown status";
+}
+
+int msa_last_cuda_error(void) { return g_last_cuda; }
+
+int msa_version(void) { return 100; }
+
+}  // extern "C"

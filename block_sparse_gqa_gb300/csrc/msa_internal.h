@@ -1,0 +1,98 @@
+// Internal declarations shared by the libmsa translation units.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/msa.h"
+
+namespace msa {
+
+constexpr int kBlock = 128;      // tokens per KV block
+constexpr int kHeadDim = 128;    // D
+constexpr int kGroup = 16;       // G = Hq / Hkv handled by the kernels
+constexpr int kTileQ = 8;        // queries per tile: 8 queries x 16 heads = 128 MMA rows
+constexpr int kChunk = 32;       // queries per bitmask word of the schedule
+constexpr int kWindow = 256;     // queries per work-list window (multiple of kChunk)
+
+constexpr int kPathKvOuter = 1;
+constexpr int kPathQOuter = 2;
+
+constexpr int kStatusBadIndex = 1;
+constexpr int kStatusTimeout = 2;
+
+// Device-resident header written by the schedule kernels and read by the attention
+// kernels (the dispatch decision never leaves the device).
+struct SchedHeader {
+  int32_t entries;  // E
+  int32_t nsb;
+  int32_t ntiles;
+  int32_t path;     // AUTO choice: kPathKvOuter or kPathQOuter
+  int32_t status;   // sticky kStatus* bits
+  int32_t pad[3];
+};
+
+struct SchedDev {
+  uint32_t* mask;        // [R][C] bit (i % 32) of word (r, i / 32): query i has an entry in row r
+  int32_t* rowbase;      // [R][C + 1] exclusive prefix of popcounts along each row
+  int32_t* counts;       // [R]
+  int32_t* offsets;      // [R + 1]
+  int32_t* qlist;        // [cap_entries]
+  int32_t* slot;         // [cap_entries]
+  int32_t* cmap;         // [N * Hkv * topK] CSR position of list slot k, or -1
+  int32_t* blist;        // [N * Hkv * topK] block id of list slot k if it is an entry, else -1
+  int4* tiles;           // [cap_tiles] (row, first, count, window)
+  int32_t* window_tiles; // [nW + 1]
+  int32_t* segoff;       // [nW * R + 1] tiles per (window, row) segment, then their exclusive prefix
+  int32_t* seg_sums;     // [nseg_blocks + 1] scan scratch: per-block sums of segment tile counts
+  SchedHeader* hdr;
+};
+
+}  // namespace msa
+
+struct msa_schedule {
+  int N, Hkv, topK, nblocks;
+  int R, C, nW;
+  int64_t cap_entries, cap_tiles, nseg, nseg_blocks;
+  void* dev_base;
+  size_t dev_bytes;
+  msa::SchedDev d;
+  // partial-output workspace (first forward call)
+  void* partial;       // bf16 [cap_entries * G, D]
+  float* plse;         // fp32 [cap_entries * G] (base-2 log-sum-exp of each partial row)
+  int partial_G;
+  cudaStream_t last_stream;
+};
+
+namespace msa {
+
+// schedule.cu
+cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream_t st);
+constexpr int kSegScanBlock = 4096;  // segments per block of the segment scan
+
+// attn_kv_outer.cu
+struct KvOuterArgs {
+  const msa_schedule* s;
+  const void* Q;
+  const void* K;
+  const void* V;
+  int Hq, Lkv;
+  float scale;
+  int force_path;  // 0 auto, 1 kv, 2 q
+  int num_ctas;
+};
+cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st);
+
+// combine.cu
+cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, int force_path,
+                           cudaStream_t st);
+
+// attn_q_outer.cu
+cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, const void* V, int Hq,
+                           float scale, void* O, float* LSE, int force_path, cudaStream_t st);
+
+// tensor maps (msa_api.cpp)
+bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz);
+
+}  // namespace msa

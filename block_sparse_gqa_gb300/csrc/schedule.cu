@@ -1,0 +1,295 @@
+// Schedule: index inversion and work list, entirely on the device.
+//
+// "Sparse Attention" (dinara-dl), Chapter 5, "Reverse index": the selector gives
+// each query its blocks; the KV-centric kernel needs, for each block, the queries
+// that chose it, plus the block's place in each query's list, and popular blocks
+// are split into several tasks.  "Kernel optimization for MiniMax M3", load-
+// balancing section: one on-device pass flattens all (kv_head, kv_block, query)
+// work into a sequence and hands each CTA a contiguous slice; shapes are fixed so
+// nothing is read back to the host.
+//
+// Determinism without atomics deciding order: every (row, query) entry sets one
+// bit of a [row][query / 32] bitmask (atomicOr is order-independent).  A query's
+// rank inside its row is then the popcount of the bits below it, so the scatter
+// that follows is a pure function of the input and rows come out sorted by query.
+//
+// Kernels, in stream order:
+//   mark        bits for every valid entry; bad ids -> sticky status bit
+//   rowscan     per row: exclusive popcount prefix over words, row count, tiles per
+//               (window, row) segment
+//   scan_rows   offsets, E, nsb and the Q-outer / KV-outer decision
+//   seg_*       exclusive scan of the segment tile counts (3 passes)
+//   scatter     qlist, slot, cmap, blist
+//   tiles       the work list, window-major, 8-entry tiles
+#include "msa_internal.h"
+#include "ptx.cuh"
+
+namespace msa {
+namespace {
+
+template <int NT>
+__device__ int block_exclusive_scan(int v, int* total, int* warp_buf) {
+  static_assert(NT % 32 == 0 && NT <= 1024, "block size");
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_buf[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = lane < NT / 32 ? warp_buf[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < NT / 32) warp_buf[lane] = w;
+  }
+  __syncthreads();
+  const int prefix = wid ? warp_buf[wid - 1] : 0;
+  *total = warp_buf[NT / 32 - 1];
+  __syncthreads();
+  return prefix + x - v;
+}
+
+// Entry test shared by mark and scatter: slot k of list `lst` (query i, own block
+// lb) is an entry iff 0 <= b <= lb and b did not occur earlier in the list.
+__device__ __forceinline__ int entry_block(const int32_t* lst, int k, int lb, int nblocks, bool* bad) {
+  const int b = lst[k];
+  if (b < -1 || b >= nblocks) {
+    *bad = true;
+    return -1;
+  }
+  if (b < 0 || b > lb) return -1;
+  for (int k2 = 0; k2 < k; ++k2)
+    if (lst[k2] == b) return -1;
+  return b;
+}
+
+__global__ void k_mark(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int C,
+                       uint32_t* __restrict__ mask, SchedHeader* hdr) {
+  const int64_t nl = static_cast<int64_t>(N) * Hkv;
+  bool bad = false;
+  for (int64_t L = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; L < nl;
+       L += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(L / Hkv), g = static_cast<int>(L % Hkv);
+    const int lb = (Lkv - N + i) / kBlock;
+    const int32_t* lst = idx + L * topK;
+    for (int k = 0; k < topK; ++k) {
+      const int b = entry_block(lst, k, lb, nblocks, &bad);
+      if (b < 0) continue;
+      const size_t r = static_cast<size_t>(g) * nblocks + b;
+      atomicOr(&mask[r * C + (i >> 5)], 1u << (i & 31));
+    }
+  }
+  if (bad) atomicOr(&hdr->status, kStatusBadIndex);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) k_rowscan(const uint32_t* __restrict__ mask, int R, int C, int nW,
+                                                int32_t* __restrict__ rowbase, int32_t* __restrict__ counts,
+                                                int32_t* __restrict__ segtiles) {
+  __shared__ int warp_buf[32];
+  constexpr int kCpw = kWindow / kChunk;
+  for (int r = blockIdx.x; r < R; r += gridDim.x) {
+    const uint32_t* m = mask + static_cast<size_t>(r) * C;
+    int32_t* rb = rowbase + static_cast<size_t>(r) * (C + 1);
+    const int per = (C + NT - 1) / NT;
+    const int c0 = min(static_cast<int>(threadIdx.x) * per, C), c1 = min(c0 + per, C);
+    int sum = 0;
+    for (int c = c0; c < c1; ++c) sum += __popc(m[c]);
+    int total;
+    int run = block_exclusive_scan<NT>(sum, &total, warp_buf);
+    for (int c = c0; c < c1; ++c) {
+      rb[c] = run;
+      run += __popc(m[c]);
+    }
+    if (threadIdx.x == 0) {
+      rb[C] = total;
+      counts[r] = total;
+    }
+    __syncthreads();
+    for (int w = threadIdx.x; w < nW; w += NT) {
+      const int cw0 = w * kCpw, cw1 = min(cw0 + kCpw, C);
+      const int cnt = rb[cw1] - rb[cw0];
+      segtiles[static_cast<size_t>(w) * R + r] = (cnt + kTileQ - 1) / kTileQ;
+    }
+    __syncthreads();
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) k_scan_rows(const int32_t* __restrict__ counts, int R, int N,
+                                                  int32_t* __restrict__ offsets, SchedHeader* hdr) {
+  __shared__ int warp_buf[32];
+  const int per = (R + NT - 1) / NT;
+  const int r0 = min(static_cast<int>(threadIdx.x) * per, R), r1 = min(r0 + per, R);
+  int sum = 0, nz = 0;
+  for (int r = r0; r < r1; ++r) {
+    sum += counts[r];
+    nz += counts[r] > 0;
+  }
+  int total, nsb;
+  int run = block_exclusive_scan<NT>(sum, &total, warp_buf);
+  block_exclusive_scan<NT>(nz, &nsb, warp_buf);
+  for (int r = r0; r < r1; ++r) {
+    offsets[r] = run;
+    run += counts[r];
+  }
+  if (threadIdx.x == 0) {
+    offsets[R] = total;
+    hdr->entries = total;
+    hdr->nsb = nsb;
+    // crossover: KV-outer when nsb / N < 2.85, in exact integers
+    hdr->path = (static_cast<int64_t>(nsb) * 100 < static_cast<int64_t>(N) * 285) ? kPathKvOuter : kPathQOuter;
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) k_seg_reduce(const int32_t* __restrict__ seg, int64_t nseg,
+                                                   int32_t* __restrict__ sums) {
+  __shared__ int warp_buf[32];
+  constexpr int per = kSegScanBlock / NT;
+  const int64_t s0 = static_cast<int64_t>(blockIdx.x) * kSegScanBlock + threadIdx.x * per;
+  int sum = 0;
+  for (int j = 0; j < per; ++j)
+    if (s0 + j < nseg) sum += seg[s0 + j];
+  int total;
+  block_exclusive_scan<NT>(sum, &total, warp_buf);
+  if (threadIdx.x == 0) sums[blockIdx.x] = total;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) k_seg_top(int32_t* __restrict__ sums, int nb, int32_t* __restrict__ segoff,
+                                                int64_t nseg, int32_t* __restrict__ window_tiles, int nW,
+                                                SchedHeader* hdr) {
+  __shared__ int warp_buf[32];
+  const int per = (nb + NT - 1) / NT;
+  const int b0 = min(static_cast<int>(threadIdx.x) * per, nb), b1 = min(b0 + per, nb);
+  int sum = 0;
+  for (int b = b0; b < b1; ++b) sum += sums[b];
+  int total;
+  int run = block_exclusive_scan<NT>(sum, &total, warp_buf);
+  for (int b = b0; b < b1; ++b) {
+    const int v = sums[b];
+    sums[b] = run;
+    run += v;
+  }
+  if (threadIdx.x == 0) {
+    sums[nb] = total;
+    segoff[nseg] = total;
+    window_tiles[nW] = total;
+    hdr->ntiles = total;
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) k_seg_down(int32_t* __restrict__ seg, int64_t nseg,
+                                                 const int32_t* __restrict__ sums, int R,
+                                                 int32_t* __restrict__ window_tiles) {
+  __shared__ int warp_buf[32];
+  constexpr int per = kSegScanBlock / NT;
+  const int64_t s0 = static_cast<int64_t>(blockIdx.x) * kSegScanBlock + threadIdx.x * per;
+  int v[per];
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < per; ++j) {
+    v[j] = (s0 + j < nseg) ? seg[s0 + j] : 0;
+    sum += v[j];
+  }
+  int total;
+  int run = block_exclusive_scan<NT>(sum, &total, warp_buf) + sums[blockIdx.x];
+#pragma unroll
+  for (int j = 0; j < per; ++j) {
+    const int64_t s = s0 + j;
+    if (s < nseg) {
+      seg[s] = run;
+      if (s % R == 0) window_tiles[s / R] = run;
+    }
+    run += v[j];
+  }
+}
+
+__global__ void k_scatter(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int C,
+                          const uint32_t* __restrict__ mask, const int32_t* __restrict__ rowbase,
+                          const int32_t* __restrict__ offsets, int32_t* __restrict__ qlist,
+                          int32_t* __restrict__ slot, int32_t* __restrict__ cmap, int32_t* __restrict__ blist) {
+  const int64_t nl = static_cast<int64_t>(N) * Hkv;
+  bool bad = false;
+  for (int64_t L = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; L < nl;
+       L += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(L / Hkv), g = static_cast<int>(L % Hkv);
+    const int lb = (Lkv - N + i) / kBlock;
+    const int32_t* lst = idx + L * topK;
+    for (int k = 0; k < topK; ++k) {
+      const int b = entry_block(lst, k, lb, nblocks, &bad);
+      int p = -1;
+      if (b >= 0) {
+        const size_t r = static_cast<size_t>(g) * nblocks + b;
+        const uint32_t word = mask[r * C + (i >> 5)];
+        const int rank = rowbase[r * (C + 1) + (i >> 5)] + __popc(word & ((1u << (i & 31)) - 1u));
+        p = offsets[r] + rank;
+        qlist[p] = i;
+        slot[p] = k;
+      }
+      cmap[L * topK + k] = p;
+      blist[L * topK + k] = b;
+    }
+  }
+}
+
+__global__ void k_tiles(const int32_t* __restrict__ segoff, int64_t nseg, int R, int C,
+                        const int32_t* __restrict__ rowbase, const int32_t* __restrict__ offsets,
+                        int4* __restrict__ tiles) {
+  constexpr int kCpw = kWindow / kChunk;
+  for (int64_t s = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; s < nseg;
+       s += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t0 = segoff[s], n = segoff[s + 1] - t0;
+    if (n == 0) continue;
+    const int w = static_cast<int>(s / R), r = static_cast<int>(s % R);
+    const int cw0 = w * kCpw, cw1 = min(cw0 + kCpw, C);
+    const int32_t* rb = rowbase + static_cast<size_t>(r) * (C + 1);
+    const int first = offsets[r] + rb[cw0];
+    const int cnt = rb[cw1] - rb[cw0];
+    for (int j = 0; j < n; ++j)
+      tiles[t0 + j] = make_int4(r, first + kTileQ * j, min(kTileQ, cnt - kTileQ * j), w);
+  }
+}
+
+int grid_for(int64_t n, int threads, int cap) {
+  int64_t g = (n + threads - 1) / threads;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return static_cast<int>(g);
+}
+
+}  // namespace
+
+cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream_t st) {
+  const SchedDev& d = s->d;
+  const int Lkv = s->nblocks * kBlock;
+  const int64_t nl = static_cast<int64_t>(s->N) * s->Hkv;
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(d.mask, 0, sizeof(uint32_t) * static_cast<size_t>(s->R) * s->C, st))) return e;
+  if ((e = cudaMemsetAsync(d.hdr, 0, sizeof(SchedHeader), st))) return e;
+  k_mark<<<grid_for(nl, 256, 1 << 16), 256, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C,
+                                                      d.mask, d.hdr);
+  k_rowscan<256><<<grid_for(s->R, 1, 1 << 20), 256, 0, st>>>(d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
+                                                             d.segoff);
+  k_scan_rows<1024><<<1, 1024, 0, st>>>(d.counts, s->R, s->N, d.offsets, d.hdr);
+  const int nb = static_cast<int>(s->nseg_blocks);
+  k_seg_reduce<256><<<nb, 256, 0, st>>>(d.segoff, s->nseg, d.seg_sums);
+  k_seg_top<1024><<<1, 1024, 0, st>>>(d.seg_sums, nb, d.segoff, s->nseg, d.window_tiles, s->nW, d.hdr);
+  k_seg_down<256><<<nb, 256, 0, st>>>(d.segoff, s->nseg, d.seg_sums, s->R, d.window_tiles);
+  k_scatter<<<grid_for(nl, 256, 1 << 16), 256, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C,
+                                                         d.mask, d.rowbase, d.offsets, d.qlist, d.slot, d.cmap,
+                                                         d.blist);
+  k_tiles<<<grid_for(s->nseg, 256, 1 << 16), 256, 0, st>>>(d.segoff, s->nseg, s->R, s->C, d.rowbase, d.offsets,
+                                                            d.tiles);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

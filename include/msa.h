@@ -1,0 +1,176 @@
+/*
+ * msa.h -- C ABI of libmsa: forward main branch of block-sparse attention on GQA
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("Kernel optimization for MiniMax M3 on NVIDIA Blackwell",
+ * opening section): the KV sequence is cut into 128-token blocks; for every query
+ * token and every KV head (GQA group) a list of topK block ids is given; each query
+ * head attends, exactly, to the keys of the blocks its group selected, and nowhere
+ * else.  The softmax of a query is normalised over the union of its selected blocks
+ * ("Sparse Attention", Chapter 1).  The query's own block is attended with a causal
+ * mask ("Flash-MSA": the local block is always kept, sliding-window style).
+ *
+ * Conventions used by every call:
+ *   - Q is [N, Hq, D], K and V are [Lkv, Hkv, D], all contiguous, on the device.
+ *     D = 128, block = 128 tokens, Lkv = 128 * nblocks, G = Hq / Hkv = 16.
+ *   - The N queries are the LAST N positions of the sequence: query i sits at
+ *     pos(i) = Lkv - N + i and sees key j iff j <= pos(i).  lb(i) = pos(i) / 128 is
+ *     its own (local) block.
+ *   - Head h uses KV head g = h / G.
+ *   - indices is int32 [N, Hkv, topK] on the device.  -1 is padding; a repeated id
+ *     counts once; an id above lb(i) contributes nothing; an id >= nblocks or < -1
+ *     is invalid (ignored, and reported by msa_schedule_query).
+ *   - O is bf16 [N, Hq, D]; LSE is fp32 [N, Hq], the natural log of
+ *     sum_j exp(scale * q.k_j) over the visible selected keys (-inf if none, with
+ *     O = 0).
+ *   - Every call is asynchronous on the given stream and never synchronises the
+ *     host, except msa_schedule_query / msa_schedule_export (documented as such).
+ *   - No call aborts, traps or prints.  Errors are returned as msa_status_t; host-
+ *     checkable errors return before anything is enqueued.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1,  /* null pointer, inconsistent shapes, bad sizes */
+  MSA_ERR_UNSUPPORTED = 2,  /* valid but not built: D != 128, G != 16, ... */
+  MSA_ERR_CUDA = 3,         /* a CUDA runtime call failed (see msa_last_cuda_error) */
+  MSA_ERR_OOM = 4,          /* device allocation failed */
+  MSA_ERR_BAD_INDEX = 5,    /* device saw block ids >= nblocks or < -1 (ignored) */
+  MSA_ERR_TIMEOUT = 6,      /* a bounded device wait expired; outputs undefined */
+  MSA_ERR_CAPACITY = 7      /* a size exceeds a fixed capacity */
+} msa_status_t;
+
+typedef enum { MSA_BF16 = 0, MSA_FP8_E4M3 = 1 } msa_dtype_t;
+
+/* Which kernel computes the attention.  AUTO follows the crossover of "Kernel
+ * optimization for MiniMax M3" (Q-outer vs KV-outer): KV-outer when nsb / N < 2.85,
+ * where nsb is the number of distinct selected (KV head, block) pairs.  The choice
+ * is made on the device by msa_build_schedule; no device-to-host copy is needed. */
+typedef enum { MSA_PATH_AUTO = 0, MSA_PATH_KV_OUTER = 1, MSA_PATH_Q_OUTER = 2 } msa_path_t;
+
+/* Opaque schedule: the reverse index of one indices tensor plus its device
+ * workspace.  It owns device memory; destroy it with msa_schedule_destroy. */
+typedef struct msa_schedule* msa_schedule_t;
+
+/* A dense [n, h, d] device tensor. */
+typedef struct {
+  const void* ptr;
+  msa_dtype_t dtype;
+  int64_t n, h, d;
+} msa_tensor_t;
+
+typedef struct {
+  cudaStream_t stream;   /* stream for every launch; 0 = legacy default stream */
+  msa_path_t path;       /* AUTO, or force one kernel (tests, studies) */
+  float q_descale;       /* fp8 only: real value = stored e4m3 value * descale */
+  float k_descale;
+  float v_descale;
+  /* Optional CUDA events recorded on `stream` (NULL = skip):
+   * [0] before the attention kernel, [1] after it, [2] after the combine. */
+  cudaEvent_t stage_events[3];
+  int num_ctas;          /* persistent grid size for the KV-outer kernel; 0 = #SMs */
+} msa_fwd_opts_t;
+
+/* Fill *opts with the defaults: stream 0, AUTO, descales 1, no events, #SMs. */
+void msa_fwd_opts_init(msa_fwd_opts_t* opts);
+
+/*
+ * msa_build_schedule -- index inversion ("Sparse Attention", Chapter 5, "Reverse
+ * index"; "Kernel optimization for MiniMax M3", load-balancing section).
+ *
+ * From indices [N, Hkv, topK] builds, on `stream`, with no host synchronisation:
+ *   - the CSR over rows r = g * nblocks + b: counts[r], offsets[r], and for every
+ *     entry the query (ascending within a row) and its slot in that query's list;
+ *   - the combine map (i, g, k) -> CSR position (or -1);
+ *   - a work list of tiles (at most 8 entries of one row) ordered by query window,
+ *     so heavy blocks are split over many CTAs;
+ *   - nsb and the Q-outer / KV-outer choice, kept on the device.
+ *
+ * *inout: NULL on entry -> a new schedule is allocated (cudaMalloc, synchronous)
+ * and returned.  A schedule from an earlier call with the same (N, Hkv, topK,
+ * nblocks) -> its workspace is reused and nothing is allocated.  `indices` is read
+ * by kernels on `stream`: keep it alive until the stream passes this call.  The
+ * schedule keeps no pointer to it.
+ *
+ * Returns MSA_ERR_INVALID_ARG for null pointers, N < 1, N > 128 * nblocks,
+ * Hkv < 1, topK < 1 or nblocks < 1; MSA_ERR_CAPACITY when N * Hkv * topK * 16
+ * exceeds 2^31 - 1; MSA_ERR_OOM / MSA_ERR_CUDA on allocation or launch failure.
+ */
+msa_status_t msa_build_schedule(const int32_t* indices, int N, int Hkv, int topK, int nblocks,
+                                cudaStream_t stream, msa_schedule_t* inout);
+
+/*
+ * msa_sparse_attn_fwd -- the forward main branch over a built schedule.
+ *
+ * KV-outer path ("Kernel optimization for MiniMax M3", kernel stages): a persistent
+ * warp-specialised tcgen05 kernel loads each selected K/V block with TMA, gathers
+ * the queries that chose it, computes S = Q K^T and P V in tensor memory with one
+ * softmax step per tile, and writes partial outputs (bf16) and their log-sum-exp in
+ * contiguous tile-ordered slabs; a combine kernel gathers each query's partials and
+ * merges them by LSE weighting ("Sparse Attention", Chapter 5, "Partial outputs and
+ * Combine").  Q-outer path (same page, Q-outer structure): one unit per (query,
+ * group) walks its own blocks with an online softmax and writes O and LSE directly.
+ *
+ * Q: [N, Hq, D]; K, V: [Lkv, Hkv, D]; all bf16, or all MSA_FP8_E4M3 with descales in
+ * opts.  O: bf16 [N, Hq, D] device; LSE: fp32 [N, Hq] device (may be NULL).
+ * scale multiplies q.k (typically 1/sqrt(D)).  opts may be NULL (defaults).
+ *
+ * The first call for a given head count allocates the partial-output workspace of
+ * the schedule (cudaMalloc, synchronous): N*Hkv*topK*G*(2*D + 4) bytes at most.
+ * Later calls allocate nothing.
+ *
+ * Returns MSA_ERR_INVALID_ARG on null pointers or shapes inconsistent with the
+ * schedule; MSA_ERR_UNSUPPORTED for D != 128, G != 16 or mixed dtypes;
+ * MSA_ERR_CUDA on launch failure.
+ */
+msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, msa_schedule_t s,
+                                 void* O, float* LSE, float scale, const msa_fwd_opts_t* opts);
+
+/* Frees the schedule's device memory (synchronises its last stream first). */
+msa_status_t msa_schedule_destroy(msa_schedule_t s);
+
+typedef struct {
+  int64_t entries;     /* E: valid (query, group, block) entries */
+  int32_t nsb;         /* distinct selected (group, block) pairs */
+  int32_t ntiles;      /* tiles in the work list */
+  int32_t path;        /* 1 = KV-outer, 2 = Q-outer (the AUTO choice) */
+  int32_t status;      /* device-side sticky flags: bit0 bad index, bit1 timeout */
+  int32_t rows;        /* Hkv * nblocks */
+  int32_t windows;     /* query windows of the work list */
+} msa_schedule_info_t;
+
+/* Synchronises the schedule's last stream and reads its device header.  Returns
+ * MSA_ERR_BAD_INDEX / MSA_ERR_TIMEOUT when the sticky flags are set (info is still
+ * filled).  Test and debug use. */
+msa_status_t msa_schedule_query(msa_schedule_t s, msa_schedule_info_t* info);
+
+/* Synchronises and copies the schedule to host arrays (any may be NULL):
+ * counts[rows], offsets[rows+1], qlist[E], slot[E], cmap[N*Hkv*topK],
+ * tiles[4*ntiles] as (row, first, count, window), window_tiles[windows+1].
+ * Test and debug use. */
+msa_status_t msa_schedule_export(msa_schedule_t s, int32_t* counts, int32_t* offsets,
+                                 int32_t* qlist, int32_t* slot, int32_t* cmap, int32_t* tiles,
+                                 int32_t* window_tiles);
+
+/* Human-readable text for a status code (static storage). */
+const char* msa_status_string(msa_status_t st);
+
+/* The last CUDA error code seen by the library on this thread (0 if none). */
+int msa_last_cuda_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int msa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MSA_H_ */

@@ -1,0 +1,92 @@
+"""Schedule parity: the device reverse index is bit-exact against the oracle.
+
+"Sparse Attention" (dinara-dl), Chapter 5 "Reverse index"; "Kernel optimization for
+MiniMax M3", load-balancing and no-D2H sections.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.util import check_worklist
+
+pytestmark = pytest.mark.gpu
+
+
+def _msa():
+    import block_sparse_gqa_gb300 as msa
+    return msa
+
+
+def gpu_schedule(idx_np, nblocks, schedule=None):
+    msa = _msa()
+    idx = torch.from_numpy(np.ascontiguousarray(idx_np, np.int32)).cuda()
+    s = msa.build_schedule(idx, nblocks, schedule=schedule)
+    return s, s.export()
+
+
+def assert_same(exp, ref, N, Lkv):
+    for k in ("counts", "offsets", "qlist", "slot", "cmap"):
+        np.testing.assert_array_equal(exp[k], ref[k], err_msg=k)
+    assert exp["E"] == ref["E"] and exp["nsb"] == ref["nsb"]
+    assert exp["path"] == oracle.dispatch(ref["nsb"], N)
+    check_worklist(exp, ref, N)
+
+
+@pytest.mark.parametrize("name", ["tiny", "m3", "long", "lowreuse", "fp8"])
+def test_schedule_matches_oracle(name):
+    cfg = workloads.CONFIGS[name]
+    idx = workloads.make_indices(cfg)
+    ref = oracle.schedule(idx, Lkv=cfg.Lkv)
+    s, exp = gpu_schedule(idx, cfg.nblocks)
+    assert exp["status"] == 0
+    assert_same(exp, ref, cfg.N, cfg.Lkv)
+    s.close()
+
+
+def test_schedule_edge_cases():
+    rng = np.random.default_rng(0)
+    cases = []
+    # pads, duplicates, future blocks; N not a multiple of 32 or 256; queries at the tail
+    N, Lkv, Hkv, topK = 300, 1024, 2, 6
+    nb = Lkv // 128
+    idx = rng.integers(-1, nb, size=(N, Hkv, topK)).astype(np.int32)
+    idx[:, :, -1] = idx[:, :, 0]
+    cases.append((idx, Lkv))
+    cases.append((np.array([[[0]]], np.int32), 128))                       # one query, topK 1
+    cases.append((np.full((64, 1, 4), -1, np.int32), 512))                 # no entries at all
+    full = np.tile(np.arange(8, dtype=np.int32)[::-1], (1024, 3, 1))       # every block, most in the future
+    cases.append((full, 1024))
+    for idx, Lkv in cases:
+        ref = oracle.schedule(idx, Lkv=Lkv)
+        s, exp = gpu_schedule(idx, Lkv // 128)
+        assert_same(exp, ref, idx.shape[0], Lkv)
+        s.close()
+
+
+def test_schedule_bad_index_flagged_and_ignored():
+    msa = _msa()
+    idx = np.array([[[0, 5, -3, 0]], [[1, 0, -1, 99]]], np.int32)  # nblocks = 2, N = 2 at the tail of 256
+    ref = oracle.schedule(idx, Lkv=256)
+    s, exp = gpu_schedule(idx, 2)
+    assert exp["status"] & 1 and ref["status"] == 1
+    for k in ("counts", "offsets", "qlist", "slot", "cmap"):
+        np.testing.assert_array_equal(exp[k], ref[k])
+    assert s.query()["status_code"] == 5  # MSA_ERR_BAD_INDEX
+    s.close()
+    with pytest.raises(msa.MsaError):
+        msa.build_schedule(torch.zeros((4, 1, 2), dtype=torch.int32, device="cuda"), 0)
+
+
+def test_schedule_deterministic_and_reusable():
+    cfg = workloads.CONFIGS["m3"]
+    idx = workloads.make_indices(cfg)
+    s, a = gpu_schedule(idx, cfg.nblocks)
+    _, b = gpu_schedule(idx, cfg.nblocks, schedule=s)
+    for k in ("counts", "offsets", "qlist", "slot", "cmap", "tiles", "window_tiles"):
+        np.testing.assert_array_equal(a[k], b[k])
+    idx2 = workloads.make_indices(cfg, seed=77)
+    _, c = gpu_schedule(idx2, cfg.nblocks, schedule=s)
+    assert_same(c, oracle.schedule(idx2, Lkv=cfg.Lkv), cfg.N, cfg.Lkv)
+    s.close()
