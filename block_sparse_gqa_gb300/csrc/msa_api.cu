@@ -45,61 +45,18 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Carves the schedule's device arrays out of one allocation.
-struct Carver {
-  size_t off = 0;
-  char* base = nullptr;
-  template <class T>
-  T* take(size_t count) {
-    const size_t o = off;
-    off = align_up(off + count * sizeof(T), 256);
-    return base ? reinterpret_cast<T*>(base + o) : nullptr;
-  }
-};
-
-void carve(msa_schedule* s, char* base) {
-  Carver c;
-  c.base = base;
-  msa::SchedDev& d = s->d;
-  d.mask = c.take<uint32_t>(static_cast<size_t>(s->R) * s->C);
-  d.rowbase = c.take<int32_t>(static_cast<size_t>(s->R) * (s->C + 1));
-  d.counts = c.take<int32_t>(s->R);
-  d.offsets = c.take<int32_t>(static_cast<size_t>(s->R) + 1);
-  d.qlist = c.take<int32_t>(s->cap_entries);
-  d.slot = c.take<int32_t>(s->cap_entries);
-  d.cmap = c.take<int32_t>(s->cap_entries);
-  d.blist = c.take<int32_t>(s->cap_entries);
-  d.tiles = c.take<int4>(s->cap_tiles);
-  d.window_tiles = c.take<int32_t>(static_cast<size_t>(s->nW) + 1);
-  d.segoff = c.take<int32_t>(static_cast<size_t>(s->nseg) + 1);
-  d.seg_sums = c.take<int32_t>(static_cast<size_t>(s->nseg_blocks) + 1);
-  d.hdr = c.take<msa::SchedHeader>(1);
-  s->dev_bytes = c.off;
-}
-
 msa_status_t schedule_create(int N, int Hkv, int topK, int nblocks, msa_schedule** out) {
   msa_schedule* s = new (std::nothrow) msa_schedule();
   if (!s) return MSA_ERR_OOM;
   std::memset(s, 0, sizeof(*s));
-  s->N = N;
-  s->Hkv = Hkv;
-  s->topK = topK;
-  s->nblocks = nblocks;
-  s->R = Hkv * nblocks;
-  s->C = (N + msa::kChunk - 1) / msa::kChunk;
-  s->nW = (N + msa::kWindow - 1) / msa::kWindow;
-  s->cap_entries = static_cast<int64_t>(N) * Hkv * topK;
-  s->nseg = static_cast<int64_t>(s->nW) * s->R;
-  s->nseg_blocks = (s->nseg + msa::kSegScanBlock - 1) / msa::kSegScanBlock;
-  const int64_t nonempty = s->nseg < s->cap_entries ? s->nseg : s->cap_entries;
-  s->cap_tiles = s->cap_entries / msa::kTileQ + nonempty + 1;
-  carve(s, nullptr);
+  msa::schedule_dims(s, N, Hkv, topK, nblocks);
+  msa::carve_schedule(s, nullptr);
   cudaError_t e = cudaMalloc(&s->dev_base, s->dev_bytes);
   if (e != cudaSuccess) {
     delete s;
     return from_cuda(e);
   }
-  carve(s, static_cast<char*>(s->dev_base));
+  msa::carve_schedule(s, static_cast<char*>(s->dev_base));
   *out = s;
   return MSA_OK;
 }
@@ -125,6 +82,56 @@ msa_status_t ensure_partials(msa_schedule* s, int G) {
 }  // namespace
 
 namespace msa {
+// Carves the schedule's device arrays out of one allocation.
+struct Carver {
+  size_t off = 0;
+  char* base = nullptr;
+  template <class T>
+  T* take(size_t count) {
+    const size_t o = off;
+    off = align_up(off + count * sizeof(T), 256);
+    return base ? reinterpret_cast<T*>(base + o) : nullptr;
+  }
+};
+
+void carve_schedule(msa_schedule* s, char* base) {
+  Carver c;
+  c.base = base;
+  msa::SchedDev& d = s->d;
+  d.mask = c.take<uint32_t>(static_cast<size_t>(s->R) * s->C);
+  d.rowbase = c.take<int32_t>(static_cast<size_t>(s->R) * (s->C + 1));
+  d.counts = c.take<int32_t>(s->R);
+  d.offsets = c.take<int32_t>(static_cast<size_t>(s->R) + 1);
+  d.qlist = c.take<int32_t>(s->cap_entries);
+  d.slot = c.take<int32_t>(s->cap_entries);
+  d.cmap = c.take<int32_t>(s->cap_entries);
+  d.blist = c.take<int32_t>(s->cap_entries);
+  d.tiles = c.take<int4>(s->cap_tiles);
+  d.window_tiles = c.take<int32_t>(static_cast<size_t>(s->nW) + 1);
+  d.segoff = c.take<int32_t>(static_cast<size_t>(s->nseg) + 1);
+  d.seg_sums = c.take<int32_t>(static_cast<size_t>(s->nseg_blocks) + 1);
+  d.hdr = c.take<msa::SchedHeader>(1);
+  s->dev_bytes = c.off;
+}
+
+// Sizes of the schedule's arrays for (N, Hkv, topK, nblocks).
+void schedule_dims(msa_schedule* s, int N, int Hkv, int topK, int nblocks) {
+  s->N = N;
+  s->Hkv = Hkv;
+  s->topK = topK;
+  s->nblocks = nblocks;
+  s->R = Hkv * nblocks;
+  s->C = (N + kChunk - 1) / kChunk;
+  s->nW = (N + kWindow - 1) / kWindow;
+  s->cap_entries = static_cast<int64_t>(N) * Hkv * topK;
+  s->nseg = static_cast<int64_t>(s->nW) * s->R;
+  s->nseg_blocks = (s->nseg + kSegScanBlock - 1) / kSegScanBlock;
+  const int64_t nonempty = s->nseg < s->cap_entries ? s->nseg : s->cap_entries;
+  s->cap_tiles = s->cap_entries / kTileQ + nonempty + 1;
+}
+
+msa_status_t status_from_cuda(cudaError_t e) { return from_cuda(e); }
+
 bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
                  const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz) {
   std::call_once(g_encode_once, load_encode);

@@ -66,6 +66,13 @@ struct msa_schedule {
 
 namespace msa {
 
+// msa_api.cu: array sizes of a schedule, and the layout of its arrays inside one
+// device buffer starting at `base` (base == nullptr only computes s->dev_bytes).
+void schedule_dims(msa_schedule* s, int N, int Hkv, int topK, int nblocks);
+void carve_schedule(msa_schedule* s, char* base);
+// msa_api.cu: maps a CUDA error to a status and records it for msa_last_cuda_error.
+msa_status_t status_from_cuda(cudaError_t e);
+
 // schedule.cu
 cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream_t st);
 constexpr int kSegScanBlock = 4096;  // segments per block of the segment scan

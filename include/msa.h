@@ -161,6 +161,38 @@ msa_status_t msa_schedule_export(msa_schedule_t s, int32_t* counts, int32_t* off
                                  int32_t* qlist, int32_t* slot, int32_t* cmap, int32_t* tiles,
                                  int32_t* window_tiles);
 
+/* Bytes of device scratch behind msa_sparse_attn_fwd_noalloc. */
+#define MSA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * msa_sparse_attn_fwd_noalloc -- the whole forward (schedule, attention, combine)
+ * in one call that allocates no device memory.
+ *
+ * The pages have no counterpart for this call: it exists for callers that cannot
+ * call cudaMalloc, for example a serving process that reserves its entire device
+ * memory budget at start-up and may not grow it afterwards, a runtime that owns all
+ * device memory through its own pool, or a latency-critical loop that cannot absorb
+ * the device-wide synchronisation of cudaMalloc / cudaFree.
+ *
+ * Arguments are those of msa_build_schedule followed by those of
+ * msa_sparse_attn_fwd (without a schedule handle); results are the same as that
+ * pair's.  The schedule and the partial outputs live in one fixed device array of
+ * MSA_NOALLOC_SCRATCH_BYTES inside libmsa, which every GPU that loads the library
+ * holds until the process exits.  Limits: the workspace for N * Hkv * topK list
+ * slots (about 4.2 KB per slot for the partial outputs, plus the schedule) must fit
+ * in that array, else MSA_ERR_CAPACITY is returned before anything is enqueued (the
+ * 1024-query, 1 KV head, topK 4 shape fits; the M3 shape does not).
+ *
+ * The first call on a device looks up the array's device address with that device
+ * current; make that first call before any stream capture.  Every call reuses the
+ * same array and it keeps the previous call's contents: the call clears what must
+ * start at zero itself.  Calls that overlap on the GPU (other streams or threads)
+ * race on the array; the caller must serialise them.
+ */
+msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int N, int Hkv, int topK, int nblocks,
+                                         msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, void* O, float* LSE,
+                                         float scale, const msa_fwd_opts_t* opts);
+
 /* Human-readable text for a status code (static storage). */
 const char* msa_status_string(msa_status_t st);
 
