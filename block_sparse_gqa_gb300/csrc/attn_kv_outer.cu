@@ -3,30 +3,43 @@
 // "Kernel optimization for MiniMax M3 on NVIDIA Blackwell" (kernel stages): a CTA
 // owns one KV block at a time and attends every query that chose it; because each
 // tile sees a single block there is exactly one softmax step and no rescale of a
-// running output; partial outputs are written tile-ordered and contiguous, and the
-// combine kernel gathers them.  "Sparse Attention", Chapter 5: the KV-centric kernel
-// writes, per query and head, a partial output and a log-sum-exp.
+// running output; the softmax warps write the row statistics (m, l) directly and
+// the output warps evacuate the raw P V accumulator, so the two never wait on each
+// other; partial outputs are written tile-ordered and contiguous, and the combine
+// kernel gathers them.  "Sparse Attention", Chapter 5: the KV-centric kernel writes,
+// per query and head, a partial output and its softmax statistics.
 //
 // Work unit (tile): up to 8 consecutive CSR entries of one (group g, block b) row,
 // i.e. 8 queries x 16 heads = 128 MMA rows (the head-packed "box" of one query is
-// 16 rows).  Tiles come from the schedule's work list, window by window; inside a
-// window, CTA c takes the c-th contiguous slice.
+// 16 rows).  The schedule lists tiles window by window (256 queries per window).
+// CTAs take chunks of 8 consecutive tiles from that list with one atomicAdd on a
+// per-launch counter: all CTAs move through the windows together (Q and K/V of the
+// current windows stay in L2) and a slow SM simply takes fewer chunks.  Each tile
+// writes fixed output rows, so results do not depend on which CTA ran it.
 //
-// Warp roles (384 threads, one CTA per SM):
-//   warp 0      producer: TMA of the Q boxes of each tile (two 64-column halves per
-//               query) and of K_b / V_b whenever the row changes
-//   warp 1      MMA issuer: S[s] = Q K^T (tcgen05, smem x smem), then
-//               O[s] = P V with P read from TMEM (it overwrites S[s] in place)
-//   warp 2      TMEM allocation (512 columns: S[0], S[1], O[0], O[1])
-//   warps 4-7   group 0: softmax + epilogue of even tiles (stage 0)
-//   warps 8-11  group 1: softmax + epilogue of odd tiles  (stage 1)
-// Each thread of a group owns one MMA row (TMEM lane) through softmax and epilogue,
-// so 1/l never leaves its register.  The epilogue normalises, rounds to bf16,
-// writes a 128-byte-swizzled staging tile and one elected thread stores it with TMA
-// at partial rows [16*first, 16*(first+count)).
+// Warp roles (512 threads = 4 warpgroups, one CTA per SM; a warp reaches TMEM
+// lanes 32 * (warp % 4) .. + 31, so a warpgroup covers all 128 rows):
+//   warp 0       producer, all 32 lanes: claims chunks, reads each tile's info and
+//                query ids (lane j <-> query j, one tile ahead), publishes them in a
+//                shared-memory ring for the other roles, issues the Q box loads (TMA,
+//                lane j loads query j's two 64-column halves) and, on a row change,
+//                K_b / V_b into the next of two K/V buffers
+//   warp 1       TMEM allocation (512 columns: S[0], S[1], O[0], O[1]) and MMA
+//                issue: S[s] = Q K^T (tcgen05, smem x smem), then O[s] = P V with P
+//                read from TMEM (it overwrites S[s] in place)
+//   warps 4-7    softmax of even tiles (stage 0)
+//   warps 8-11   softmax of odd tiles  (stage 1)
+//   warps 12-15  output: O[s] -> bf16 -> swizzled staging -> TMA store
+// Registers are rebalanced per warpgroup with setmaxnreg: 56 for the control
+// warpgroup, 176 for the softmax warpgroups (a row's 128 scores stay in registers),
+// 104 for the output warpgroup: 128*56 + 256*176 + 128*104 = 65536, the block's
+// launch allocation (512 x 128), so every increase can be granted.
+// A softmax thread owns one MMA row (TMEM lane): row maximum m (base-2 units,
+// scale folded in), P = 2^(s*scale*log2e - m) written back over S as bf16 pairs,
+// row sum l; (m, l) go to global as one float2 per row.
 //
-// Partial layout: bf16 [E*16, 128] (row = 16*CSR position + head-in-group) and
-// base-2 log-sum-exp fp32 [E*16].
+// Partial layout: raw bf16 [E*16, 128] (row = 16*CSR position + head-in-group;
+// O_k = sum_j P_j V_j, not yet divided by l) and float2 (m, l) [E*16].
 #include <cfloat>
 
 #include "msa_internal.h"
@@ -35,52 +48,140 @@
 namespace msa {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr uint32_t kQBytes = 128 * 128 * 2;  // one Q tile (two 16 KB halves)
-constexpr uint32_t kKVBytes = 128 * 128 * 2;
-constexpr uint32_t kOffQ0 = 0, kOffQ1 = 32768, kOffK = 65536, kOffV = 98304, kOffSt0 = 131072,
-                   kOffSt1 = 163840, kOffCtl = 196608;
-constexpr uint32_t kSmemBytes = kOffCtl + 256 + 1024;  // + alignment slack
+constexpr int kThreads = 512;
+constexpr int kChunkTiles = 8;  // tiles per claimed chunk
+constexpr int kRing = 8;        // tile-info ring slots
+constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one Q / K / V / staging tile (two 16 KB halves)
+constexpr uint32_t kOffQ0 = 0, kOffQ1 = 32768, kOffK0 = 65536, kOffV0 = 98304, kOffK1 = 131072, kOffV1 = 163840,
+                   kOffSt = 196608, kOffCtl = 229376;
+constexpr uint32_t kCtlBytes = 1024;
+constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + alignment slack
 
-// barrier slots (8 bytes each) in the control area
+// barrier slots (8 bytes each) at the start of the control area
 enum {
-  B_QFULL0 = 0, B_QFULL1, B_QFREE0, B_QFREE1, B_KFULL, B_KFREE, B_VFULL, B_VFREE,
-  B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_PVDONE0, B_PVDONE1, B_COUNT
+  B_QFULL0 = 0, B_QFREE0 = 2, B_KFULL0 = 4, B_KFREE0 = 6, B_VFULL0 = 8, B_VFREE0 = 10,
+  B_SFULL0 = 12, B_PFULL0 = 14, B_PVDONE0 = 16, B_OFREE0 = 18, B_TFULL0 = 20, B_TEMPTY0 = 20 + kRing,
+  B_COUNT = 20 + 2 * kRing
 };
+constexpr uint32_t kOffTmemSlot = 8 * B_COUNT;  // 4 bytes
+constexpr uint32_t kOffRing = 512;              // kRing entries of 64 bytes
+static_assert(kOffTmemSlot + 4 <= kOffRing && kOffRing + 64 * kRing <= kCtlBytes, "control area");
+
+// One published tile: row (g * nblocks + b), first CSR position, count (0 = no more
+// work), flags (bit 0: new row, bits 8-15: K/V buffer), then the query ids.
+struct TileInfo {
+  int row, first, count, flags;
+  int q[kTileQ];
+  int pad[4];
+};
+static_assert(sizeof(TileInfo) == 64, "ring entry");
 
 struct KvParams {
   const int4* tiles;
-  const int32_t* window_tiles;
   const int32_t* qlist;
   SchedHeader* hdr;
-  float* plse;
-  int nW, N, Lkv, nblocks;
+  float2* pstat;
+  int N, Lkv, nblocks;
   float sl2;  // scale * log2(e)
   int force_path;
 };
 
-// This CTA's tiles, window by window: in window w (tiles [a, b)) it takes
-// [a + n*c/P, a + n*(c+1)/P).
-struct TileIter {
-  const int32_t* wt;
-  int nW, cta, P, w;
-  int64_t t, tend;
-  __device__ void init(const int32_t* wt_, int nW_, int cta_, int P_) {
-    wt = wt_; nW = nW_; cta = cta_; P = P_; w = -1; t = tend = 0;
-  }
-  __device__ bool next(int* ti) {
-    while (t >= tend) {
-      if (++w >= nW) return false;
-      const int64_t a = wt[w], n = wt[w + 1] - a;
-      t = a + n * cta / P;
-      tend = a + n * (cta + 1) / P;
-    }
-    *ti = static_cast<int>(t++);
-    return true;
-  }
-};
-
 __device__ __forceinline__ void flag_timeout(SchedHeader* hdr) { atomicOr(&hdr->status, kStatusTimeout); }
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (x0, x1) * s + c for a pair of floats held as one 64-bit register
+__device__ __forceinline__ uint64_t ffma2(uint64_t x, uint64_t s, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(s), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+
+// One row of a tile: scores v[0..127] (raw S), keys c > lim masked when kMasked.
+// Writes P = 2^(v * sl2 - m2) as bf16 pairs over columns [0, 64) of the row's S
+// columns in TMEM and returns (m2, l).  A positive scale is assumed here; a
+// negative one goes through softmax_row_any_scale.
+template <bool kMasked>
+__device__ __forceinline__ float2 softmax_row(uint32_t (&v)[128], int lim, float sl2, uint32_t tS) {
+  float a0 = -FLT_MAX, a1 = -FLT_MAX, a2 = -FLT_MAX, a3 = -FLT_MAX;
+#pragma unroll
+  for (int e = 0; e < 128; e += 8) {
+    float x[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) x[q] = (kMasked && e + q > lim) ? -FLT_MAX : __uint_as_float(v[e + q]);
+    a0 = max3(a0, x[0], x[1]);
+    a1 = max3(a1, x[2], x[3]);
+    a2 = max3(a2, x[4], x[5]);
+    a3 = max3(a3, x[6], x[7]);
+  }
+  const float m2 = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2;
+  const uint64_t sl2x2 = pack2(sl2, sl2), negm2 = pack2(-m2, -m2);
+  uint64_t s0 = 0, s1 = 0;  // pairs of partial row sums
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int col = 32 * c + e;
+      float x0, x1;
+      unpack2(ffma2(pack2(__uint_as_float(v[col]), __uint_as_float(v[col + 1])), sl2x2, negm2), x0, x1);
+      float p0 = ex2(x0), p1 = ex2(x1);
+      if (kMasked) {
+        if (col > lim) p0 = 0.f;
+        if (col + 1 > lim) p1 = 0.f;
+      }
+      if ((e >> 1) & 1) s1 = fadd2(s1, pack2(p0, p1));
+      else s0 = fadd2(s0, pack2(p0, p1));
+      pk[e >> 1] = pack_bf16x2(p0, p1);
+    }
+    tmem_st16(tS + c * 16, pk);
+  }
+  float l0, l1, l2, l3;
+  unpack2(s0, l0, l1);
+  unpack2(s1, l2, l3);
+  return make_float2(m2, (l0 + l1) + (l2 + l3));
+}
+
+// Any finite scale: the row extremum of v * sl2 taken directly (slower, rare).
+__device__ __forceinline__ float2 softmax_row_any_scale(uint32_t (&v)[128], int lim, float sl2, uint32_t tS) {
+  float m2 = -FLT_MAX;
+  for (int e = 0; e < 128; ++e)
+    if (e <= lim) m2 = fmaxf(m2, __uint_as_float(v[e]) * sl2);
+  float l = 0.f;
+  for (int c = 0; c < 4; ++c) {
+    uint32_t pk[16];
+    for (int e = 0; e < 32; e += 2) {
+      const int col = 32 * c + e;
+      const float p0 = col <= lim ? ex2(fmaf(__uint_as_float(v[col]), sl2, -m2)) : 0.f;
+      const float p1 = col + 1 <= lim ? ex2(fmaf(__uint_as_float(v[col + 1]), sl2, -m2)) : 0.f;
+      l += p0 + p1;
+      pk[e >> 1] = pack_bf16x2(p0, p1);
+    }
+    tmem_st16(tS + c * 16, pk);
+  }
+  return make_float2(m2, l);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -95,27 +196,37 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw_u + pad;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffCtl);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffCtl + 8 * B_COUNT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffCtl + kOffTmemSlot);
+  TileInfo* ring = reinterpret_cast<TileInfo*>(smem + kOffCtl + kOffRing);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // zero the Q stages once so rows of a partly filled tile never hold NaN patterns
-  for (uint32_t o = tid * 16; o < 2 * kQBytes; o += kThreads * 16)
+  for (uint32_t o = tid * 16; o < 2 * kTileBytes; o += kThreads * 16)
     *reinterpret_cast<uint4*>(smem + kOffQ0 + o) = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
 
   if (tid == 0) {
-    mbar_init(bar(B_QFULL0), 1); mbar_init(bar(B_QFULL1), 1);
-    mbar_init(bar(B_QFREE0), 1); mbar_init(bar(B_QFREE1), 1);
-    mbar_init(bar(B_KFULL), 1);  mbar_init(bar(B_KFREE), 1);
-    mbar_init(bar(B_VFULL), 1);  mbar_init(bar(B_VFREE), 1);
-    mbar_init(bar(B_SFULL0), 1); mbar_init(bar(B_SFULL1), 1);
-    mbar_init(bar(B_PFULL0), 128); mbar_init(bar(B_PFULL1), 128);
-    mbar_init(bar(B_PVDONE0), 1); mbar_init(bar(B_PVDONE1), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_QFULL0 + s), 1);
+      mbar_init(bar(B_QFREE0 + s), 1);
+      mbar_init(bar(B_KFULL0 + s), 1);
+      mbar_init(bar(B_KFREE0 + s), 1);
+      mbar_init(bar(B_VFULL0 + s), 1);
+      mbar_init(bar(B_VFREE0 + s), 1);
+      mbar_init(bar(B_SFULL0 + s), 1);
+      mbar_init(bar(B_PFULL0 + s), 128);
+      mbar_init(bar(B_PVDONE0 + s), 1);
+      mbar_init(bar(B_OFREE0 + s), 128);
+    }
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(bar(B_TFULL0 + r), 1);
+      mbar_init(bar(B_TEMPTY0 + r), 1);
+    }
     mbar_fence_init();
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -124,174 +235,235 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  TileIter iter;
-  iter.init(p.window_tiles, p.nW, blockIdx.x, gridDim.x);
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV);
+  if (warp < 4) {
+    regs_dec<56>();
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer (whole warp)
+      if (lane == 0) { tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); }
       const uint64_t pol_q = policy_evict_normal(), pol_kv = policy_evict_last();
-      int ti, it = 0, prev_row = -1, nk = 0;
-      while (iter.next(&ti)) {
-        const int4 tl = p.tiles[ti];
+      int* counter = &p.hdr->pad[0];
+      const int T = p.hdr->ntiles;
+      // tiles come in chunks of kChunkTiles; the next chunk is claimed one chunk ahead
+      int chunk = 0, next_chunk = 0;
+      if (lane == 0) {
+        chunk = atomicAdd(counter, 1);
+        next_chunk = atomicAdd(counter, 1);
+      }
+      chunk = __shfl_sync(0xffffffffu, chunk, 0);
+      next_chunk = __shfl_sync(0xffffffffu, next_chunk, 0);
+      int ti = chunk * kChunkTiles, tend = min(ti + kChunkTiles, T);
+      if (ti >= T) ti = T;
+      auto advance = [&]() {  // ti -> the next tile index, or T when no work is left
+        if (++ti < tend) return;
+        chunk = next_chunk;
+        int nc = 0;
+        if (lane == 0 && chunk * kChunkTiles < T) nc = atomicAdd(counter, 1);
+        next_chunk = __shfl_sync(0xffffffffu, nc, 0);
+        ti = chunk * kChunkTiles;
+        tend = min(ti + kChunkTiles, T);
+        if (ti >= T) ti = T;
+      };
+      int4 tl = ti < T ? p.tiles[ti] : make_int4(0, 0, 0, 0);
+      int qv = (ti < T && lane < tl.z) ? p.qlist[tl.y + lane] : 0;
+      int prev_row = -1, nk = 0;
+      bool ok = true;
+      // writes ring entry `it` (count 0 marks the end of the work); false on timeout
+      auto publish = [&](int it, int row, int first, int count, int flags, int q) -> bool {
+        const int slot = it % kRing;
+        bool w = true;
+        if (lane == 0) w = mbar_wait(bar(B_TEMPTY0 + slot), ((it / kRing) & 1) ^ 1);
+        if (!__shfl_sync(0xffffffffu, w, 0)) return false;
+        if (lane < kTileQ) ring[slot].q[lane] = q;
+        if (lane == 0) {
+          ring[slot].row = row;
+          ring[slot].first = first;
+          ring[slot].count = count;
+          ring[slot].flags = flags;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_TFULL0 + slot));
+        return true;
+      };
+      for (int it = 0;; ++it) {
+        const bool have = ti < T;
+        if (!have) {
+          // two end markers: the softmax warpgroups read alternate entries
+          if (!publish(it, 0, 0, 0, 0, 0) || !publish(it + 1, 0, 0, 0, 0, 0))
+            if (lane == 0) flag_timeout(p.hdr);
+          break;
+        }
+        const bool new_row = tl.x != prev_row;
+        const int kb = new_row ? (nk & 1) : ((nk - 1) & 1);
+        if (!publish(it, tl.x, tl.y, tl.z, (new_row ? 1 : 0) | (kb << 8), qv)) {
+          if (lane == 0) flag_timeout(p.hdr);
+          break;
+        }
+        // the tile after this one: its info now, its query ids at the end of the iteration
+        advance();
+        const bool have2 = ti < T;
+        const int4 tl2 = have2 ? p.tiles[ti] : make_int4(0, 0, 0, 0);
         const int s = it & 1;
         const int g = tl.x / p.nblocks, b = tl.x - g * p.nblocks;
-        if (!mbar_wait(bar(B_QFREE0 + s), ((it >> 1) & 1) ^ 1)) { flag_timeout(p.hdr); break; }
-        mbar_expect_tx(bar(B_QFULL0 + s), static_cast<uint32_t>(tl.z) * 4096u);
-        const uint32_t dq = sb + (s ? kOffQ1 : kOffQ0);
-        for (int j = 0; j < tl.z; ++j) {
-          const int q = p.qlist[tl.y + j];
-          tma_load_3d(dq + j * 2048, &tmQ, 0, g * kGroup, q, bar(B_QFULL0 + s), pol_q);
-          tma_load_3d(dq + 16384 + j * 2048, &tmQ, 64, g * kGroup, q, bar(B_QFULL0 + s), pol_q);
+        if (lane == 0) {
+          ok = mbar_wait(bar(B_QFREE0 + s), ((it >> 1) & 1) ^ 1);
+          if (ok) mbar_expect_tx(bar(B_QFULL0 + s), static_cast<uint32_t>(tl.z) * 4096u);
         }
-        if (tl.x != prev_row) {
-          if (!mbar_wait(bar(B_KFREE), (nk & 1) ^ 1)) { flag_timeout(p.hdr); break; }
-          mbar_expect_tx(bar(B_KFULL), kKVBytes);
-          tma_load_3d(sb + kOffK, &tmK, 0, g, b * kBlock, bar(B_KFULL), pol_kv);
-          tma_load_3d(sb + kOffK + 16384, &tmK, 64, g, b * kBlock, bar(B_KFULL), pol_kv);
-          if (!mbar_wait(bar(B_VFREE), (nk & 1) ^ 1)) { flag_timeout(p.hdr); break; }
-          mbar_expect_tx(bar(B_VFULL), kKVBytes);
-          tma_load_3d(sb + kOffV, &tmV, 0, g, b * kBlock, bar(B_VFULL), pol_kv);
-          tma_load_3d(sb + kOffV + 16384, &tmV, 64, g, b * kBlock, bar(B_VFULL), pol_kv);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) { if (lane == 0) flag_timeout(p.hdr); break; }
+        if (lane < tl.z) {
+          const uint32_t dq = sb + (s ? kOffQ1 : kOffQ0) + lane * 2048;
+          tma_load_3d(dq, &tmQ, 0, g * kGroup, qv, bar(B_QFULL0 + s), pol_q);
+          tma_load_3d(dq + 16384, &tmQ, 64, g * kGroup, qv, bar(B_QFULL0 + s), pol_q);
+        }
+        if (new_row) {
+          if (lane == 0) {
+            const uint32_t par = ((nk >> 1) & 1) ^ 1;
+            const uint32_t dk = sb + (kb ? kOffK1 : kOffK0), dv = sb + (kb ? kOffV1 : kOffV0);
+            ok = mbar_wait(bar(B_KFREE0 + kb), par);
+            if (ok) {
+              mbar_expect_tx(bar(B_KFULL0 + kb), kTileBytes);
+              tma_load_3d(dk, &tmK, 0, g, b * kBlock, bar(B_KFULL0 + kb), pol_kv);
+              tma_load_3d(dk + 16384, &tmK, 64, g, b * kBlock, bar(B_KFULL0 + kb), pol_kv);
+              ok = mbar_wait(bar(B_VFREE0 + kb), par);
+            }
+            if (ok) {
+              mbar_expect_tx(bar(B_VFULL0 + kb), kTileBytes);
+              tma_load_3d(dv, &tmV, 0, g, b * kBlock, bar(B_VFULL0 + kb), pol_kv);
+              tma_load_3d(dv + 16384, &tmV, 64, g, b * kBlock, bar(B_VFULL0 + kb), pol_kv);
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, ok, 0)) { if (lane == 0) flag_timeout(p.hdr); break; }
           ++nk;
           prev_row = tl.x;
         }
-        ++it;
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_f16(128, 128, 1, 1, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_f16(128, 128, 1, 1, 0, 1);
-      int ti, ti2;
-      bool have = iter.next(&ti);
-      int4 tl = have ? p.tiles[ti] : make_int4(0, 0, 0, 0);
-      int it = 0, prev_row = -1, nk = 0, nv = 0;
-      bool pv_pending = false, pv_new_row = false, pv_last = false;
-      bool ok = true;
-      while (ok && (have || pv_pending)) {
-        bool new_row = false, last = false, have2 = false;
-        int4 tl2 = make_int4(0, 0, 0, 0);
-        if (have) {
-          have2 = iter.next(&ti2);
-          if (have2) tl2 = p.tiles[ti2];
-          const int s = it & 1;
-          // S[s] / P[s] is reused: PV of tile it-2 must have consumed P
-          if (it >= 2 && !mbar_wait(bar(B_PVDONE0 + s), ((it - 2) >> 1) & 1)) { ok = false; break; }
-          new_row = tl.x != prev_row;
-          last = !have2 || tl2.x != tl.x;
-          if (new_row) {
-            if (!mbar_wait(bar(B_KFULL), nk & 1)) { ok = false; break; }
-            ++nk;
-          }
-          if (!mbar_wait(bar(B_QFULL0 + s), (it >> 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t qa = sb + (s ? kOffQ1 : kOffQ0), ka = sb + kOffK;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-            mma_f16_ss(tmem + s * 128, smem_desc(qa + off, 16, 1024, 2), smem_desc(ka + off, 16, 1024, 2), idesc_qk,
-                       k > 0);
-          }
-          mma_commit(bar(B_SFULL0 + s));
-          mma_commit(bar(B_QFREE0 + s));
-          if (last) mma_commit(bar(B_KFREE));
-        }
-        if (pv_pending) {
-          const int u = it - 1, s = u & 1;
-          if (pv_new_row) {
-            if (!mbar_wait(bar(B_VFULL), nv & 1)) { ok = false; break; }
-            ++nv;
-          }
-          if (!mbar_wait(bar(B_PFULL0 + s), (u >> 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t va = sb + kOffV;
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_f16_ts(tmem + 256 + s * 128, tmem + s * 128 + k * 8, smem_desc(va + k * 2048, 16384, 1024, 2),
-                       idesc_pv, k > 0);
-          mma_commit(bar(B_PVDONE0 + s));
-          if (pv_last) mma_commit(bar(B_VFREE));
-        }
-        pv_pending = have;
-        pv_new_row = new_row;
-        pv_last = last;
-        if (have) prev_row = tl.x;
-        have = have2;
+        qv = (have2 && lane < tl2.z) ? p.qlist[tl2.y + lane] : 0;
         tl = tl2;
-        ti = ti2;
-        ++it;
       }
-      if (!ok) flag_timeout(p.hdr);
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = idesc_f16(128, 128, 1, 1, 0, 0);
+        constexpr uint32_t idesc_pv = idesc_f16(128, 128, 1, 1, 0, 1);
+        bool ok = true, pv_pending = false, pv_new = false;
+        int pv_seg = 0, seg = -1, nk = 0;
+        for (int it = 0;; ++it) {
+          // ------------------------------------------------ S = Q K^T for tile it
+          const int slot = it % kRing;
+          if (!(ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1))) break;
+          const int count = ring[slot].count, flags = ring[slot].flags;
+          const bool have = count > 0, new_row = have && (flags & 1);
+          if (have) {
+            const int s = it & 1;
+            // S[s] / P[s] is reused: P V of tile it-2 must have consumed P
+            if (it >= 2 && !(ok = mbar_wait(bar(B_PVDONE0 + s), ((it - 2) >> 1) & 1))) break;
+            if (new_row) {
+              seg = nk++;
+              if (!(ok = mbar_wait(bar(B_KFULL0 + (seg & 1)), (seg >> 1) & 1))) break;
+            }
+            if (!(ok = mbar_wait(bar(B_QFULL0 + s), (it >> 1) & 1))) break;
+            tc_fence_after();
+            const uint32_t qa = sb + (s ? kOffQ1 : kOffQ0), ka = sb + ((seg & 1) ? kOffK1 : kOffK0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+              mma_f16_ss(tmem + s * 128, smem_desc(qa + off, 16, 1024, 2), smem_desc(ka + off, 16, 1024, 2),
+                         idesc_qk, k > 0);
+            }
+            mma_commit(bar(B_SFULL0 + s));
+            mma_commit(bar(B_QFREE0 + s));
+            // a new row: the previous row's K buffer is read no more
+            if (new_row && seg > 0) mma_commit(bar(B_KFREE0 + ((seg - 1) & 1)));
+          }
+          // ------------------------------------------------ O = P V for tile it-1
+          if (pv_pending) {
+            const int u = it - 1, s = u & 1;
+            if (pv_new && !(ok = mbar_wait(bar(B_VFULL0 + (pv_seg & 1)), (pv_seg >> 1) & 1))) break;
+            if (!(ok = mbar_wait(bar(B_PFULL0 + s), (u >> 1) & 1))) break;
+            // O[s] is reused: the output warps must have read O of tile u-2
+            if (u >= 2 && !(ok = mbar_wait(bar(B_OFREE0 + s), ((u - 2) >> 1) & 1))) break;
+            tc_fence_after();
+            const uint32_t va = sb + ((pv_seg & 1) ? kOffV1 : kOffV0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_f16_ts(tmem + 256 + s * 128, tmem + s * 128 + k * 8, smem_desc(va + k * 2048, 16384, 1024, 2),
+                         idesc_pv, k > 0);
+            mma_commit(bar(B_PVDONE0 + s));
+            // a new row: the previous row's V buffer is read no more
+            if (pv_new && pv_seg > 0) mma_commit(bar(B_VFREE0 + ((pv_seg - 1) & 1)));
+          }
+          if (!have) break;
+          pv_pending = true;
+          pv_new = new_row;
+          pv_seg = seg;
+        }
+        if (!ok) flag_timeout(p.hdr);
+      }
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int wg = (warp - 4) >> 2;  // 0 or 1: stage handled
+  } else if (warp < 12) {
+    regs_inc<176>();
+    // ------------------------------------------------------------ softmax
+    const int wg = (warp - 4) >> 2;  // 0 or 1: the stage (tile parity) handled
     const uint32_t bar_id = 1 + wg;
     const int row = 32 * (warp & 3) + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t tS = tmem + lane_base + wg * 128;
-    const uint32_t tO = tmem + lane_base + 256 + wg * 128;
-    const bool elected = (tid == 128 + wg * 128);
-    const uint32_t st_off = wg ? kOffSt1 : kOffSt0;
-    uint8_t* stage = smem + st_off;
-    const uint64_t pol_st = policy_evict_first();
-    if (elected) { tma_prefetch_desc(&tmP128); tma_prefetch_desc(&tmP16); }
-    int ti, it = 0;
-    bool stored_before = false;
-    while (iter.next(&ti)) {
-      if ((it & 1) != wg) { ++it; continue; }
-      const int4 tl = p.tiles[ti];
+    const uint32_t tS = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + wg * 128;
+    const bool neg = p.sl2 < 0.f;  // a negative scale turns the row maximum into a minimum
+    for (int it = wg;; it += 2) {
+      const int slot = it % kRing;
+      bool ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1);
+      if (!named_bar_and(bar_id, 128, ok)) { flag_timeout(p.hdr); break; }
+      const int count = ring[slot].count;
+      if (count == 0) break;
       const int j = row >> 4;
-      const bool valid = j < tl.z;
-      const int qi = valid ? p.qlist[tl.y + j] : 0;
-      const int b = tl.x % p.nblocks;
-      const int lim = (p.Lkv - p.N + qi) - b * kBlock;  // keys c <= lim visible
+      const bool valid = j < count;
+      const int qi = valid ? ring[slot].q[j] : 0;
+      const int first = ring[slot].first;
+      const int b = ring[slot].row % p.nblocks;
+      // keys c <= lim are visible; only rows whose own block is b are masked
+      const int lim = valid ? (p.Lkv - p.N + qi) - b * kBlock : kBlock - 1;
+      // The branch below contains warp-collective tcgen05.st: take it warp-uniformly
+      // (a row with lim >= 127 is unaffected by the masked path).
+      const bool masked = __any_sync(0xffffffffu, lim < kBlock - 1);
 
-      bool ok = mbar_wait(bar(B_SFULL0 + wg), (it >> 1) & 1);
+      ok = mbar_wait(bar(B_SFULL0 + wg), (it >> 1) & 1);
       if (!named_bar_and(bar_id, 128, ok)) { flag_timeout(p.hdr); break; }
       tc_fence_after();
-
-      // pass 1: row maximum of s * scale * log2(e) over visible keys
-      float m2 = -FLT_MAX;
+      uint32_t v[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + c * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (c * 32 + e <= lim) m2 = fmaxf(m2, __uint_as_float(v[e]) * p.sl2);
-      }
-      // pass 2: P = 2^(s*sl2 - m2), row sum, P as bf16 pairs over the S columns
-      float l = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32], pk[16];
-        tmem_ld32(tS + c * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = (c * 32 + e <= lim) ? ex2(fmaf(__uint_as_float(v[e]), p.sl2, -m2)) : 0.f;
-          const float p1 = (c * 32 + e + 1 <= lim) ? ex2(fmaf(__uint_as_float(v[e + 1]), p.sl2, -m2)) : 0.f;
-          l += p0 + p1;
-          pk[e >> 1] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tS + c * 16, pk);
-      }
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+      tmem_ld_wait();
+      float2 ml;
+      if (neg) ml = softmax_row_any_scale(v, lim, p.sl2, tS);
+      else if (masked) ml = softmax_row<true>(v, lim, p.sl2, tS);
+      else ml = softmax_row<false>(v, lim, p.sl2, tS);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL0 + wg));
-      if (valid) p.plse[static_cast<size_t>(tl.y) * kGroup + row] = m2 + lg2(l);
-      const float linv = 1.f / l;
-
-      // epilogue: wait for O = P V, normalise, bf16, swizzled staging, TMA store
-      ok = mbar_wait(bar(B_PVDONE0 + wg), (it >> 1) & 1);
-      if (elected && stored_before) bulk_wait_read0();
+      if (valid) p.pstat[static_cast<size_t>(first) * kGroup + row] = ml;
+    }
+  } else {
+    regs_dec<104>();
+    // ------------------------------------------------------------ output (raw O -> bf16 -> TMA store)
+    const uint32_t bar_id = 3;
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const bool elected = (tid == 384);
+    uint8_t* stage = smem + kOffSt;
+    const uint64_t pol_st = policy_evict_first();
+    if (elected) { tma_prefetch_desc(&tmP128); tma_prefetch_desc(&tmP16); }
+    bool stored_before = false;
+    for (int it = 0;; ++it) {
+      const int slot = it % kRing;
+      bool ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1);
       if (!named_bar_and(bar_id, 128, ok)) { flag_timeout(p.hdr); break; }
+      const int count = ring[slot].count, first = ring[slot].first;
+      if (count == 0) break;
+      const int s = it & 1;
+      ok = mbar_wait(bar(B_PVDONE0 + s), (it >> 1) & 1);
+      if (elected && stored_before) bulk_wait_read0();  // staging free again
+      if (!named_bar_and(bar_id, 128, ok)) { flag_timeout(p.hdr); break; }
+      // every thread has read the ring entry before the barrier above: release the slot
+      if (elected) mbar_arrive(bar(B_TEMPTY0 + slot));
       tc_fence_after();
+      const uint32_t tO = tmem + lane_base + 256 + s * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
@@ -301,32 +473,32 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int q = 0; q < 4; ++q) {
           const int ch = c * 4 + q;
           uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * linv, __uint_as_float(v[q * 8 + 1]) * linv);
-          w.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * linv, __uint_as_float(v[q * 8 + 3]) * linv);
-          w.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * linv, __uint_as_float(v[q * 8 + 5]) * linv);
-          w.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * linv, __uint_as_float(v[q * 8 + 7]) * linv);
+          w.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]), __uint_as_float(v[q * 8 + 1]));
+          w.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]), __uint_as_float(v[q * 8 + 3]));
+          w.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]), __uint_as_float(v[q * 8 + 5]));
+          w.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]), __uint_as_float(v[q * 8 + 7]));
           const uint32_t off = (ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
           *reinterpret_cast<uint4*>(stage + off) = w;
         }
       }
       tc_fence_before();
+      mbar_arrive(bar(B_OFREE0 + s));
       fence_proxy_async_smem();
       named_bar_sync(bar_id, 128);
       if (elected) {
-        const uint32_t src = sb + st_off;
-        if (tl.z == kTileQ) {
-          tma_store_2d(&tmP128, 0, tl.y * kGroup, src, pol_st);
-          tma_store_2d(&tmP128, 64, tl.y * kGroup, src + 16384, pol_st);
+        const uint32_t src = sb + kOffSt;
+        if (count == kTileQ) {
+          tma_store_2d(&tmP128, 0, first * kGroup, src, pol_st);
+          tma_store_2d(&tmP128, 64, first * kGroup, src + 16384, pol_st);
         } else {
-          for (int q = 0; q < tl.z; ++q) {
-            tma_store_2d(&tmP16, 0, (tl.y + q) * kGroup, src + q * 2048, pol_st);
-            tma_store_2d(&tmP16, 64, (tl.y + q) * kGroup, src + 16384 + q * 2048, pol_st);
+          for (int q = 0; q < count; ++q) {
+            tma_store_2d(&tmP16, 0, (first + q) * kGroup, src + q * 2048, pol_st);
+            tma_store_2d(&tmP16, 64, (first + q) * kGroup, src + 16384 + q * 2048, pol_st);
           }
         }
         bulk_commit();
       }
       stored_before = true;
-      ++it;
     }
     if (elected) bulk_wait_all0();
   }
@@ -334,7 +506,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem, 512);
+  if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
@@ -371,11 +543,9 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   }
   KvParams p;
   p.tiles = s->d.tiles;
-  p.window_tiles = s->d.window_tiles;
   p.qlist = s->d.qlist;
   p.hdr = s->d.hdr;
-  p.plse = s->plse;
-  p.nW = s->nW;
+  p.pstat = s->pstat;
   p.N = s->N;
   p.Lkv = a.Lkv;
   p.nblocks = s->nblocks;
@@ -387,6 +557,9 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  // the chunk counter this launch claims its work from starts at zero
+  cudaError_t e = cudaMemsetAsync(&s->d.hdr->pad[0], 0, sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
   kv_outer_kernel<<<a.num_ctas, kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, tmP128, tmP16, p);
   return cudaGetLastError();
 }

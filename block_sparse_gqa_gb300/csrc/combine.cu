@@ -1,21 +1,23 @@
-// Combine: merge each query's partial outputs by log-sum-exp weighting.
+// Combine: merge each query's partial outputs by their softmax statistics.
 //
 // "Sparse Attention" (dinara-dl), Chapter 5, "Partial outputs and Combine": every
-// selected block of a query yields a partial output and an LSE; combine turns the
-// LSEs into relative weights and merges the partials (not a plain average).
-// "Kernel optimization for MiniMax M3", load/store section: the attention kernel
-// stores partials tile-ordered; combine gathers them through the map
-// (query, kv_head, top-i) -> partial row.  It is bandwidth-bound and tolerant of
-// gather latency.
+// selected block of a query yields a partial output and its softmax statistics;
+// combine turns them into relative weights and merges the partials (not a plain
+// average).  "Kernel optimization for MiniMax M3", load/store section: the
+// attention kernel stores partials tile-ordered and raw (normalisation deferred to
+// combine); combine gathers them through the map (query, kv_head, top-i) ->
+// partial row.  It is bandwidth-bound and tolerant of gather latency.
 //
 // Partial k of (query i, group g, head h) is row 16 * cmap[i, g, k] + h of the
-// bf16 [E*16, 128] slab, already normalised by its own softmax sum, with base-2
-// log-sum-exp lse2_k.  With M = max_k lse2_k and w_k = 2^(lse2_k - M):
-//   O = sum_k w_k O_k / sum_k w_k,   LSE = ln 2 * (M + log2 sum_k w_k).
+// bf16 [E*16, 128] slab: O_k = sum_j 2^(x_j - m_k) V_j over the block's visible keys
+// (x = score * scale * log2 e), with statistics (m_k, l_k = sum_j 2^(x_j - m_k)).
+// With M = max_k m_k and w_k = 2^(m_k - M):
+//   O = sum_k w_k O_k / sum_k w_k l_k,   LSE = ln 2 * (M + log2 sum_k w_k l_k).
 //
 // One CTA of 256 threads per (i, g) unit: thread (h, c) owns head h and output
-// columns [8c, 8c + 8) and gathers 16-byte pieces of each partial row, so a warp
-// reads 512 contiguous bytes per partial.
+// columns [8c, 8c + 8); a warp reads 512 contiguous bytes of each partial.  The
+// statistics and partial loads of all slots are issued together once the combine
+// map is known, so a unit costs two dependent memory round trips.
 #include <cuda_bf16.h>
 
 #include "msa_internal.h"
@@ -37,53 +39,57 @@ __device__ __forceinline__ void acc8(float (&a)[8], const uint4& v, float w) {
 }
 
 __global__ void __launch_bounds__(kThreads)
-combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ partial, const float* __restrict__ plse,
-               int N, int Hkv, int topK, int Hq, __nv_bfloat16* __restrict__ O, float* __restrict__ LSE,
-               const SchedHeader* __restrict__ hdr, int force_path) {
+combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ partial,
+               const float2* __restrict__ pstat, int N, int Hkv, int topK, int Hq,
+               __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, const SchedHeader* __restrict__ hdr,
+               int force_path) {
   const int path = force_path ? force_path : hdr->path;
   if (path != kPathKvOuter) return;
   const int h = threadIdx.x >> 4, c = threadIdx.x & 15;
   const int64_t units = static_cast<int64_t>(N) * Hkv;
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const int32_t* cm = cmap + u * topK;
-    // weights: max and sum of 2^(lse2 - M) over the valid partials
-    float M = -INFINITY;
-    for (int k = 0; k < topK; ++k) {
-      const int pk = __ldg(cm + k);
-      if (pk >= 0) M = fmaxf(M, __ldg(plse + static_cast<int64_t>(pk) * kGroup + h));
-    }
+    float M = -INFINITY, L = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float S = 0.f;
     for (int k0 = 0; k0 < topK; k0 += kKChunk) {
       int pos[kKChunk];
-      float w[kKChunk];
+#pragma unroll
+      for (int k = 0; k < kKChunk; ++k) pos[k] = (k0 + k < topK) ? __ldg(cm + k0 + k) : -1;
+      float2 st[kKChunk];
       uint4 v[kKChunk];
 #pragma unroll
       for (int k = 0; k < kKChunk; ++k) {
-        pos[k] = (k0 + k < topK) ? __ldg(cm + k0 + k) : -1;
-        w[k] = pos[k] >= 0 ? ex2(__ldg(plse + static_cast<int64_t>(pos[k]) * kGroup + h) - M) : 0.f;
+        const int64_t r = static_cast<int64_t>(pos[k]) * kGroup + h;
+        st[k] = pos[k] >= 0 ? __ldg(pstat + r) : make_float2(-INFINITY, 0.f);
+        v[k] = pos[k] >= 0 ? __ldg(partial + r * 16 + c) : make_uint4(0, 0, 0, 0);
       }
+      float Mc = M;
 #pragma unroll
-      for (int k = 0; k < kKChunk; ++k)
-        v[k] = pos[k] >= 0 ? __ldg(partial + (static_cast<int64_t>(pos[k]) * kGroup + h) * 16 + c)
-                           : make_uint4(0, 0, 0, 0);
+      for (int k = 0; k < kKChunk; ++k) Mc = fmaxf(Mc, st[k].x);
+      if (Mc == -INFINITY) continue;  // no partial so far
+      const float r = ex2(M - Mc);     // rescale what earlier chunks accumulated (0 when M = -inf)
+      L *= r;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] *= r;
 #pragma unroll
       for (int k = 0; k < kKChunk; ++k) {
-        S += w[k];
-        acc8(acc, v[k], w[k]);
+        const float w = pos[k] >= 0 ? ex2(st[k].x - Mc) : 0.f;
+        L = fmaf(w, st[k].y, L);
+        acc8(acc, v[k], w);
       }
+      M = Mc;
     }
     const int64_t i = u / Hkv, g = u % Hkv;
     const int64_t orow = i * Hq + g * kGroup + h;
     uint4 out;
     float lse;
-    if (S > 0.f) {
-      const float inv = 1.f / S;
+    if (L > 0.f) {
+      const float inv = 1.f / L;
       out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
       out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
       out.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
       out.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-      lse = (M + lg2(S)) * 0.6931471805599453f;
+      lse = (M + lg2(L)) * 0.6931471805599453f;
     } else {
       out = make_uint4(0, 0, 0, 0);
       lse = -INFINITY;
@@ -103,7 +109,7 @@ cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, i
   int64_t grid = sms * 8;
   if (grid > units) grid = units;
   combine_kernel<<<static_cast<int>(grid), kThreads, 0, st>>>(
-      s->d.cmap, static_cast<const uint4*>(s->partial), s->plse, s->N, s->Hkv, s->topK, Hq,
+      s->d.cmap, static_cast<const uint4*>(s->partial), s->pstat, s->N, s->Hkv, s->topK, Hq,
       static_cast<__nv_bfloat16*>(O), LSE, s->d.hdr, force_path);
   return cudaGetLastError();
 }

@@ -66,15 +66,15 @@ msa_status_t ensure_partials(msa_schedule* s, int G) {
   if (s->partial) {
     cudaFree(s->partial);
     s->partial = nullptr;
-    s->plse = nullptr;
+    s->pstat = nullptr;
   }
   const size_t rows = static_cast<size_t>(s->cap_entries) * G;
-  const size_t bytes = align_up(rows * msa::kHeadDim * 2, 256) + rows * sizeof(float);
+  const size_t obytes = align_up(rows * msa::kHeadDim * 2, 256);
   void* p = nullptr;
-  cudaError_t e = cudaMalloc(&p, bytes);
+  cudaError_t e = cudaMalloc(&p, obytes + rows * sizeof(float2));
   if (e != cudaSuccess) return from_cuda(e);
   s->partial = p;
-  s->plse = reinterpret_cast<float*>(static_cast<char*>(p) + align_up(rows * msa::kHeadDim * 2, 256));
+  s->pstat = reinterpret_cast<float2*>(static_cast<char*>(p) + obytes);
   s->partial_G = G;
   return MSA_OK;
 }

@@ -4,7 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/msa.h"
+#include "msa.h"
 
 namespace msa {
 
@@ -58,8 +58,8 @@ struct msa_schedule {
   size_t dev_bytes;
   msa::SchedDev d;
   // partial-output workspace (first forward call)
-  void* partial;       // bf16 [cap_entries * G, D]
-  float* plse;         // fp32 [cap_entries * G] (base-2 log-sum-exp of each partial row)
+  void* partial;       // bf16 [cap_entries * G, D]: raw P V of each (entry, head) row
+  float2* pstat;       // [cap_entries * G]: (m, l) of each partial row, m in base-2 units
   int partial_G;
   cudaStream_t last_stream;
 };

@@ -92,7 +92,7 @@ extern "C" msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int 
   if (opts->path != MSA_PATH_AUTO && opts->path != MSA_PATH_KV_OUTER && opts->path != MSA_PATH_Q_OUTER)
     return MSA_ERR_INVALID_ARG;
 
-  // layout inside the scratch array: schedule arrays, then partial outputs and LSEs
+  // layout inside the scratch array: schedule arrays, then partial outputs and their (m, l)
   msa_schedule s;
   std::memset(&s, 0, sizeof(s));
   msa::schedule_dims(&s, N, Hkv, topK, nblocks);
@@ -100,7 +100,7 @@ extern "C" msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int 
   const size_t rows = static_cast<size_t>(s.cap_entries) * msa::kGroup;
   const size_t sched_bytes = round256(s.dev_bytes);
   const size_t part_bytes = round256(rows * msa::kHeadDim * 2);
-  const size_t total = sched_bytes + part_bytes + rows * sizeof(float);
+  const size_t total = sched_bytes + part_bytes + rows * sizeof(float2);
   if (total > MSA_NOALLOC_SCRATCH_BYTES) return MSA_ERR_CAPACITY;
 
   void* base = nullptr;
@@ -110,7 +110,7 @@ extern "C" msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int 
   msa::carve_schedule(&s, b);
   s.dev_base = b;
   s.partial = b + sched_bytes;
-  s.plse = reinterpret_cast<float*>(b + sched_bytes + part_bytes);
+  s.pstat = reinterpret_cast<float2*>(b + sched_bytes + part_bytes);
   s.partial_G = msa::kGroup;
 
   const cudaStream_t stream = opts->stream;
