@@ -19,20 +19,27 @@
 //
 // Warp roles (512 threads = 4 warpgroups, one CTA per SM; a warp reaches TMEM
 // lanes 32 * (warp % 4) .. + 31, so a warpgroup covers all 128 rows):
-//   warp 0       producer, all 32 lanes: claims chunks, reads each tile's info and
-//                query ids (lane j <-> query j, one tile ahead), publishes them in a
-//                shared-memory ring for the other roles, issues the Q box loads (TMA,
-//                lane j loads query j's two 64-column halves) and, on a row change,
-//                K_b / V_b into the next of two K/V buffers
+//   warp 0       scheduler, all 32 lanes: claims chunks, reads the next chunk's
+//                tile info and query ids ahead of time and publishes each tile in a
+//                shared-memory ring for the other roles (it only waits for ring slots)
+//   warp 2       K/V loader: on a row change loads K_b into the next of two K
+//                buffers and V_b into the V buffer (TMA); a ring slot is reused only
+//                after both this warp and the output warps have released it
 //   warp 1       TMEM allocation (512 columns: S[0], S[1], O[0], O[1]) and MMA
 //                issue: S[s] = Q K^T (tcgen05, smem x smem), then O[s] = P V with P
 //                read from TMEM (it overwrites S[s] in place)
-//   warps 4-7    softmax of even tiles (stage 0)
-//   warps 8-11   softmax of odd tiles  (stage 1)
+//   warps 4-7    softmax of even tiles (TMEM stage 0)
+//   warps 8-11   softmax of odd tiles  (TMEM stage 1); after tile it, a softmax
+//                warpgroup gathers Q of tile it + 3 into Q stage it % 3 (three
+//                stages): 16-byte cp.async copies of the 8 query boxes (contiguous
+//                4 KB of G x D each) straight into the 128-byte-swizzled MMA layout,
+//                completion signalled by cp.async.mbarrier.arrive.noinc.  Small
+//                boxes are slow through the TMA unit, which keeps the large K/V
+//                loads and the output stores.
 //   warps 12-15  output: O[s] -> bf16 -> swizzled staging -> TMA store
-// Registers are rebalanced per warpgroup with setmaxnreg: 56 for the control
+// Registers are rebalanced per warpgroup with setmaxnreg: 64 for the control
 // warpgroup, 176 for the softmax warpgroups (a row's 128 scores stay in registers),
-// 104 for the output warpgroup: 128*56 + 256*176 + 128*104 = 65536, the block's
+// 96 for the output warpgroup: 128*64 + 256*176 + 128*96 = 65536, the block's
 // launch allocation (512 x 128), so every increase can be granted.
 // A softmax thread owns one MMA row (TMEM lane): row maximum m (base-2 units,
 // scale folded in), P = 2^(s*scale*log2e - m) written back over S as bf16 pairs,
@@ -41,6 +48,8 @@
 // Partial layout: raw bf16 [E*16, 128] (row = 16*CSR position + head-in-group;
 // O_k = sum_j P_j V_j, not yet divided by l) and float2 (m, l) [E*16].
 #include <cfloat>
+
+#include <cuda_bf16.h>
 
 #include "msa_internal.h"
 #include "ptx.cuh"
@@ -52,16 +61,17 @@ constexpr int kThreads = 512;
 constexpr int kChunkTiles = 8;  // tiles per claimed chunk
 constexpr int kRing = 8;        // tile-info ring slots
 constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one Q / K / V / staging tile (two 16 KB halves)
-constexpr uint32_t kOffQ0 = 0, kOffQ1 = 32768, kOffK0 = 65536, kOffV0 = 98304, kOffK1 = 131072, kOffV1 = 163840,
+constexpr int kQStages = 3;
+constexpr uint32_t kOffQ = 0 /* + 32 KB * stage */, kOffK0 = 98304, kOffK1 = 131072, kOffV = 163840,
                    kOffSt = 196608, kOffCtl = 229376;
 constexpr uint32_t kCtlBytes = 1024;
 constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + alignment slack
 
 // barrier slots (8 bytes each) at the start of the control area
 enum {
-  B_QFULL0 = 0, B_QFREE0 = 2, B_KFULL0 = 4, B_KFREE0 = 6, B_VFULL0 = 8, B_VFREE0 = 10,
-  B_SFULL0 = 12, B_PFULL0 = 14, B_PVDONE0 = 16, B_OFREE0 = 18, B_TFULL0 = 20, B_TEMPTY0 = 20 + kRing,
-  B_COUNT = 20 + 2 * kRing
+  B_QFULL0 = 0, B_KFULL0 = 3, B_KFREE0 = 5, B_VFULL = 7, B_VFREE = 8,
+  B_SFULL0 = 9, B_PFULL0 = 11, B_PVDONE0 = 13, B_OFREE0 = 15, B_TFULL0 = 17, B_TEMPTY0 = 17 + kRing,
+  B_COUNT = 17 + 2 * kRing
 };
 constexpr uint32_t kOffTmemSlot = 8 * B_COUNT;  // 4 bytes
 constexpr uint32_t kOffRing = 512;              // kRing entries of 64 bytes
@@ -77,6 +87,8 @@ struct TileInfo {
 static_assert(sizeof(TileInfo) == 64, "ring entry");
 
 struct KvParams {
+  const __nv_bfloat16* Q;
+  int Hq;
   const int4* tiles;
   const int32_t* qlist;
   SchedHeader* hdr;
@@ -111,6 +123,14 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
 }
 __device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// the barrier receives one arrive when all of this thread's earlier cp.async copies have landed
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 template <uint32_t N>
@@ -203,18 +223,17 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // zero the Q stages once so rows of a partly filled tile never hold NaN patterns
-  for (uint32_t o = tid * 16; o < 2 * kTileBytes; o += kThreads * 16)
-    *reinterpret_cast<uint4*>(smem + kOffQ0 + o) = make_uint4(0, 0, 0, 0);
+  for (uint32_t o = tid * 16; o < kQStages * kTileBytes; o += kThreads * 16)
+    *reinterpret_cast<uint4*>(smem + kOffQ + o) = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
 
   if (tid == 0) {
+    for (int s = 0; s < kQStages; ++s) mbar_init(bar(B_QFULL0 + s), 128);  // one cp.async arrive per gather thread
+    mbar_init(bar(B_VFULL), 1);
+    mbar_init(bar(B_VFREE), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_QFULL0 + s), 1);
-      mbar_init(bar(B_QFREE0 + s), 1);
       mbar_init(bar(B_KFULL0 + s), 1);
       mbar_init(bar(B_KFREE0 + s), 1);
-      mbar_init(bar(B_VFULL0 + s), 1);
-      mbar_init(bar(B_VFREE0 + s), 1);
       mbar_init(bar(B_SFULL0 + s), 1);
       mbar_init(bar(B_PFULL0 + s), 128);
       mbar_init(bar(B_PVDONE0 + s), 1);
@@ -222,7 +241,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(bar(B_TFULL0 + r), 1);
-      mbar_init(bar(B_TEMPTY0 + r), 1);
+      mbar_init(bar(B_TEMPTY0 + r), 2);  // released by the output warps and the K/V loader
     }
     mbar_fence_init();
   }
@@ -236,43 +255,49 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    regs_dec<56>();
+    regs_dec<64>();
     if (warp == 0) {
       // ---------------------------------------------------------- producer (whole warp)
-      if (lane == 0) { tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); }
-      const uint64_t pol_q = policy_evict_normal(), pol_kv = policy_evict_last();
       int* counter = &p.hdr->pad[0];
       const int T = p.hdr->ntiles;
-      // tiles come in chunks of kChunkTiles; the next chunk is claimed one chunk ahead
-      int chunk = 0, next_chunk = 0;
-      if (lane == 0) {
-        chunk = atomicAdd(counter, 1);
-        next_chunk = atomicAdd(counter, 1);
-      }
-      chunk = __shfl_sync(0xffffffffu, chunk, 0);
-      next_chunk = __shfl_sync(0xffffffffu, next_chunk, 0);
-      int ti = chunk * kChunkTiles, tend = min(ti + kChunkTiles, T);
-      if (ti >= T) ti = T;
-      auto advance = [&]() {  // ti -> the next tile index, or T when no work is left
-        if (++ti < tend) return;
-        chunk = next_chunk;
-        int nc = 0;
-        if (lane == 0 && chunk * kChunkTiles < T) nc = atomicAdd(counter, 1);
-        next_chunk = __shfl_sync(0xffffffffu, nc, 0);
-        ti = chunk * kChunkTiles;
-        tend = min(ti + kChunkTiles, T);
-        if (ti >= T) ti = T;
+      const unsigned full = 0xffffffffu;
+      // Metadata of a chunk, spread over the warp: lane k < 8 holds tile k's
+      // (row, first, count, -) in `tile`; lane j holds the id of query (j % 8) of
+      // tile j / 8 in qa and of tile j / 8 + 4 in qb.  Loaded one chunk ahead.
+      struct Meta {
+        int4 tile;
+        int qa, qb, n;
       };
-      int4 tl = ti < T ? p.tiles[ti] : make_int4(0, 0, 0, 0);
-      int qv = (ti < T && lane < tl.z) ? p.qlist[tl.y + lane] : 0;
-      int prev_row = -1, nk = 0;
-      bool ok = true;
+      auto load_tiles = [&](int c, Meta& m) {
+        const int base = c * kChunkTiles;
+        m.n = base < T ? min(kChunkTiles, T - base) : 0;
+        m.tile = lane < m.n ? p.tiles[base + lane] : make_int4(0, 0, 0, 0);
+      };
+      auto load_ids = [&](Meta& m) {
+        const int t0 = lane >> 3, j = lane & 7;
+        const int f0 = __shfl_sync(full, m.tile.y, t0), n0 = __shfl_sync(full, m.tile.z, t0);
+        const int f1 = __shfl_sync(full, m.tile.y, t0 + 4), n1 = __shfl_sync(full, m.tile.z, t0 + 4);
+        m.qa = j < n0 ? p.qlist[f0 + j] : 0;
+        m.qb = j < n1 ? p.qlist[f1 + j] : 0;
+      };
+      int c_cur = 0, c_next = 0, c_claim = 0;
+      if (lane == 0) {
+        c_cur = atomicAdd(counter, 1);
+        c_next = atomicAdd(counter, 1);
+        c_claim = atomicAdd(counter, 1);
+      }
+      c_cur = __shfl_sync(full, c_cur, 0);
+      c_next = __shfl_sync(full, c_next, 0);
+      Meta cur, nxt;
+      load_tiles(c_cur, cur);
+      load_ids(cur);
+      load_tiles(c_next, nxt);
       // writes ring entry `it` (count 0 marks the end of the work); false on timeout
       auto publish = [&](int it, int row, int first, int count, int flags, int q) -> bool {
         const int slot = it % kRing;
         bool w = true;
         if (lane == 0) w = mbar_wait(bar(B_TEMPTY0 + slot), ((it / kRing) & 1) ^ 1);
-        if (!__shfl_sync(0xffffffffu, w, 0)) return false;
+        if (!__shfl_sync(full, w, 0)) return false;
         if (lane < kTileQ) ring[slot].q[lane] = q;
         if (lane == 0) {
           ring[slot].row = row;
@@ -284,60 +309,39 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (lane == 0) mbar_arrive(bar(B_TFULL0 + slot));
         return true;
       };
-      for (int it = 0;; ++it) {
-        const bool have = ti < T;
-        if (!have) {
-          // two end markers: the softmax warpgroups read alternate entries
-          if (!publish(it, 0, 0, 0, 0, 0) || !publish(it + 1, 0, 0, 0, 0, 0))
-            if (lane == 0) flag_timeout(p.hdr);
+      int it = 0, prev_row = -1, nk = 0;
+      bool ok = true;
+      while (ok) {
+        if (cur.n == 0) {
+          // three end markers: the softmax warpgroups read alternate entries and
+          // gather Q up to three entries ahead of the tile they finished last
+          for (int e = 0; e < 3 && ok; ++e) ok = publish(it + e, 0, 0, 0, 0, 0);
           break;
         }
-        const bool new_row = tl.x != prev_row;
-        const int kb = new_row ? (nk & 1) : ((nk - 1) & 1);
-        if (!publish(it, tl.x, tl.y, tl.z, (new_row ? 1 : 0) | (kb << 8), qv)) {
-          if (lane == 0) flag_timeout(p.hdr);
-          break;
-        }
-        // the tile after this one: its info now, its query ids at the end of the iteration
-        advance();
-        const bool have2 = ti < T;
-        const int4 tl2 = have2 ? p.tiles[ti] : make_int4(0, 0, 0, 0);
-        const int s = it & 1;
-        const int g = tl.x / p.nblocks, b = tl.x - g * p.nblocks;
-        if (lane == 0) {
-          ok = mbar_wait(bar(B_QFREE0 + s), ((it >> 1) & 1) ^ 1);
-          if (ok) mbar_expect_tx(bar(B_QFULL0 + s), static_cast<uint32_t>(tl.z) * 4096u);
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) { if (lane == 0) flag_timeout(p.hdr); break; }
-        if (lane < tl.z) {
-          const uint32_t dq = sb + (s ? kOffQ1 : kOffQ0) + lane * 2048;
-          tma_load_3d(dq, &tmQ, 0, g * kGroup, qv, bar(B_QFULL0 + s), pol_q);
-          tma_load_3d(dq + 16384, &tmQ, 64, g * kGroup, qv, bar(B_QFULL0 + s), pol_q);
-        }
-        if (new_row) {
-          if (lane == 0) {
-            const uint32_t par = ((nk >> 1) & 1) ^ 1;
-            const uint32_t dk = sb + (kb ? kOffK1 : kOffK0), dv = sb + (kb ? kOffV1 : kOffV0);
-            ok = mbar_wait(bar(B_KFREE0 + kb), par);
-            if (ok) {
-              mbar_expect_tx(bar(B_KFULL0 + kb), kTileBytes);
-              tma_load_3d(dk, &tmK, 0, g, b * kBlock, bar(B_KFULL0 + kb), pol_kv);
-              tma_load_3d(dk + 16384, &tmK, 64, g, b * kBlock, bar(B_KFULL0 + kb), pol_kv);
-              ok = mbar_wait(bar(B_VFREE0 + kb), par);
-            }
-            if (ok) {
-              mbar_expect_tx(bar(B_VFULL0 + kb), kTileBytes);
-              tma_load_3d(dv, &tmV, 0, g, b * kBlock, bar(B_VFULL0 + kb), pol_kv);
-              tma_load_3d(dv + 16384, &tmV, 64, g, b * kBlock, bar(B_VFULL0 + kb), pol_kv);
-            }
+        bool ids_next = false;
+        for (int t = 0; t < cur.n; ++t, ++it) {
+          if (t == 3) { load_ids(nxt); ids_next = true; }  // the next chunk's tiles have arrived by now
+          const int row = __shfl_sync(full, cur.tile.x, t);
+          const int first = __shfl_sync(full, cur.tile.y, t);
+          const int count = __shfl_sync(full, cur.tile.z, t);
+          const int qv = __shfl_sync(full, t < 4 ? cur.qa : cur.qb, ((t & 3) << 3) | (lane & 7));
+          const bool new_row = row != prev_row;
+          const int kb = new_row ? (nk & 1) : ((nk - 1) & 1);
+          if (!publish(it, row, first, count, (new_row ? 1 : 0) | (kb << 8), qv)) { ok = false; break; }
+          if (new_row) {
+            ++nk;
+            prev_row = row;
           }
-          if (!__shfl_sync(0xffffffffu, ok, 0)) { if (lane == 0) flag_timeout(p.hdr); break; }
-          ++nk;
-          prev_row = tl.x;
         }
-        qv = (have2 && lane < tl2.z) ? p.qlist[tl2.y + lane] : 0;
-        tl = tl2;
+        if (!ok) break;
+        if (!ids_next) load_ids(nxt);
+        cur = nxt;
+        // claim the chunk after next; the claim made a chunk ago becomes the next one
+        const int claimed = __shfl_sync(full, c_claim, 0);
+        if (lane == 0 && claimed * kChunkTiles < T) c_claim = atomicAdd(counter, 1);
+        load_tiles(claimed, nxt);
       }
+      if (!ok && lane == 0) flag_timeout(p.hdr);
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
       if (lane == 0) {
@@ -359,9 +363,12 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
               seg = nk++;
               if (!(ok = mbar_wait(bar(B_KFULL0 + (seg & 1)), (seg >> 1) & 1))) break;
             }
-            if (!(ok = mbar_wait(bar(B_QFULL0 + s), (it >> 1) & 1))) break;
+            const int qs = it % kQStages;
+            if (!(ok = mbar_wait(bar(B_QFULL0 + qs), (it / kQStages) & 1))) break;
+            // Q was written by cp.async (generic proxy); the MMA reads it through the async proxy
+            fence_proxy_async_smem();
             tc_fence_after();
-            const uint32_t qa = sb + (s ? kOffQ1 : kOffQ0), ka = sb + ((seg & 1) ? kOffK1 : kOffK0);
+            const uint32_t qa = sb + kOffQ + qs * kTileBytes, ka = sb + ((seg & 1) ? kOffK1 : kOffK0);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
@@ -369,31 +376,61 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                          idesc_qk, k > 0);
             }
             mma_commit(bar(B_SFULL0 + s));
-            mma_commit(bar(B_QFREE0 + s));
             // a new row: the previous row's K buffer is read no more
             if (new_row && seg > 0) mma_commit(bar(B_KFREE0 + ((seg - 1) & 1)));
           }
           // ------------------------------------------------ O = P V for tile it-1
           if (pv_pending) {
             const int u = it - 1, s = u & 1;
-            if (pv_new && !(ok = mbar_wait(bar(B_VFULL0 + (pv_seg & 1)), (pv_seg >> 1) & 1))) break;
+            if (pv_new && !(ok = mbar_wait(bar(B_VFULL), pv_seg & 1))) break;
             if (!(ok = mbar_wait(bar(B_PFULL0 + s), (u >> 1) & 1))) break;
             // O[s] is reused: the output warps must have read O of tile u-2
             if (u >= 2 && !(ok = mbar_wait(bar(B_OFREE0 + s), ((u - 2) >> 1) & 1))) break;
             tc_fence_after();
-            const uint32_t va = sb + ((pv_seg & 1) ? kOffV1 : kOffV0);
+            const uint32_t va = sb + kOffV;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               mma_f16_ts(tmem + 256 + s * 128, tmem + s * 128 + k * 8, smem_desc(va + k * 2048, 16384, 1024, 2),
                          idesc_pv, k > 0);
             mma_commit(bar(B_PVDONE0 + s));
-            // a new row: the previous row's V buffer is read no more
-            if (pv_new && pv_seg > 0) mma_commit(bar(B_VFREE0 + ((pv_seg - 1) & 1)));
+            // the next tile starts a new row: this was the last P V reading the V buffer
+            if (new_row) mma_commit(bar(B_VFREE));
           }
           if (!have) break;
           pv_pending = true;
           pv_new = new_row;
           pv_seg = seg;
+        }
+        if (!ok) flag_timeout(p.hdr);
+      }
+    } else if (warp == 2) {
+      // ---------------------------------------------------------- K/V loader
+      if (lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        const uint64_t pol_kv = policy_evict_last();
+        int nk = 0;
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+          const int slot = it % kRing;
+          if (!(ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1))) break;
+          const int count = ring[slot].count, row = ring[slot].row, flags = ring[slot].flags;
+          mbar_arrive(bar(B_TEMPTY0 + slot));
+          if (count == 0) break;
+          if (!(flags & 1)) continue;
+          const int g = row / p.nblocks, b = row - g * p.nblocks, kb = nk & 1;
+          // K: two buffers, buffer kb was last read by the row before the previous one
+          const uint32_t dk = sb + (kb ? kOffK1 : kOffK0);
+          if (!(ok = mbar_wait(bar(B_KFREE0 + kb), ((nk >> 1) & 1) ^ 1))) break;
+          mbar_expect_tx(bar(B_KFULL0 + kb), kTileBytes);
+          tma_load_3d(dk, &tmK, 0, g, b * kBlock, bar(B_KFULL0 + kb), pol_kv);
+          tma_load_3d(dk + 16384, &tmK, 64, g, b * kBlock, bar(B_KFULL0 + kb), pol_kv);
+          // V: one buffer, freed after the previous row's last P V
+          if (!(ok = mbar_wait(bar(B_VFREE), (nk & 1) ^ 1))) break;
+          mbar_expect_tx(bar(B_VFULL), kTileBytes);
+          tma_load_3d(sb + kOffV, &tmV, 0, g, b * kBlock, bar(B_VFULL), pol_kv);
+          tma_load_3d(sb + kOffV + 16384, &tmV, 64, g, b * kBlock, bar(B_VFULL), pol_kv);
+          ++nk;
         }
         if (!ok) flag_timeout(p.hdr);
       }
@@ -406,7 +443,31 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int row = 32 * (warp & 3) + lane;
     const uint32_t tS = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + wg * 128;
     const bool neg = p.sl2 < 0.f;  // a negative scale turns the row maximum into a minimum
-    for (int it = wg;; it += 2) {
+    // Q of tile t >= 0 is gathered by warpgroup (t + 1) % 2: tiles 0, 1, 2 here, tile
+    // it + 3 right after the softmax of tile it.  Returns false on a timed-out wait.
+    const int gtid = tid - 128 - 128 * wg;  // 0..127 within the warpgroup
+    auto gather = [&](int t) -> bool {
+      const int slot = t % kRing;
+      const bool ok = mbar_wait(bar(B_TFULL0 + slot), (t / kRing) & 1);
+      if (!named_bar_and(bar_id, 128, ok)) return false;
+      const int count = ring[slot].count;
+      if (count == 0) return true;
+      const int g = ring[slot].row / p.nblocks;
+      const uint32_t dq = sb + kOffQ + (t % kQStages) * kTileBytes;
+      // chunk c (16 B) of query j, head h: idx = j * 256 + h * 16 + c
+      for (int idx = gtid; idx < count * 256; idx += 128) {
+        const int j = idx >> 8, h = (idx >> 4) & 15, c = idx & 15;
+        const int r = j * 16 + h;  // MMA row
+        const __nv_bfloat16* src =
+            p.Q + (static_cast<size_t>(ring[slot].q[j]) * p.Hq + g * kGroup + h) * kHeadDim + c * 8;
+        cp_async16(dq + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4), src);
+      }
+      cp_async_arrive_noinc(bar(B_QFULL0 + t % kQStages));
+      return true;
+    };
+    bool gok = wg == 0 ? gather(1) : (gather(0) && gather(2));
+    if (!gok) flag_timeout(p.hdr);
+    for (int it = wg; gok; it += 2) {
       const int slot = it % kRing;
       bool ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1);
       if (!named_bar_and(bar_id, 128, ok)) { flag_timeout(p.hdr); break; }
@@ -438,9 +499,10 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_before();
       mbar_arrive(bar(B_PFULL0 + wg));
       if (valid) p.pstat[static_cast<size_t>(first) * kGroup + row] = ml;
+      if (!gather(it + 3)) { flag_timeout(p.hdr); break; }
     }
   } else {
-    regs_dec<104>();
+    regs_dec<96>();
     // ------------------------------------------------------------ output (raw O -> bf16 -> TMA store)
     const uint32_t bar_id = 3;
     const int row = 32 * (warp & 3) + lane;
@@ -542,6 +604,8 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
       return cudaErrorInvalidValue;
   }
   KvParams p;
+  p.Q = static_cast<const __nv_bfloat16*>(a.Q);
+  p.Hq = a.Hq;
   p.tiles = s->d.tiles;
   p.qlist = s->d.qlist;
   p.hdr = s->d.hdr;
