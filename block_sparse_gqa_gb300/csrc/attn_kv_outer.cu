@@ -1,4 +1,4 @@
-// KV-outer (KV-stationary) attention kernel, bf16, tcgen05 + TMA, persistent.
+// KV-outer (KV-stationary) attention kernel, bf16 or fp8 E4M3, tcgen05 + TMA, persistent.
 //
 // "Kernel optimization for MiniMax M3 on NVIDIA Blackwell" (kernel stages): a CTA
 // owns one KV block at a time and attends every query that chose it; because each
@@ -47,6 +47,13 @@
 //
 // Partial layout: raw bf16 [E*16, 128] (row = 16*CSR position + head-in-group;
 // O_k = sum_j P_j V_j, not yet divided by l) and float2 (m, l) [E*16].
+//
+// fp8 E4M3 inputs (per-tensor descales): S = Q K^T runs on kind::f8f6f4 (K-major, one
+// 128-byte swizzle span per row, 32 elements per MMA); q and k descales are folded
+// into the softmax scale.  P V runs in f16: the loader converts each V block from
+// E4M3 to f16 once (exact) into the layout the bf16 path loads by TMA, and P is
+// packed as f16 (more mantissa than bf16 for values in [0, 1]).  The v descale is
+// applied by the combine.
 #include <cfloat>
 
 #include <cuda_bf16.h>
@@ -60,18 +67,30 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kChunkTiles = 8;  // tiles per claimed chunk
 constexpr int kRing = 8;        // tile-info ring slots
-constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one Q / K / V / staging tile (two 16 KB halves)
 constexpr int kQStages = 3;
-constexpr uint32_t kOffQ = 0 /* + 32 KB * stage */, kOffK0 = 98304, kOffK1 = 131072, kOffV = 163840,
-                   kOffSt = 196608, kOffCtl = 229376;
 constexpr uint32_t kCtlBytes = 1024;
-constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + alignment slack
+constexpr uint32_t kTileBytes = 128 * 128 * 2;  // a 16-bit 128 x 128 tile (two 16 KB halves)
+
+// Shared-memory layout per input type (offsets from the 1024-aligned base).
+template <bool kFp8>
+struct Lay {
+  static constexpr uint32_t kInTile = kFp8 ? 16384 : 32768;  // Q or K tile in the input type
+  static constexpr uint32_t kOffQ = 0;                       // + kInTile * stage
+  static constexpr uint32_t kOffK0 = kQStages * kInTile;
+  static constexpr uint32_t kOffK1 = kOffK0 + kInTile;
+  static constexpr uint32_t kOffV = kOffK1 + kInTile;         // 16-bit V (bf16, or f16 from E4M3)
+  static constexpr uint32_t kOffVst = kOffV + kTileBytes;     // E4M3 V as loaded (fp8 only)
+  static constexpr uint32_t kOffSt = kOffVst + (kFp8 ? 16384 : 0);  // output staging
+  static constexpr uint32_t kOffCtl = kOffSt + kTileBytes;
+  static constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + alignment slack
+};
+static_assert(Lay<false>::kSmemBytes <= 232448 && Lay<true>::kSmemBytes <= 232448, "shared memory");
 
 // barrier slots (8 bytes each) at the start of the control area
 enum {
-  B_QFULL0 = 0, B_KFULL0 = 3, B_KFREE0 = 5, B_VFULL = 7, B_VFREE = 8,
-  B_SFULL0 = 9, B_PFULL0 = 11, B_PVDONE0 = 13, B_OFREE0 = 15, B_TFULL0 = 17, B_TEMPTY0 = 17 + kRing,
-  B_COUNT = 17 + 2 * kRing
+  B_QFULL0 = 0, B_KFULL0 = 3, B_KFREE0 = 5, B_VFULL = 7, B_VFREE = 8, B_VSTAGE = 9,
+  B_SFULL0 = 10, B_PFULL0 = 12, B_PVDONE0 = 14, B_OFREE0 = 16, B_TFULL0 = 18, B_TEMPTY0 = 18 + kRing,
+  B_COUNT = 18 + 2 * kRing
 };
 constexpr uint32_t kOffTmemSlot = 8 * B_COUNT;  // 4 bytes
 constexpr uint32_t kOffRing = 512;              // kRing entries of 64 bytes
@@ -87,14 +106,14 @@ struct TileInfo {
 static_assert(sizeof(TileInfo) == 64, "ring entry");
 
 struct KvParams {
-  const __nv_bfloat16* Q;
+  const uint8_t* Q;  // bf16 or E4M3 elements
   int Hq;
   const int4* tiles;
   const int32_t* qlist;
   SchedHeader* hdr;
   float2* pstat;
   int N, Lkv, nblocks;
-  float sl2;  // scale * log2(e)
+  float sl2;  // scale * log2(e) (* q descale * k descale for E4M3)
   int force_path;
 };
 
@@ -133,6 +152,17 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// 16-bit P pair: f16 for the E4M3 path (its P V runs on f16 V), bf16 otherwise
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+  return kF16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
 template <uint32_t N>
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
 template <uint32_t N>
@@ -142,7 +172,7 @@ __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.a
 // Writes P = 2^(v * sl2 - m2) as bf16 pairs over columns [0, 64) of the row's S
 // columns in TMEM and returns (m2, l).  A positive scale is assumed here; a
 // negative one goes through softmax_row_any_scale.
-template <bool kMasked>
+template <bool kMasked, bool kF16>
 __device__ __forceinline__ float2 softmax_row(uint32_t (&v)[128], int lim, float sl2, uint32_t tS) {
   float a0 = -FLT_MAX, a1 = -FLT_MAX, a2 = -FLT_MAX, a3 = -FLT_MAX;
 #pragma unroll
@@ -173,7 +203,7 @@ __device__ __forceinline__ float2 softmax_row(uint32_t (&v)[128], int lim, float
       }
       if ((e >> 1) & 1) s1 = fadd2(s1, pack2(p0, p1));
       else s0 = fadd2(s0, pack2(p0, p1));
-      pk[e >> 1] = pack_bf16x2(p0, p1);
+      pk[e >> 1] = pack_p<kF16>(p0, p1);
     }
     tmem_st16(tS + c * 16, pk);
   }
@@ -184,6 +214,7 @@ __device__ __forceinline__ float2 softmax_row(uint32_t (&v)[128], int lim, float
 }
 
 // Any finite scale: the row extremum of v * sl2 taken directly (slower, rare).
+template <bool kF16>
 __device__ __forceinline__ float2 softmax_row_any_scale(uint32_t (&v)[128], int lim, float sl2, uint32_t tS) {
   float m2 = -FLT_MAX;
   for (int e = 0; e < 128; ++e)
@@ -196,17 +227,19 @@ __device__ __forceinline__ float2 softmax_row_any_scale(uint32_t (&v)[128], int 
       const float p0 = col <= lim ? ex2(fmaf(__uint_as_float(v[col]), sl2, -m2)) : 0.f;
       const float p1 = col + 1 <= lim ? ex2(fmaf(__uint_as_float(v[col + 1]), sl2, -m2)) : 0.f;
       l += p0 + p1;
-      pk[e >> 1] = pack_bf16x2(p0, p1);
+      pk[e >> 1] = pack_p<kF16>(p0, p1);
     }
     tmem_st16(tS + c * 16, pk);
   }
   return make_float2(m2, l);
 }
 
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
-kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmP128,
-                const __grid_constant__ CUtensorMap tmP16, const KvParams p) {
+kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const __grid_constant__ CUtensorMap tmP128, const __grid_constant__ CUtensorMap tmP16,
+                const KvParams p) {
+  using L = Lay<kFp8>;
   const int path = p.force_path ? p.force_path : p.hdr->path;
   if (path != kPathKvOuter) return;
 
@@ -215,22 +248,23 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t pad = (1024u - (raw_u & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw_u + pad;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffCtl);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffCtl + kOffTmemSlot);
-  TileInfo* ring = reinterpret_cast<TileInfo*>(smem + kOffCtl + kOffRing);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffCtl);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffCtl + kOffTmemSlot);
+  TileInfo* ring = reinterpret_cast<TileInfo*>(smem + L::kOffCtl + kOffRing);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // zero the Q stages once so rows of a partly filled tile never hold NaN patterns
-  for (uint32_t o = tid * 16; o < kQStages * kTileBytes; o += kThreads * 16)
-    *reinterpret_cast<uint4*>(smem + kOffQ + o) = make_uint4(0, 0, 0, 0);
+  for (uint32_t o = tid * 16; o < kQStages * L::kInTile; o += kThreads * 16)
+    *reinterpret_cast<uint4*>(smem + L::kOffQ + o) = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
 
   if (tid == 0) {
     for (int s = 0; s < kQStages; ++s) mbar_init(bar(B_QFULL0 + s), 128);  // one cp.async arrive per gather thread
     mbar_init(bar(B_VFULL), 1);
     mbar_init(bar(B_VFREE), 1);
+    mbar_init(bar(B_VSTAGE), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_KFULL0 + s), 1);
       mbar_init(bar(B_KFREE0 + s), 1);
@@ -345,8 +379,9 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
       if (lane == 0) {
-        constexpr uint32_t idesc_qk = idesc_f16(128, 128, 1, 1, 0, 0);
-        constexpr uint32_t idesc_pv = idesc_f16(128, 128, 1, 1, 0, 1);
+        constexpr uint32_t idesc_qk = kFp8 ? idesc_f8(128, 128, 0, 0) : idesc_f16(128, 128, 1, 1, 0, 0);
+        // P V: f16 x f16 for the E4M3 path (V converted to f16), bf16 x bf16 otherwise; V MN-major
+        constexpr uint32_t idesc_pv = kFp8 ? idesc_f16(128, 128, 0, 0, 0, 1) : idesc_f16(128, 128, 1, 1, 0, 1);
         bool ok = true, pv_pending = false, pv_new = false;
         int pv_seg = 0, seg = -1, nk = 0;
         for (int it = 0;; ++it) {
@@ -368,12 +403,20 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // Q was written by cp.async (generic proxy); the MMA reads it through the async proxy
             fence_proxy_async_smem();
             tc_fence_after();
-            const uint32_t qa = sb + kOffQ + qs * kTileBytes, ka = sb + ((seg & 1) ? kOffK1 : kOffK0);
+            const uint32_t qa = sb + L::kOffQ + qs * L::kInTile, ka = sb + ((seg & 1) ? L::kOffK1 : L::kOffK0);
+            if constexpr (kFp8) {
+              // E4M3: K = 128 bytes = one swizzle span, 32 elements per MMA
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-              mma_f16_ss(tmem + s * 128, smem_desc(qa + off, 16, 1024, 2), smem_desc(ka + off, 16, 1024, 2),
-                         idesc_qk, k > 0);
+              for (int k = 0; k < 4; ++k)
+                mma_f8_ss(tmem + s * 128, smem_desc(qa + k * 32, 16, 1024, 2), smem_desc(ka + k * 32, 16, 1024, 2),
+                          idesc_qk, k > 0);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                mma_f16_ss(tmem + s * 128, smem_desc(qa + off, 16, 1024, 2), smem_desc(ka + off, 16, 1024, 2),
+                           idesc_qk, k > 0);
+              }
             }
             mma_commit(bar(B_SFULL0 + s));
             // a new row: the previous row's K buffer is read no more
@@ -387,7 +430,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // O[s] is reused: the output warps must have read O of tile u-2
             if (u >= 2 && !(ok = mbar_wait(bar(B_OFREE0 + s), ((u - 2) >> 1) & 1))) break;
             tc_fence_after();
-            const uint32_t va = sb + kOffV;
+            const uint32_t va = sb + L::kOffV;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               mma_f16_ts(tmem + 256 + s * 128, tmem + s * 128 + k * 8, smem_desc(va + k * 2048, 16384, 1024, 2),
@@ -404,36 +447,87 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (!ok) flag_timeout(p.hdr);
       }
     } else if (warp == 2) {
-      // ---------------------------------------------------------- K/V loader
-      if (lane == 0) {
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-        const uint64_t pol_kv = policy_evict_last();
-        int nk = 0;
-        bool ok = true;
-        for (int it = 0; ok; ++it) {
-          const int slot = it % kRing;
-          if (!(ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1))) break;
-          const int count = ring[slot].count, row = ring[slot].row, flags = ring[slot].flags;
-          mbar_arrive(bar(B_TEMPTY0 + slot));
-          if (count == 0) break;
-          if (!(flags & 1)) continue;
-          const int g = row / p.nblocks, b = row - g * p.nblocks, kb = nk & 1;
-          // K: two buffers, buffer kb was last read by the row before the previous one
-          const uint32_t dk = sb + (kb ? kOffK1 : kOffK0);
-          if (!(ok = mbar_wait(bar(B_KFREE0 + kb), ((nk >> 1) & 1) ^ 1))) break;
-          mbar_expect_tx(bar(B_KFULL0 + kb), kTileBytes);
-          tma_load_3d(dk, &tmK, 0, g, b * kBlock, bar(B_KFULL0 + kb), pol_kv);
-          tma_load_3d(dk + 16384, &tmK, 64, g, b * kBlock, bar(B_KFULL0 + kb), pol_kv);
-          // V: one buffer, freed after the previous row's last P V
-          if (!(ok = mbar_wait(bar(B_VFREE), (nk & 1) ^ 1))) break;
-          mbar_expect_tx(bar(B_VFULL), kTileBytes);
-          tma_load_3d(sb + kOffV, &tmV, 0, g, b * kBlock, bar(B_VFULL), pol_kv);
-          tma_load_3d(sb + kOffV + 16384, &tmV, 64, g, b * kBlock, bar(B_VFULL), pol_kv);
-          ++nk;
+      // ---------------------------------------------------------- K/V loader (lane 0 issues,
+      // the whole warp converts E4M3 V to f16)
+      const unsigned full = 0xffffffffu;
+      if (lane == 0) { tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); }
+      const uint64_t pol_kv = policy_evict_last();
+      int nk = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int slot = it % kRing;
+        int count = 0, row = 0, flags = 0;
+        if (lane == 0) {
+          ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1);
+          if (ok) {
+            count = ring[slot].count;
+            row = ring[slot].row;
+            flags = ring[slot].flags;
+            mbar_arrive(bar(B_TEMPTY0 + slot));
+          }
         }
-        if (!ok) flag_timeout(p.hdr);
+        ok = __shfl_sync(full, ok, 0);
+        count = __shfl_sync(full, count, 0);
+        row = __shfl_sync(full, row, 0);
+        flags = __shfl_sync(full, flags, 0);
+        if (!ok || count == 0) break;
+        if (!(flags & 1)) continue;
+        const int g = row / p.nblocks, b = row - g * p.nblocks, kb = nk & 1;
+        if (lane == 0) {
+          // K: two buffers, buffer kb was last read by the row before the previous one
+          const uint32_t dk = sb + (kb ? L::kOffK1 : L::kOffK0);
+          ok = mbar_wait(bar(B_KFREE0 + kb), ((nk >> 1) & 1) ^ 1);
+          if (ok) {
+            mbar_expect_tx(bar(B_KFULL0 + kb), L::kInTile);
+            tma_load_3d(dk, &tmK, 0, g, b * kBlock, bar(B_KFULL0 + kb), pol_kv);
+            if constexpr (!kFp8) tma_load_3d(dk + 16384, &tmK, 64, g, b * kBlock, bar(B_KFULL0 + kb), pol_kv);
+            if constexpr (kFp8) {
+              // E4M3 V lands in its own staging area at once; the V buffer is filled later
+              mbar_expect_tx(bar(B_VSTAGE), 16384);
+              tma_load_3d(sb + L::kOffVst, &tmV, 0, g, b * kBlock, bar(B_VSTAGE), pol_kv);
+            }
+            // V: one buffer, freed after the previous row's last P V
+            ok = mbar_wait(bar(B_VFREE), (nk & 1) ^ 1);
+            if constexpr (kFp8) {
+              const bool staged = mbar_wait(bar(B_VSTAGE), nk & 1);  // also on failure: no copy left in flight
+              ok = ok && staged;
+            }
+          }
+          if (ok) {
+            if constexpr (!kFp8) {
+              mbar_expect_tx(bar(B_VFULL), kTileBytes);
+              tma_load_3d(sb + L::kOffV, &tmV, 0, g, b * kBlock, bar(B_VFULL), pol_kv);
+              tma_load_3d(sb + L::kOffV + 16384, &tmV, 64, g, b * kBlock, bar(B_VFULL), pol_kv);
+            }
+          }
+        }
+        ok = __shfl_sync(full, ok, 0);
+        if (!ok) break;
+        if constexpr (kFp8) {
+          // E4M3 [128 keys][128 B, swizzled] -> f16 [2 halves][128 keys][128 B, swizzled]:
+          // unit (key k, 16-byte source chunk c) = D columns 16c .. 16c + 15
+          for (int u = lane; u < 128 * 8; u += 32) {
+            const int k = u >> 3, c = u & 7;
+            const uint4 src = *reinterpret_cast<const uint4*>(smem + L::kOffVst + k * 128 + ((c ^ (k & 7)) << 4));
+            const uint32_t w[4] = {src.x, src.y, src.z, src.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * q]) : "h"(static_cast<uint16_t>(w[q] & 0xFFFFu)));
+              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * q + 1]) : "h"(static_cast<uint16_t>(w[q] >> 16)));
+            }
+            const int half = c >> 2, ch = (2 * c) & 7;  // D 16c.. lies in half c/4, 16-byte chunks 2c%8, +1
+            uint8_t* dst = smem + L::kOffV + half * 16384 + k * 128;
+            *reinterpret_cast<uint4*>(dst + ((ch ^ (k & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(dst + (((ch + 1) ^ (k & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+          }
+          fence_proxy_async_smem();  // read next by the tensor cores
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_VFULL));
+        }
+        ++nk;
       }
+      if (!ok && lane == 0) flag_timeout(p.hdr);
     }
   } else if (warp < 12) {
     regs_inc<176>();
@@ -453,14 +547,24 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const int count = ring[slot].count;
       if (count == 0) return true;
       const int g = ring[slot].row / p.nblocks;
-      const uint32_t dq = sb + kOffQ + (t % kQStages) * kTileBytes;
-      // chunk c (16 B) of query j, head h: idx = j * 256 + h * 16 + c
-      for (int idx = gtid; idx < count * 256; idx += 128) {
-        const int j = idx >> 8, h = (idx >> 4) & 15, c = idx & 15;
-        const int r = j * 16 + h;  // MMA row
-        const __nv_bfloat16* src =
-            p.Q + (static_cast<size_t>(ring[slot].q[j]) * p.Hq + g * kGroup + h) * kHeadDim + c * 8;
-        cp_async16(dq + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4), src);
+      const uint32_t dq = sb + L::kOffQ + (t % kQStages) * L::kInTile;
+      if constexpr (kFp8) {
+        // chunk c (16 B = 16 elements) of query j, head h: idx = j * 128 + h * 8 + c
+        for (int idx = gtid; idx < count * 128; idx += 128) {
+          const int j = idx >> 7, h = (idx >> 3) & 15, c = idx & 7;
+          const int r = j * 16 + h;  // MMA row
+          const uint8_t* src = p.Q + (static_cast<size_t>(ring[slot].q[j]) * p.Hq + g * kGroup + h) * kHeadDim + c * 16;
+          cp_async16(dq + r * 128 + ((c ^ (r & 7)) << 4), src);
+        }
+      } else {
+        // chunk c (16 B = 8 elements) of query j, head h: idx = j * 256 + h * 16 + c
+        for (int idx = gtid; idx < count * 256; idx += 128) {
+          const int j = idx >> 8, h = (idx >> 4) & 15, c = idx & 15;
+          const int r = j * 16 + h;  // MMA row
+          const uint8_t* src =
+              p.Q + ((static_cast<size_t>(ring[slot].q[j]) * p.Hq + g * kGroup + h) * kHeadDim + c * 8) * 2;
+          cp_async16(dq + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4), src);
+        }
       }
       cp_async_arrive_noinc(bar(B_QFULL0 + t % kQStages));
       return true;
@@ -492,9 +596,9 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
       tmem_ld_wait();
       float2 ml;
-      if (neg) ml = softmax_row_any_scale(v, lim, p.sl2, tS);
-      else if (masked) ml = softmax_row<true>(v, lim, p.sl2, tS);
-      else ml = softmax_row<false>(v, lim, p.sl2, tS);
+      if (neg) ml = softmax_row_any_scale<kFp8>(v, lim, p.sl2, tS);
+      else if (masked) ml = softmax_row<true, kFp8>(v, lim, p.sl2, tS);
+      else ml = softmax_row<false, kFp8>(v, lim, p.sl2, tS);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL0 + wg));
@@ -508,7 +612,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const bool elected = (tid == 384);
-    uint8_t* stage = smem + kOffSt;
+    uint8_t* stage = smem + L::kOffSt;
     const uint64_t pol_st = policy_evict_first();
     if (elected) { tma_prefetch_desc(&tmP128); tma_prefetch_desc(&tmP16); }
     bool stored_before = false;
@@ -548,7 +652,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       fence_proxy_async_smem();
       named_bar_sync(bar_id, 128);
       if (elected) {
-        const uint32_t src = sb + kOffSt;
+        const uint32_t src = sb + L::kOffSt;
         if (count == kTileQ) {
           tma_store_2d(&tmP128, 0, first * kGroup, src, pol_st);
           tma_store_2d(&tmP128, 64, first * kGroup, src + 16384, pol_st);
@@ -575,21 +679,19 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
 cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   const msa_schedule* s = a.s;
-  CUtensorMap tmQ, tmK, tmV, tmP128, tmP16;
+  const bool fp8 = a.fp8;
+  const uint64_t es = fp8 ? 1 : 2;  // bytes per input element
+  CUtensorMap tmK, tmV, tmP128, tmP16;
   {
-    const uint64_t dims[3] = {kHeadDim, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(s->N)};
-    const uint64_t strides[2] = {kHeadDim * 2, static_cast<uint64_t>(a.Hq) * kHeadDim * 2};
-    const uint32_t box[3] = {64, kGroup, 1};
-    if (!encode_tmap(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
-  {
+    // K / V [Lkv][Hkv][128]: one block of one group per load, 64 elements (bf16) or
+    // 128 elements (E4M3) = 128 bytes per box row
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t dims[3] = {kHeadDim, static_cast<uint64_t>(s->Hkv), static_cast<uint64_t>(a.Lkv)};
-    const uint64_t strides[2] = {kHeadDim * 2, static_cast<uint64_t>(s->Hkv) * kHeadDim * 2};
-    const uint32_t box[3] = {64, 1, kBlock};
-    if (!encode_tmap(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.K, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint64_t strides[2] = {kHeadDim * es, static_cast<uint64_t>(s->Hkv) * kHeadDim * es};
+    const uint32_t box[3] = {fp8 ? 128u : 64u, 1, kBlock};
+    if (!encode_tmap(&tmK, dt, 3, a.K, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-    if (!encode_tmap(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.V, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_tmap(&tmV, dt, 3, a.V, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   {
@@ -604,7 +706,7 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
       return cudaErrorInvalidValue;
   }
   KvParams p;
-  p.Q = static_cast<const __nv_bfloat16*>(a.Q);
+  p.Q = static_cast<const uint8_t*>(a.Q);
   p.Hq = a.Hq;
   p.tiles = s->d.tiles;
   p.qlist = s->d.qlist;
@@ -613,18 +715,23 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   p.N = s->N;
   p.Lkv = a.Lkv;
   p.nblocks = s->nblocks;
-  p.sl2 = a.scale * 1.4426950408889634f;
+  p.sl2 = a.scale * a.qk_descale * 1.4426950408889634f;
   p.force_path = a.force_path;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kv_outer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static bool attr_set[2] = {false, false};
+  const uint32_t smem = fp8 ? Lay<true>::kSmemBytes : Lay<false>::kSmemBytes;
+  if (!attr_set[fp8]) {
+    cudaError_t e = fp8 ? cudaFuncSetAttribute(kv_outer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                        : cudaFuncSetAttribute(kv_outer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[fp8] = true;
   }
   // the chunk counter this launch claims its work from starts at zero
   cudaError_t e = cudaMemsetAsync(&s->d.hdr->pad[0], 0, sizeof(int32_t), st);
   if (e != cudaSuccess) return e;
-  kv_outer_kernel<<<a.num_ctas, kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, tmP128, tmP16, p);
+  if (fp8)
+    kv_outer_kernel<true><<<a.num_ctas, kThreads, smem, st>>>(tmK, tmV, tmP128, tmP16, p);
+  else
+    kv_outer_kernel<false><<<a.num_ctas, kThreads, smem, st>>>(tmK, tmV, tmP128, tmP16, p);
   return cudaGetLastError();
 }
 

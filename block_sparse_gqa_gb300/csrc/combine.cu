@@ -11,6 +11,8 @@
 // Partial k of (query i, group g, head h) is row 16 * cmap[i, g, k] + h of the
 // bf16 [E*16, 128] slab: O_k = sum_j 2^(x_j - m_k) V_j over the block's visible keys
 // (x = score * scale * log2 e), with statistics (m_k, l_k = sum_j 2^(x_j - m_k)).
+// For E4M3 inputs the V descale multiplies the merged output (the partials hold P V
+// of the stored E4M3 values).
 // With M = max_k m_k and w_k = 2^(m_k - M):
 //   O = sum_k w_k O_k / sum_k w_k l_k,   LSE = ln 2 * (M + log2 sum_k w_k l_k).
 //
@@ -41,8 +43,8 @@ __device__ __forceinline__ void acc8(float (&a)[8], const uint4& v, float w) {
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ partial,
                const float2* __restrict__ pstat, int N, int Hkv, int topK, int Hq,
-               __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, const SchedHeader* __restrict__ hdr,
-               int force_path) {
+               __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, float v_descale,
+               const SchedHeader* __restrict__ hdr, int force_path) {
   const int path = force_path ? force_path : hdr->path;
   if (path != kPathKvOuter) return;
   const int h = threadIdx.x >> 4, c = threadIdx.x & 15;
@@ -84,7 +86,7 @@ combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ parti
     uint4 out;
     float lse;
     if (L > 0.f) {
-      const float inv = 1.f / L;
+      const float inv = v_descale / L;
       out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
       out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
       out.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
@@ -101,7 +103,8 @@ combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ parti
 
 }  // namespace
 
-cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, int force_path, cudaStream_t st) {
+cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, float v_descale, int force_path,
+                           cudaStream_t st) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -110,7 +113,7 @@ cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, i
   if (grid > units) grid = units;
   combine_kernel<<<static_cast<int>(grid), kThreads, 0, st>>>(
       s->d.cmap, static_cast<const uint4*>(s->partial), s->pstat, s->N, s->Hkv, s->topK, Hq,
-      static_cast<__nv_bfloat16*>(O), LSE, s->d.hdr, force_path);
+      static_cast<__nv_bfloat16*>(O), LSE, v_descale, s->d.hdr, force_path);
   return cudaGetLastError();
 }
 

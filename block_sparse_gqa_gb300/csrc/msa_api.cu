@@ -203,23 +203,31 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
   if (Q.d != K.d || K.d != V.d) return MSA_ERR_INVALID_ARG;
   if (Q.dtype != K.dtype || K.dtype != V.dtype) return MSA_ERR_UNSUPPORTED;
   if (Q.d != msa::kHeadDim || Q.h / K.h != msa::kGroup) return MSA_ERR_UNSUPPORTED;
-  if (Q.dtype != MSA_BF16) return MSA_ERR_UNSUPPORTED;
+  if (Q.dtype != MSA_BF16 && Q.dtype != MSA_FP8_E4M3) return MSA_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return MSA_ERR_INVALID_ARG;
   if (opts->path != MSA_PATH_AUTO && opts->path != MSA_PATH_KV_OUTER && opts->path != MSA_PATH_Q_OUTER)
     return MSA_ERR_INVALID_ARG;
+  const bool fp8 = Q.dtype == MSA_FP8_E4M3;
+  if (fp8 && !(std::isfinite(opts->q_descale) && std::isfinite(opts->k_descale) && std::isfinite(opts->v_descale) &&
+               opts->q_descale > 0.f && opts->k_descale > 0.f && opts->v_descale > 0.f))
+    return MSA_ERR_INVALID_ARG;
+  if (fp8 && opts->path == MSA_PATH_Q_OUTER) return MSA_ERR_UNSUPPORTED;  // the Q-outer kernel is bf16 only
   msa_status_t st = ensure_partials(s, msa::kGroup);
   if (st != MSA_OK) return st;
-  const int force = opts->path == MSA_PATH_AUTO ? 0 : static_cast<int>(opts->path);
+  // E4M3 inputs always take the KV-outer kernel (the only one with an E4M3 instance)
+  const int force = fp8 ? msa::kPathKvOuter : opts->path == MSA_PATH_AUTO ? 0 : static_cast<int>(opts->path);
+  const float qk_descale = fp8 ? opts->q_descale * opts->k_descale : 1.f;
+  const float v_descale = fp8 ? opts->v_descale : 1.f;
   const cudaStream_t stream = opts->stream;
   int ctas = opts->num_ctas > 0 ? opts->num_ctas : device_sms();
   if (ctas < 1) return MSA_ERR_CUDA;
   const int Hq = static_cast<int>(Q.h);
   cudaError_t e;
   if (opts->stage_events[0] && (e = cudaEventRecord(opts->stage_events[0], stream))) return from_cuda(e);
-  msa::KvOuterArgs a{s, Q.ptr, K.ptr, V.ptr, Hq, s->nblocks * msa::kBlock, scale, force, ctas};
+  msa::KvOuterArgs a{s, Q.ptr, K.ptr, V.ptr, Hq, s->nblocks * msa::kBlock, scale, force, ctas, fp8, qk_descale};
   if ((e = msa::launch_kv_outer(a, stream))) return from_cuda(e);
   if (opts->stage_events[1] && (e = cudaEventRecord(opts->stage_events[1], stream))) return from_cuda(e);
-  if ((e = msa::launch_combine(s, Hq, O, LSE, force, stream))) return from_cuda(e);
+  if ((e = msa::launch_combine(s, Hq, O, LSE, v_descale, force, stream))) return from_cuda(e);
   if ((e = msa::launch_q_outer(s, Q.ptr, K.ptr, V.ptr, Hq, scale, O, LSE, force, stream))) return from_cuda(e);
   if (opts->stage_events[2] && (e = cudaEventRecord(opts->stage_events[2], stream))) return from_cuda(e);
   s->last_stream = stream;

@@ -87,11 +87,13 @@ struct KvOuterArgs {
   float scale;
   int force_path;  // 0 auto, 1 kv, 2 q
   int num_ctas;
+  bool fp8;          // E4M3 inputs
+  float qk_descale;  // q descale * k descale (1 for bf16)
 };
 cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st);
 
 // combine.cu
-cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, int force_path,
+cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, float v_descale, int force_path,
                            cudaStream_t st);
 
 // attn_q_outer.cu

@@ -120,17 +120,20 @@ msa_status_t msa_build_schedule(const int32_t* indices, int N, int Hkv, int topK
  * Combine").  Q-outer path (same page, Q-outer structure): one unit per (query,
  * group) walks its own blocks with an online softmax and writes O and LSE directly.
  *
- * Q: [N, Hq, D]; K, V: [Lkv, Hkv, D]; all bf16, or all MSA_FP8_E4M3 with descales in
- * opts.  O: bf16 [N, Hq, D] device; LSE: fp32 [N, Hq] device (may be NULL).
+ * Q: [N, Hq, D]; K, V: [Lkv, Hkv, D]; all bf16, or all MSA_FP8_E4M3 (one byte per
+ * element, real value = stored value * the tensor's descale in opts; descales must be
+ * finite and > 0).  O: bf16 [N, Hq, D] device; LSE: fp32 [N, Hq] device (may be NULL).
  * scale multiplies q.k (typically 1/sqrt(D)).  opts may be NULL (defaults).
+ * E4M3 inputs always run the KV-outer path (AUTO included): S = Q K^T on E4M3
+ * tensor cores, V widened to f16 on chip, P V in f16, output bf16.
  *
  * The first call for a given head count allocates the partial-output workspace of
  * the schedule (cudaMalloc, synchronous): N*Hkv*topK*G*(2*D + 4) bytes at most.
  * Later calls allocate nothing.
  *
  * Returns MSA_ERR_INVALID_ARG on null pointers or shapes inconsistent with the
- * schedule; MSA_ERR_UNSUPPORTED for D != 128, G != 16 or mixed dtypes;
- * MSA_ERR_CUDA on launch failure.
+ * schedule or non-positive E4M3 descales; MSA_ERR_UNSUPPORTED for D != 128, G != 16,
+ * mixed dtypes, or E4M3 with MSA_PATH_Q_OUTER forced; MSA_ERR_CUDA on launch failure.
  */
 msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, msa_schedule_t s,
                                  void* O, float* LSE, float scale, const msa_fwd_opts_t* opts);
