@@ -41,7 +41,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="m3", choices=["tiny", "m3", "long", "lowreuse"])
+    ap.add_argument("--workload", default="m3", choices=["tiny", "m3", "long", "lowreuse", "fp8"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -234,9 +234,11 @@ def run_ours(args, world, rank, local, pg):
             e.record(stream)  # materialise the CUDA event handle
         return evs
 
+    descales = (wl.q_descale, wl.k_descale, wl.v_descale)
+
     def step(stage):
         msa.build_schedule(idx_d, cfg.nblocks, schedule=sched)
-        msa.sparse_attn_fwd(Q, K, V, sched, scale=cfg.scale, O=O, LSE=LSE,
+        msa.sparse_attn_fwd(Q, K, V, sched, scale=cfg.scale, O=O, LSE=LSE, descales=descales,
                             stage_events=[e.cuda_event for e in stage] if stage else None)
 
     for _ in range(args.warmup):
@@ -263,6 +265,9 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.synchronize()
     barrier(pg)
     clock_info = clocks.stop()
+    after = sched.query()  # the device's sticky flags after the timed steps
+    if after["status"] != 0:
+        raise SystemExit(f"device status {after['status']} after the timed steps (1 bad index, 2 wait timed out)")
 
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     attn_ms = [st[0].elapsed_time(st[1]) for st in stages]
@@ -275,9 +280,10 @@ def run_ours(args, world, rank, local, pg):
     # algorithmic bytes ("Roofline"): attention kernel and whole step
     E, nsb, T = info["entries"], info["nsb"], info["ntiles"]
     G, D = cfg.G, cfg.D
-    q_bytes = cfg.N * cfg.Hq * D * 2
-    kv_bytes = nsb * 2 * 128 * D * 2
-    part_bytes = E * G * (2 * D + 4)
+    es = 1 if cfg.dtype == "e4m3" else 2  # bytes per input element
+    q_bytes = cfg.N * cfg.Hq * D * es
+    kv_bytes = nsb * 2 * 128 * D * es
+    part_bytes = E * G * (2 * D + 8)  # bf16 partial row + float2 (m, l)
     meta_attn = E * 4 + T * 16
     attn_bytes = q_bytes + kv_bytes + part_bytes + meta_attn
     comb_bytes = part_bytes + cfg.N * cfg.Hkv * cfg.topK * 4 + cfg.N * cfg.Hq * (2 * D + 4)
@@ -302,7 +308,7 @@ def run_ours(args, world, rank, local, pg):
             dQ.copy_(hQ, non_blocking=True); dK.copy_(hK, non_blocking=True)
             dV.copy_(hV, non_blocking=True); dI.copy_(hI, non_blocking=True)
             e_sched = msa.build_schedule(dI, cfg.nblocks, schedule=e_sched)
-            msa.sparse_attn_fwd(dQ, dK, dV, e_sched, scale=cfg.scale, O=dO, LSE=dL)
+            msa.sparse_attn_fwd(dQ, dK, dV, e_sched, scale=cfg.scale, O=dO, LSE=dL, descales=descales)
             hO.copy_(dO, non_blocking=True); hL.copy_(dL, non_blocking=True)
 
         for _ in range(max(1, args.warmup)):
@@ -335,9 +341,10 @@ def run_ours(args, world, rank, local, pg):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) Q/K/V, uniform block picks)",
+        "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)" if es == 1 else "bf16",
+        "data": f"synthetic (seeded N(0,1) Q/K/V{', per-tensor E4M3' if es == 1 else ''}, {cfg.picks} block picks)",
         "config": {"workload": f"{cfg.name}: N={cfg.N} Lkv={cfg.Lkv} Hq={cfg.Hq} Hkv={cfg.Hkv} D={cfg.D} block=128 "
-                               f"topK={cfg.topK}, causal, own block + {cfg.topK - 1} uniform earlier blocks",
+                               f"topK={cfg.topK}, causal, own block + up to {cfg.topK - 1} {cfg.picks} earlier blocks",
                    "l2": "flushed (256 MiB write) before every timed step, outside the step events",
                    "parallelism": f"independent problem per GPU x{world}", "path": "kv_outer",
                    "entries": E, "nsb": nsb, "tiles": T},

@@ -128,7 +128,7 @@ msa_status_t msa_build_schedule(const int32_t* indices, int N, int Hkv, int topK
  * tensor cores, V widened to f16 on chip, P V in f16, output bf16.
  *
  * The first call for a given head count allocates the partial-output workspace of
- * the schedule (cudaMalloc, synchronous): N*Hkv*topK*G*(2*D + 4) bytes at most.
+ * the schedule (cudaMalloc, synchronous): N*Hkv*topK*G*(2*D + 8) bytes at most (bf16 rows + float2 (m, l)).
  * Later calls allocate nothing.
  *
  * Returns MSA_ERR_INVALID_ARG on null pointers or shapes inconsistent with the
