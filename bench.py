@@ -32,7 +32,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "sparse-attn fwd useful TFLOP/s and % HBM roofline, M3 shape top16, 1 GB300"
-KERNELS_PER_STEP = 11  # mark, rowscan, scan_rows, seg_reduce, seg_top, seg_down, scatter, tiles, kv_outer, combine, q_outer
+
+
+def kernels_per_step(cfg):
+    """Launches of libmsa kernels in one step: schedule (mark, rowscan, one fused scan or
+    four scan kernels when there are more than 32768 (window, row) segments, scatter,
+    tiles) + kv_outer + combine + q_outer (the two attention kernels not chosen exit at
+    once)."""
+    nseg = -(-cfg.N // 256) * cfg.Hkv * cfg.nblocks
+    return (5 if nseg <= 32768 else 8) + 3
 
 
 def parse_args():
@@ -357,7 +365,7 @@ def run_ours(args, world, rank, local, pg):
         "stage_ms": {"schedule": statistics.mean(sched_ms), "attention": attn_mean,
                      "combine": statistics.mean(comb_ms)},
         "selected_pair_tflops": world * 4.0 * 128 * D * G * E / (ms_per_step * 1e-3) / 1e12,
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": kernels_per_step(cfg) * args.steps,
         "clocks": clock_info,
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -14,13 +14,15 @@
 // that follows is a pure function of the input and rows come out sorted by query.
 //
 // Kernels, in stream order:
-//   mark        bits for every valid entry; bad ids -> sticky status bit
-//   rowscan     per row: exclusive popcount prefix over words, row count, tiles per
-//               (window, row) segment
-//   scan_rows   offsets, E, nsb and the Q-outer / KV-outer decision
-//   seg_*       exclusive scan of the segment tile counts (3 passes)
-//   scatter     qlist, slot, cmap, blist
-//   tiles       the work list, window-major, 8-entry tiles
+//   entries<mark>     one thread per list slot: bits for every valid entry; bad ids ->
+//                     sticky status bit
+//   rowscan           per row: exclusive popcount prefix over words, row count, tiles
+//                     per (window, row) segment
+//   scan_small        one CTA: offsets, E, nsb, the Q-outer / KV-outer decision and the
+//                     exclusive scan of the segment tile counts (at most 32768 segments);
+//                     more segments: scan_rows + seg_reduce / seg_top / seg_down
+//   entries<scatter>  qlist, slot, cmap, blist
+//   tiles             the work list, window-major, 8-entry tiles
 #include "msa_internal.h"
 #include "ptx.cuh"
 
@@ -55,37 +57,69 @@ __device__ int block_exclusive_scan(int v, int* total, int* warp_buf) {
   return prefix + x - v;
 }
 
-// Entry test shared by mark and scatter: slot k of list `lst` (query i, own block
-// lb) is an entry iff 0 <= b <= lb and b did not occur earlier in the list.
-__device__ __forceinline__ int entry_block(const int32_t* lst, int k, int lb, int nblocks, bool* bad) {
-  const int b = lst[k];
-  if (b < -1 || b >= nblocks) {
-    *bad = true;
-    return -1;
-  }
-  if (b < 0 || b > lb) return -1;
-  for (int k2 = 0; k2 < k; ++k2)
-    if (lst[k2] == b) return -1;
-  return b;
-}
+// One thread per list slot; each CTA stages whole lists in shared memory.  Slot k of
+// list (query i, group g) with own block lb is an entry iff its id b satisfies
+// 0 <= b <= lb and b does not occur in an earlier slot of the same list.  Ids >= nblocks
+// or < -1 are errors: ignored, and (mark pass) the sticky status bit is set.
+//   kScatter = false (mark): set bit (row g * nblocks + b, query i) of the bitmask.
+//   kScatter = true: the entry's CSR position p = offsets[row] + (entries of the row
+//   with a smaller query) -> qlist[p] = i, slot[p] = k; every slot gets cmap (p or -1)
+//   and blist (b or -1).
+constexpr int kEntThreads = 256;
 
-__global__ void k_mark(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int C,
-                       uint32_t* __restrict__ mask, SchedHeader* hdr) {
+template <bool kScatter>
+__global__ void __launch_bounds__(kEntThreads)
+k_entries(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int C, int lists_per_cta,
+          uint32_t* __restrict__ mask, const int32_t* __restrict__ rowbase, const int32_t* __restrict__ offsets,
+          int32_t* __restrict__ qlist, int32_t* __restrict__ slot, int32_t* __restrict__ cmap,
+          int32_t* __restrict__ blist, SchedHeader* hdr) {
+  __shared__ int32_t s_idx[kEntThreads];
   const int64_t nl = static_cast<int64_t>(N) * Hkv;
+  const int t = threadIdx.x;
   bool bad = false;
-  for (int64_t L = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; L < nl;
-       L += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int i = static_cast<int>(L / Hkv), g = static_cast<int>(L % Hkv);
-    const int lb = (Lkv - N + i) / kBlock;
-    const int32_t* lst = idx + L * topK;
-    for (int k = 0; k < topK; ++k) {
-      const int b = entry_block(lst, k, lb, nblocks, &bad);
-      if (b < 0) continue;
-      const size_t r = static_cast<size_t>(g) * nblocks + b;
-      atomicOr(&mask[r * C + (i >> 5)], 1u << (i & 31));
+  for (int64_t L0 = static_cast<int64_t>(blockIdx.x) * lists_per_cta; L0 < nl;
+       L0 += static_cast<int64_t>(gridDim.x) * lists_per_cta) {
+    const int64_t e0 = L0 * topK;
+    const int nle = static_cast<int>(min(static_cast<int64_t>(lists_per_cta), nl - L0)) * topK;
+    const int b = t < nle ? idx[e0 + t] : -1;
+    s_idx[t] = b;
+    __syncthreads();
+    if (t < nle) {
+      const int lk = t / topK, k = t - lk * topK;
+      const int64_t L = L0 + lk;
+      const int i = static_cast<int>(L / Hkv), g = static_cast<int>(L % Hkv);
+      const int lb = (Lkv - N + i) / kBlock;
+      bool entry = true;
+      if (b < -1 || b >= nblocks) {
+        bad = true;
+        entry = false;
+      } else if (b < 0 || b > lb) {
+        entry = false;
+      } else {
+        for (int k2 = 0; k2 < k; ++k2)
+          if (s_idx[lk * topK + k2] == b) {
+            entry = false;
+            break;
+          }
+      }
+      const size_t r = static_cast<size_t>(g) * nblocks + (entry ? b : 0);
+      if constexpr (!kScatter) {
+        if (entry) atomicOr(&mask[r * C + (i >> 5)], 1u << (i & 31));
+      } else {
+        int p = -1;
+        if (entry) {
+          const uint32_t word = mask[r * C + (i >> 5)];
+          p = offsets[r] + rowbase[r * (C + 1) + (i >> 5)] + __popc(word & ((1u << (i & 31)) - 1u));
+          qlist[p] = i;
+          slot[p] = k;
+        }
+        cmap[e0 + t] = p;
+        blist[e0 + t] = entry ? b : -1;
+      }
     }
+    __syncthreads();
   }
-  if (bad) atomicOr(&hdr->status, kStatusBadIndex);
+  if (!kScatter && bad) atomicOr(&hdr->status, kStatusBadIndex);
 }
 
 template <int NT>
@@ -145,6 +179,57 @@ __global__ void __launch_bounds__(NT) k_scan_rows(const int32_t* __restrict__ co
     hdr->nsb = nsb;
     // crossover: KV-outer when nsb / N < 2.85, in exact integers
     hdr->path = (static_cast<int64_t>(nsb) * 100 < static_cast<int64_t>(N) * 285) ? kPathKvOuter : kPathQOuter;
+  }
+}
+
+// Rows (as k_scan_rows) and, in the same CTA, the exclusive scan of the per-(window,
+// row) segment tile counts when there are few segments (at most NT * kSmallSegPer).
+constexpr int kSmallSegPer = 32;
+
+template <int NT>
+__global__ void __launch_bounds__(NT) k_scan_small(const int32_t* __restrict__ counts, int R, int N,
+                                                   int32_t* __restrict__ offsets, int32_t* __restrict__ seg,
+                                                   int nseg, int32_t* __restrict__ window_tiles, int nW,
+                                                   SchedHeader* hdr) {
+  __shared__ int warp_buf[32];
+  {
+    const int per = (R + NT - 1) / NT;
+    const int r0 = min(static_cast<int>(threadIdx.x) * per, R), r1 = min(r0 + per, R);
+    int sum = 0, nz = 0;
+    for (int r = r0; r < r1; ++r) {
+      sum += counts[r];
+      nz += counts[r] > 0;
+    }
+    int total, nsb;
+    int run = block_exclusive_scan<NT>(sum, &total, warp_buf);
+    block_exclusive_scan<NT>(nz, &nsb, warp_buf);
+    for (int r = r0; r < r1; ++r) {
+      offsets[r] = run;
+      run += counts[r];
+    }
+    if (threadIdx.x == 0) {
+      offsets[R] = total;
+      hdr->entries = total;
+      hdr->nsb = nsb;
+      hdr->path = (static_cast<int64_t>(nsb) * 100 < static_cast<int64_t>(N) * 285) ? kPathKvOuter : kPathQOuter;
+    }
+  }
+  const int per = (nseg + NT - 1) / NT;
+  const int s0 = min(static_cast<int>(threadIdx.x) * per, nseg), s1 = min(s0 + per, nseg);
+  int sum = 0;
+  for (int q = s0; q < s1; ++q) sum += seg[q];
+  int total;
+  int run = block_exclusive_scan<NT>(sum, &total, warp_buf);
+  for (int q = s0; q < s1; ++q) {
+    const int v = seg[q];
+    seg[q] = run;
+    if (q % R == 0) window_tiles[q / R] = run;
+    run += v;
+  }
+  if (threadIdx.x == 0) {
+    seg[nseg] = total;
+    window_tiles[nW] = total;
+    hdr->ntiles = total;
   }
 }
 
@@ -213,34 +298,6 @@ __global__ void __launch_bounds__(NT) k_seg_down(int32_t* __restrict__ seg, int6
   }
 }
 
-__global__ void k_scatter(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int C,
-                          const uint32_t* __restrict__ mask, const int32_t* __restrict__ rowbase,
-                          const int32_t* __restrict__ offsets, int32_t* __restrict__ qlist,
-                          int32_t* __restrict__ slot, int32_t* __restrict__ cmap, int32_t* __restrict__ blist) {
-  const int64_t nl = static_cast<int64_t>(N) * Hkv;
-  bool bad = false;
-  for (int64_t L = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; L < nl;
-       L += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int i = static_cast<int>(L / Hkv), g = static_cast<int>(L % Hkv);
-    const int lb = (Lkv - N + i) / kBlock;
-    const int32_t* lst = idx + L * topK;
-    for (int k = 0; k < topK; ++k) {
-      const int b = entry_block(lst, k, lb, nblocks, &bad);
-      int p = -1;
-      if (b >= 0) {
-        const size_t r = static_cast<size_t>(g) * nblocks + b;
-        const uint32_t word = mask[r * C + (i >> 5)];
-        const int rank = rowbase[r * (C + 1) + (i >> 5)] + __popc(word & ((1u << (i & 31)) - 1u));
-        p = offsets[r] + rank;
-        qlist[p] = i;
-        slot[p] = k;
-      }
-      cmap[L * topK + k] = p;
-      blist[L * topK + k] = b;
-    }
-  }
-}
-
 __global__ void k_tiles(const int32_t* __restrict__ segoff, int64_t nseg, int R, int C,
                         const int32_t* __restrict__ rowbase, const int32_t* __restrict__ offsets,
                         int4* __restrict__ tiles) {
@@ -272,21 +329,29 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
   const SchedDev& d = s->d;
   const int Lkv = s->nblocks * kBlock;
   const int64_t nl = static_cast<int64_t>(s->N) * s->Hkv;
+  const int lists_per_cta = kEntThreads / s->topK;  // topK <= 64
+  const int ent_grid = grid_for(nl, lists_per_cta, 1 << 20);
   cudaError_t e;
   if ((e = cudaMemsetAsync(d.mask, 0, sizeof(uint32_t) * static_cast<size_t>(s->R) * s->C, st))) return e;
   if ((e = cudaMemsetAsync(d.hdr, 0, sizeof(SchedHeader), st))) return e;
-  k_mark<<<grid_for(nl, 256, 1 << 16), 256, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C,
-                                                      d.mask, d.hdr);
+  k_entries<false><<<ent_grid, kEntThreads, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C,
+                                                      lists_per_cta, d.mask, nullptr, nullptr, nullptr, nullptr,
+                                                      nullptr, nullptr, d.hdr);
   k_rowscan<256><<<grid_for(s->R, 1, 1 << 20), 256, 0, st>>>(d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
                                                              d.segoff);
-  k_scan_rows<1024><<<1, 1024, 0, st>>>(d.counts, s->R, s->N, d.offsets, d.hdr);
-  const int nb = static_cast<int>(s->nseg_blocks);
-  k_seg_reduce<256><<<nb, 256, 0, st>>>(d.segoff, s->nseg, d.seg_sums);
-  k_seg_top<1024><<<1, 1024, 0, st>>>(d.seg_sums, nb, d.segoff, s->nseg, d.window_tiles, s->nW, d.hdr);
-  k_seg_down<256><<<nb, 256, 0, st>>>(d.segoff, s->nseg, d.seg_sums, s->R, d.window_tiles);
-  k_scatter<<<grid_for(nl, 256, 1 << 16), 256, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C,
-                                                         d.mask, d.rowbase, d.offsets, d.qlist, d.slot, d.cmap,
-                                                         d.blist);
+  if (s->nseg <= 1024 * kSmallSegPer) {
+    k_scan_small<1024><<<1, 1024, 0, st>>>(d.counts, s->R, s->N, d.offsets, d.segoff, static_cast<int>(s->nseg),
+                                           d.window_tiles, s->nW, d.hdr);
+  } else {
+    k_scan_rows<1024><<<1, 1024, 0, st>>>(d.counts, s->R, s->N, d.offsets, d.hdr);
+    const int nb = static_cast<int>(s->nseg_blocks);
+    k_seg_reduce<256><<<nb, 256, 0, st>>>(d.segoff, s->nseg, d.seg_sums);
+    k_seg_top<1024><<<1, 1024, 0, st>>>(d.seg_sums, nb, d.segoff, s->nseg, d.window_tiles, s->nW, d.hdr);
+    k_seg_down<256><<<nb, 256, 0, st>>>(d.segoff, s->nseg, d.seg_sums, s->R, d.window_tiles);
+  }
+  k_entries<true><<<ent_grid, kEntThreads, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C,
+                                                     lists_per_cta, d.mask, d.rowbase, d.offsets, d.qlist, d.slot,
+                                                     d.cmap, d.blist, d.hdr);
   k_tiles<<<grid_for(s->nseg, 256, 1 << 16), 256, 0, st>>>(d.segoff, s->nseg, s->R, s->C, d.rowbase, d.offsets,
                                                             d.tiles);
   return cudaGetLastError();
