@@ -16,10 +16,11 @@
 // With M = max_k m_k and w_k = 2^(m_k - M):
 //   O = sum_k w_k O_k / sum_k w_k l_k,   LSE = ln 2 * (M + log2 sum_k w_k l_k).
 //
-// One CTA of 256 threads per (i, g) unit: thread (h, c) owns head h and output
-// columns [8c, 8c + 8); a warp reads 512 contiguous bytes of each partial.  The
-// statistics and partial loads of all slots are issued together once the combine
-// map is known, so a unit costs two dependent memory round trips.
+// One CTA of 256 threads per (i, g) unit at a time: thread (h, c) owns head h and
+// output columns [8c, 8c + 8); a warp reads 512 contiguous bytes of each partial.  The
+// statistics and partial loads of 8 slots are issued together once the combine map is
+// known; 64 registers per thread keep 4 CTAs (32 warps) resident per SM so that enough
+// loads are in flight to cover HBM latency.
 #include <cuda_bf16.h>
 
 #include "msa_internal.h"
@@ -29,7 +30,7 @@ namespace msa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kKChunk = 16;
+constexpr int kKChunk = 8;
 
 __device__ __forceinline__ void acc8(float (&a)[8], const uint4& v, float w) {
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -40,7 +41,7 @@ __device__ __forceinline__ void acc8(float (&a)[8], const uint4& v, float w) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ partial,
                const float2* __restrict__ pstat, int N, int Hkv, int topK, int Hq,
                __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, float v_descale,
@@ -109,7 +110,7 @@ cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, f
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t units = static_cast<int64_t>(s->N) * s->Hkv;
-  int64_t grid = sms * 8;
+  int64_t grid = sms * 16;
   if (grid > units) grid = units;
   combine_kernel<<<static_cast<int>(grid), kThreads, 0, st>>>(
       s->d.cmap, static_cast<const uint4*>(s->partial), s->pstat, s->N, s->Hkv, s->topK, Hq,
