@@ -37,10 +37,11 @@
 //                boxes are slow through the TMA unit, which keeps the large K/V
 //                loads and the output stores.
 //   warps 12-15  output: O[s] -> bf16 -> swizzled staging -> TMA store
-// Registers are rebalanced per warpgroup with setmaxnreg: 64 for the control
-// warpgroup, 176 for the softmax warpgroups (a row's 128 scores stay in registers),
-// 96 for the output warpgroup: 128*64 + 256*176 + 128*96 = 65536, the block's
-// launch allocation (512 x 128), so every increase can be granted.
+// Registers are rebalanced per warpgroup with setmaxnreg: 72 for the control
+// warpgroup (at 64 its scheduler / MMA code spills, which costs 6% of kernel time),
+// 176 for the softmax warpgroups (a row's 128 scores stay in registers), 88 for the
+// output warpgroup: 128*72 + 256*176 + 128*88 = 65536, the block's launch allocation
+// (512 x 128), so every increase can be granted.
 // A softmax thread owns one MMA row (TMEM lane): row maximum m (base-2 units,
 // scale folded in), P = 2^(s*scale*log2e - m) written back over S as bf16 pairs,
 // row sum l; (m, l) go to global as one float2 per row.
@@ -289,7 +290,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    regs_dec<64>();
+    regs_dec<72>();
     if (warp == 0) {
       // ---------------------------------------------------------- producer (whole warp)
       int* counter = &p.hdr->pad[0];
@@ -606,7 +607,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       if (!gather(it + 3)) { flag_timeout(p.hdr); break; }
     }
   } else {
-    regs_dec<96>();
+    regs_dec<88>();
     // ------------------------------------------------------------ output (raw O -> bf16 -> TMA store)
     const uint32_t bar_id = 3;
     const int row = 32 * (warp & 3) + lane;
