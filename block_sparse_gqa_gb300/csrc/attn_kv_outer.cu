@@ -25,9 +25,11 @@
 //   warp 2       K/V loader: on a row change loads K_b into the next of two K
 //                buffers and V_b into the V buffer (TMA); a ring slot is reused only
 //                after both this warp and the output warps have released it
-//   warp 1       TMEM allocation (512 columns: S[0], S[1], O[0], O[1]) and MMA
-//                issue: S[s] = Q K^T (tcgen05, smem x smem), then O[s] = P V with P
-//                read from TMEM (it overwrites S[s] in place)
+//   warp 1       TMEM allocation (512 columns: S[0], S[1], O[0], O[1]) and issue of
+//                S[s] = Q K^T (tcgen05, smem x smem) for tile t into stage s = t % 2
+//   warp 3       issue of O[s] = P V with P read from TMEM (it overwrites S[s] in
+//                place).  Two issuing threads: S of tile t + 1 never waits behind
+//                the P V of tile t (its softmax, or an E4M3 V block being widened)
 //   warps 4-7    softmax of even tiles (TMEM stage 0)
 //   warps 8-11   softmax of odd tiles  (TMEM stage 1); after tile it, a softmax
 //                warpgroup gathers Q of tile it + 3 into Q stage it % 3 (three
@@ -378,72 +380,46 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       }
       if (!ok && lane == 0) flag_timeout(p.hdr);
     } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer
+      // ---------------------------------------------------------- S = Q K^T issuer
       if (lane == 0) {
         constexpr uint32_t idesc_qk = kFp8 ? idesc_f8(128, 128, 0, 0) : idesc_f16(128, 128, 1, 1, 0, 0);
-        // P V: f16 x f16 for the E4M3 path (V converted to f16), bf16 x bf16 otherwise; V MN-major
-        constexpr uint32_t idesc_pv = kFp8 ? idesc_f16(128, 128, 0, 0, 0, 1) : idesc_f16(128, 128, 1, 1, 0, 1);
-        bool ok = true, pv_pending = false, pv_new = false;
-        int pv_seg = 0, seg = -1, nk = 0;
+        bool ok = true;
+        int seg = -1;
         for (int it = 0;; ++it) {
-          // ------------------------------------------------ S = Q K^T for tile it
           const int slot = it % kRing;
           if (!(ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1))) break;
           const int count = ring[slot].count, flags = ring[slot].flags;
-          const bool have = count > 0, new_row = have && (flags & 1);
-          if (have) {
-            const int s = it & 1;
-            // S[s] / P[s] is reused: P V of tile it-2 must have consumed P
-            if (it >= 2 && !(ok = mbar_wait(bar(B_PVDONE0 + s), ((it - 2) >> 1) & 1))) break;
-            if (new_row) {
-              seg = nk++;
-              if (!(ok = mbar_wait(bar(B_KFULL0 + (seg & 1)), (seg >> 1) & 1))) break;
-            }
-            const int qs = it % kQStages;
-            if (!(ok = mbar_wait(bar(B_QFULL0 + qs), (it / kQStages) & 1))) break;
-            // Q was written by cp.async (generic proxy); the MMA reads it through the async proxy
-            fence_proxy_async_smem();
-            tc_fence_after();
-            const uint32_t qa = sb + L::kOffQ + qs * L::kInTile, ka = sb + ((seg & 1) ? L::kOffK1 : L::kOffK0);
-            if constexpr (kFp8) {
-              // E4M3: K = 128 bytes = one swizzle span, 32 elements per MMA
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_f8_ss(tmem + s * 128, smem_desc(qa + k * 32, 16, 1024, 2), smem_desc(ka + k * 32, 16, 1024, 2),
-                          idesc_qk, k > 0);
-            } else {
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                mma_f16_ss(tmem + s * 128, smem_desc(qa + off, 16, 1024, 2), smem_desc(ka + off, 16, 1024, 2),
-                           idesc_qk, k > 0);
-              }
-            }
-            mma_commit(bar(B_SFULL0 + s));
-            // a new row: the previous row's K buffer is read no more
-            if (new_row && seg > 0) mma_commit(bar(B_KFREE0 + ((seg - 1) & 1)));
+          if (count == 0) break;
+          const int s = it & 1;
+          if (flags & 1) {
+            // a new row: the previous row's K buffer is read no more once the S MMAs
+            // issued so far are done
+            if (++seg > 0) mma_commit(bar(B_KFREE0 + ((seg - 1) & 1)));
           }
-          // ------------------------------------------------ O = P V for tile it-1
-          if (pv_pending) {
-            const int u = it - 1, s = u & 1;
-            if (pv_new && !(ok = mbar_wait(bar(B_VFULL), pv_seg & 1))) break;
-            if (!(ok = mbar_wait(bar(B_PFULL0 + s), (u >> 1) & 1))) break;
-            // O[s] is reused: the output warps must have read O of tile u-2
-            if (u >= 2 && !(ok = mbar_wait(bar(B_OFREE0 + s), ((u - 2) >> 1) & 1))) break;
-            tc_fence_after();
-            const uint32_t va = sb + L::kOffV;
+          // S[s] / P[s] is reused: P V of tile it-2 must have consumed P
+          if (it >= 2 && !(ok = mbar_wait(bar(B_PVDONE0 + s), ((it - 2) >> 1) & 1))) break;
+          if ((flags & 1) && !(ok = mbar_wait(bar(B_KFULL0 + (seg & 1)), (seg >> 1) & 1))) break;
+          const int qs = it % kQStages;
+          if (!(ok = mbar_wait(bar(B_QFULL0 + qs), (it / kQStages) & 1))) break;
+          // Q was written by cp.async (generic proxy); the MMA reads it through the async proxy
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t qa = sb + L::kOffQ + qs * L::kInTile, ka = sb + ((seg & 1) ? L::kOffK1 : L::kOffK0);
+          if constexpr (kFp8) {
+            // E4M3: K = 128 bytes = one swizzle span, 32 elements per MMA
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_f16_ts(tmem + 256 + s * 128, tmem + s * 128 + k * 8, smem_desc(va + k * 2048, 16384, 1024, 2),
-                         idesc_pv, k > 0);
-            mma_commit(bar(B_PVDONE0 + s));
-            // the next tile starts a new row: this was the last P V reading the V buffer
-            if (new_row) mma_commit(bar(B_VFREE));
+            for (int k = 0; k < 4; ++k)
+              mma_f8_ss(tmem + s * 128, smem_desc(qa + k * 32, 16, 1024, 2), smem_desc(ka + k * 32, 16, 1024, 2),
+                        idesc_qk, k > 0);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+              mma_f16_ss(tmem + s * 128, smem_desc(qa + off, 16, 1024, 2), smem_desc(ka + off, 16, 1024, 2),
+                         idesc_qk, k > 0);
+            }
           }
-          if (!have) break;
-          pv_pending = true;
-          pv_new = new_row;
-          pv_seg = seg;
+          mma_commit(bar(B_SFULL0 + s));
         }
         if (!ok) flag_timeout(p.hdr);
       }
@@ -529,6 +505,37 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
         ++nk;
       }
       if (!ok && lane == 0) flag_timeout(p.hdr);
+    } else if (warp == 3) {
+      // ---------------------------------------------------------- O = P V issuer
+      if (lane == 0) {
+        // P V: f16 x f16 for the E4M3 path (V converted to f16), bf16 x bf16 otherwise; V MN-major
+        constexpr uint32_t idesc_pv = kFp8 ? idesc_f16(128, 128, 0, 0, 0, 1) : idesc_f16(128, 128, 1, 1, 0, 1);
+        bool ok = true;
+        int vseg = -1;
+        for (int u = 0;; ++u) {
+          const int slot = u % kRing;
+          if (!(ok = mbar_wait(bar(B_TFULL0 + slot), (u / kRing) & 1))) break;
+          const int count = ring[slot].count, flags = ring[slot].flags;
+          if (count == 0) break;
+          const int s = u & 1;
+          if (flags & 1) {
+            // a new row: the V buffer is free once the P V MMAs issued so far are done
+            if (++vseg > 0) mma_commit(bar(B_VFREE));
+            if (!(ok = mbar_wait(bar(B_VFULL), vseg & 1))) break;
+          }
+          if (!(ok = mbar_wait(bar(B_PFULL0 + s), (u >> 1) & 1))) break;
+          // O[s] is reused: the output warps must have read O of tile u-2
+          if (u >= 2 && !(ok = mbar_wait(bar(B_OFREE0 + s), ((u - 2) >> 1) & 1))) break;
+          tc_fence_after();
+          const uint32_t va = sb + L::kOffV;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_f16_ts(tmem + 256 + s * 128, tmem + s * 128 + k * 8, smem_desc(va + k * 2048, 16384, 1024, 2),
+                       idesc_pv, k > 0);
+          mma_commit(bar(B_PVDONE0 + s));
+        }
+        if (!ok) flag_timeout(p.hdr);
+      }
     }
   } else if (warp < 12) {
     regs_inc<176>();
