@@ -1,17 +1,33 @@
-// Q-outer (query-stationary) attention, bf16: the low-reuse fallback.
+// Q-outer (query-stationary) attention, bf16, tcgen05 + TMA: the low-reuse fallback.
 //
 // "Kernel optimization for MiniMax M3 on NVIDIA Blackwell", Q-outer vs KV-outer
-// section: when nsb / N >= 2.85 (few queries share a block) each query walks its
-// own selected blocks; no partial outputs and no combine are needed.
+// section: when nsb / N >= 2.85 (few queries share a block) each query walks its own
+// selected blocks; no partial outputs and no combine are needed.
 //
-// Unit = (query i, group g): the 16 heads of the group form one m16 MMA tile.  A CTA
-// of 4 warps takes a unit; warp w covers keys [32w, 32w + 32) of every selected
-// block, streaming its K/V slices through a two-stage cp.async buffer and keeping an
-// online softmax (running max, running sum, rescaled accumulator) across blocks.
-// The four warps merge their (max, sum, output) at the end of the unit and write O
-// and LSE directly.  Tensor work uses warp-level mma.sync m16n8k16 (bf16 in, fp32
-// accumulate): this path moves ~64 KB of K/V per selected block per unit and is
-// bound by memory, not by the tensor pipe.
+// Unit = (query i, group g): the 16 heads of the group against each selected block
+// of the (deduplicated, causally filtered) list, with an online softmax across the
+// blocks.  The MMAs run transposed so that tcgen05 sees M = 128 (keys, then D) and
+// N = 16 (the heads):
+//   S^T[key][h] = K_b[key][:] . Q[h][:]     (A = K_b, K-major; B = Q, K-major)
+//   O^T[d][h]  += V_b[:][d] . P^T[:][h]     (A = V_b read MN-major; B = P^T, K-major)
+// S^T and the block's O^T live in tensor memory (lane = key or d, column = head).
+//
+// Persistent CTAs of 192 threads, units taken round-robin:
+//   warp 0       TMA producer: Q of each unit (two 2 KB boxes, double-buffered) and
+//                K_b, V_b of every selected block through a ring of six 32 KB slots
+//                (K freed after its S MMA, V after its P V MMA),
+//                one 32 KB box per tensor through a tensor-map view that keeps both
+//                halves of each 256-byte row in one request burst
+//   warp 1       TMEM allocation (64 columns: S[0], S[1], O) and MMA issue: S^T of
+//                item x + 1 is issued before P V of item x (one issuing thread: a second
+//                one lets S run ahead and queue in front of the P V the softmax warps
+//                wait for, which measured slower)
+//   warps 2-5    one warpgroup, thread = key (for S) and = d (for O): per block the
+//                per-head max and sum over the 128 keys (warp shuffles + shared
+//                memory), P^T (bf16) into shared memory in the MMA's B layout, and the
+//                running output o[h] (its column d) rescaled by 2^(m_old - m_new)
+// The causal limit only matters in the query's own block (keys > pos(i) get p = 0).
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "msa_internal.h"
@@ -20,239 +36,370 @@
 namespace msa {
 namespace {
 
-constexpr int kWarps = 4, kThreads = 128;
-constexpr int kStride = 136;                            // bf16 per padded smem row (272 B): conflict-free
-constexpr int kSliceElems = 32 * kStride;               // one 32-key slice
-constexpr int kWarpElems = 2 /*stages*/ * 2 /*K,V*/ * kSliceElems;
-constexpr uint32_t kSmemBytes = kWarps * kWarpElems * 2 + 1024;
+constexpr int kThreads = 192;
+constexpr int kSlots = 6;                // K/V ring: K of item x in slot 2x % 6, V in slot (2x + 1) % 6
+constexpr uint32_t kSlotBytes = 32768;   // one 128 x 128 bf16 block
+constexpr uint32_t kOffKV = 0;
+constexpr uint32_t kOffQ = kSlots * kSlotBytes;  // 2 x 4 KB
+constexpr uint32_t kOffP = kOffQ + 8192;           // 4 KB
+constexpr uint32_t kOffRed = kOffP + 4096;         // [max, sum][2 blocks][16 heads][4 warps] floats
+constexpr uint32_t kOffCtl = kOffRed + 1024;
+constexpr uint32_t kSmemBytes = kOffCtl + 256 + 1024;
+constexpr uint32_t kTmemCols = 64;
 
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                              uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+enum {
+  B_FULL0 = 0, B_EMPTY0 = 6, B_QFULL0 = 12, B_QEMPTY0 = 14, B_SFULL0 = 16, B_SFREE0 = 18, B_PREADY = 20,
+  B_PVDONE = 21, B_COUNT = 22
+};
+static_assert(8 * B_COUNT + 4 <= 256, "control area");
 
 struct QoParams {
-  const __nv_bfloat16* Q;
-  const __nv_bfloat16* K;
-  const __nv_bfloat16* V;
   const int32_t* blist;
   const SchedHeader* hdr;
+  SchedHeader* hdr_w;
   __nv_bfloat16* O;
   float* LSE;
-  int N, Lkv, Hq, Hkv, topK;
-  float sl2;
+  int N, Lkv, Hq, Hkv, topK, nblocks;
+  float sl2;  // scale * log2(e)
   int force_path;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) q_outer_kernel(const QoParams p) {
+__device__ __forceinline__ void flag_timeout(SchedHeader* hdr) { atomicOr(&hdr->status, kStatusTimeout); }
+
+// Valid block ids of unit u's list (topK <= 64), in list order: returns their count;
+// the k-th id is held by lane k % 32 in ids[k / 32] (read it with block_at).
+struct UnitIds {
+  int ids[2];
+};
+__device__ __forceinline__ int unit_blocks(const QoParams& p, int64_t u, int lane, UnitIds& out) {
+  const int32_t* lst = p.blist + u * p.topK;
+  int cnt = 0;
+  out.ids[0] = out.ids[1] = -1;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int k = 32 * c + lane;
+    const int b = k < p.topK ? lst[k] : -1;
+    const unsigned m = __ballot_sync(0xffffffffu, b >= 0);
+    // compaction: the valid id of lane src goes to slot cnt + (valid lanes below src)
+    for (int src = 0; src < 32; ++src) {
+      const int v = __shfl_sync(0xffffffffu, b, src);
+      if ((m >> src) & 1u) {
+        const int dst = cnt + __popc(m & ((1u << src) - 1u));
+        if ((dst & 31) == lane) {
+          if (dst < 32) out.ids[0] = v;
+          else out.ids[1] = v;
+        }
+      }
+    }
+    cnt += __popc(m);
+  }
+  return cnt;
+}
+__device__ __forceinline__ int block_at(const UnitIds& ids, int k) {
+  const int lo = __shfl_sync(0xffffffffu, ids.ids[0], k & 31);
+  const int hi = __shfl_sync(0xffffffffu, ids.ids[1], k & 31);
+  return k < 32 ? lo : hi;
+}
+
+// Reduce 16 per-lane values (one per head) over the 32 lanes of a warp with 16 shuffles:
+// at each step a lane keeps half of its values and receives the partner's partial of
+// that half, so after 5 steps lane l holds the full result for head (l >> 1) % 16.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  float a[8], b[4], c[2];
+  bool up = lane & 16;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float keep = up ? v[j + 8] : v[j], send = up ? v[j] : v[j + 8];
+    a[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+  up = lane & 8;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float keep = up ? a[j + 4] : a[j], send = up ? a[j] : a[j + 4];
+    b[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+  up = lane & 4;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float keep = up ? b[j + 2] : b[j], send = up ? b[j] : b[j + 2];
+    c[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+  up = lane & 2;
+  float d = op(up ? c[1] : c[0], __shfl_xor_sync(0xffffffffu, up ? c[0] : c[1], 2));
+  return op(d, __shfl_xor_sync(0xffffffffu, d, 1));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const QoParams p) {
   const int path = p.force_path ? p.force_path : p.hdr->path;
   if (path != kPathQOuter) return;
+
   extern __shared__ uint8_t smem_raw[];
-  __nv_bfloat16* smem = reinterpret_cast<__nv_bfloat16*>(smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023));
-  __shared__ float s_ml[kWarps][kGroup][2];
-  __shared__ int s_blocks[64];
-  __shared__ int s_nb;
+  const uint32_t raw_u = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_u & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sb = raw_u + pad;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffCtl);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffCtl + 8 * B_COUNT);
+  float* red = reinterpret_cast<float*>(smem + kOffRed);  // [2][4 warps][16 heads]
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  __nv_bfloat16* wbuf = smem + warp * kWarpElems;  // [stage][K|V][32][kStride]
-  const uint32_t wbuf_u = smem_u32(wbuf);
   const int64_t units = static_cast<int64_t>(p.N) * p.Hkv;
 
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    const int i = static_cast<int>(u / p.Hkv), g = static_cast<int>(u % p.Hkv);
-    const int pos = p.Lkv - p.N + i;
-    if (tid == 0) {
-      int nb = 0;
-      for (int k = 0; k < p.topK && nb < 64; ++k) {
-        const int b = p.blist[u * p.topK + k];
-        if (b >= 0) s_blocks[nb++] = b;
-      }
-      s_nb = nb;
+  if (tid == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(bar(B_FULL0 + s), 1);
+      mbar_init(bar(B_EMPTY0 + s), 1);
     }
-    __syncthreads();
-    const int nb = s_nb;
-
-    // Q fragments of the 16 heads (A operand, row-major 16 x 128)
-    uint32_t qa[8][4];
-    {
-      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(p.Q + (static_cast<int64_t>(i) * p.Hq + g * kGroup + gid) * kHeadDim);
-      const uint32_t* q8 = q0 + 8 * kHeadDim / 2;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        qa[kk][0] = __ldg(q0 + kk * 8 + tig);
-        qa[kk][1] = __ldg(q8 + kk * 8 + tig);
-        qa[kk][2] = __ldg(q0 + kk * 8 + 4 + tig);
-        qa[kk][3] = __ldg(q8 + kk * 8 + 4 + tig);
-      }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_QFULL0 + s), 1);
+      mbar_init(bar(B_QEMPTY0 + s), 1);
+      mbar_init(bar(B_SFULL0 + s), 1);
+      mbar_init(bar(B_SFREE0 + s), 128);
     }
-    float o[16][4];
-#pragma unroll
-    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-
-    auto prefetch = [&](int t) {
-      const int b = s_blocks[t];
-      const int st = t & 1;
-      for (int idx = lane; idx < 32 * 16; idx += 32) {
-        const int r = idx >> 4, c = idx & 15;
-        const int64_t key = static_cast<int64_t>(b) * kBlock + warp * 32 + r;
-        const int64_t goff = (key * p.Hkv + g) * kHeadDim + c * 8;
-        const uint32_t soff = ((st * 2) * kSliceElems + r * kStride + c * 8) * 2;
-        cp_async16(wbuf_u + soff, p.K + goff);
-        cp_async16(wbuf_u + soff + kSliceElems * 2, p.V + goff);
-      }
-    };
-    if (nb > 0) prefetch(0);
-    cp_async_commit();
-    for (int t = 0; t < nb; ++t) {
-      if (t + 1 < nb) prefetch(t + 1);
-      cp_async_commit();
-      cp_async_wait1();
-      __syncwarp();
-      const int st = t & 1, b = s_blocks[t];
-      const __nv_bfloat16* sK = wbuf + (st * 2) * kSliceElems;
-      const uint32_t sV_u = wbuf_u + ((st * 2 + 1) * kSliceElems) * 2;
-      // S = Q K^T over this warp's 32 keys (4 n-tiles of 8 keys)
-      float s[4][4];
-#pragma unroll
-      for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-          const uint32_t* kr = reinterpret_cast<const uint32_t*>(sK + (n * 8 + gid) * kStride + kk * 16);
-          mma_bf16_16816(s[n], qa[kk], kr[tig], kr[4 + tig]);
-        }
-      }
-      // scale to base-2 units, mask keys beyond the query's position, online softmax
-      const int key0 = b * kBlock + warp * 32;
-      float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-      for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int key = key0 + n * 8 + 2 * tig + (e & 1);
-          s[n][e] = key <= pos ? s[n][e] * p.sl2 : -INFINITY;
-          mx[e >> 1] = fmaxf(mx[e >> 1], s[n][e]);
-        }
-      float alpha[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-        const float mnew = fmaxf(mrow[r], mx[r]);
-        alpha[r] = (mnew == -INFINITY) ? 1.f : ex2(mrow[r] - mnew);
-        mrow[r] = mnew;
-        lrow[r] *= alpha[r];
-      }
-#pragma unroll
-      for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float v = s[n][e] == -INFINITY ? 0.f : ex2(s[n][e] - mrow[e >> 1]);
-          s[n][e] = v;
-          lrow[e >> 1] += v;
-        }
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        o[n][0] *= alpha[0]; o[n][1] *= alpha[0];
-        o[n][2] *= alpha[1]; o[n][3] *= alpha[1];
-      }
-      // O += P V: two k-steps of 16 keys
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        uint32_t pa[4];
-        pa[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-        pa[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-        pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-        pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-        const int mat = lane >> 3, rr = lane & 7;
-        const int krow = kk * 16 + (mat & 1) * 8 + rr;
-#pragma unroll
-        for (int n = 0; n < 16; n += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_trans(sV_u + (krow * kStride + (n + (mat >> 1)) * 8) * 2, b0, b1, b2, b3);
-          mma_bf16_16816(o[n], pa, b0, b1);
-          mma_bf16_16816(o[n + 1], pa, b2, b3);
-        }
-      }
-      __syncwarp();
-    }
-    cp_async_wait0();
-    // row sums over the four lanes that share a row
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-      lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-    }
-    __syncthreads();  // every warp is done with its buffers
-    if (tig == 0) {
-      s_ml[warp][gid][0] = mrow[0]; s_ml[warp][gid][1] = lrow[0];
-      s_ml[warp][gid + 8][0] = mrow[1]; s_ml[warp][gid + 8][1] = lrow[1];
-    }
-    __syncthreads();
-    float* red = reinterpret_cast<float*>(wbuf);  // this warp's scaled output, fp32 [16][128]
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int row = gid + 8 * r;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w][row][0]);
-      float L = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w)
-        if (s_ml[w][row][0] != -INFINITY) L += s_ml[w][row][1] * ex2(s_ml[w][row][0] - M);
-      const float fac = (L > 0.f && mrow[r] != -INFINITY) ? ex2(mrow[r] - M) / L : 0.f;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        red[row * 128 + n * 8 + 2 * tig] = o[n][2 * r] * fac;
-        red[row * 128 + n * 8 + 2 * tig + 1] = o[n][2 * r + 1] * fac;
-      }
-      if (warp == 0 && tig == 0 && p.LSE)
-        p.LSE[static_cast<int64_t>(i) * p.Hq + g * kGroup + row] =
-            L > 0.f ? (M + lg2(L)) * 0.6931471805599453f : -INFINITY;
-    }
-    __syncthreads();
-    // sum the four warps' scaled outputs: thread handles 16 consecutive outputs
-    {
-      const int idx0 = tid * 16;
-      const int row = idx0 >> 7, col = idx0 & 127;
-      float acc[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float* rw = reinterpret_cast<const float*>(smem + w * kWarpElems) + row * 128 + col;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] += rw[e];
-      }
-      uint4 out[2];
-      out[0].x = pack_bf16x2(acc[0], acc[1]);   out[0].y = pack_bf16x2(acc[2], acc[3]);
-      out[0].z = pack_bf16x2(acc[4], acc[5]);   out[0].w = pack_bf16x2(acc[6], acc[7]);
-      out[1].x = pack_bf16x2(acc[8], acc[9]);   out[1].y = pack_bf16x2(acc[10], acc[11]);
-      out[1].z = pack_bf16x2(acc[12], acc[13]); out[1].w = pack_bf16x2(acc[14], acc[15]);
-      uint4* dst = reinterpret_cast<uint4*>(p.O + (static_cast<int64_t>(i) * p.Hq + g * kGroup + row) * kHeadDim + col);
-      dst[0] = out[0];
-      dst[1] = out[1];
-    }
-    __syncthreads();  // buffers and s_blocks are reused by the next unit
+    mbar_init(bar(B_PREADY), 128);
+    mbar_init(bar(B_PVDONE), 1);
+    mbar_fence_init();
   }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) { tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); }
+    const uint64_t pol = policy_evict_normal();
+    bool ok = true;
+    int item = 0, nu = 0;
+    for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      UnitIds mine;
+      const int nb = unit_blocks(p, u, lane, mine);
+      if (nb == 0) continue;
+      const int i = static_cast<int>(u / p.Hkv), g = static_cast<int>(u % p.Hkv);
+      const int qb = nu & 1;
+      if (lane == 0) {
+        // Q buffer qb was last read by the S MMAs of unit nu - 2
+        if (nu >= 2) ok = mbar_wait(bar(B_QEMPTY0 + qb), ((nu >> 1) - 1) & 1);
+        if (ok) {
+          const uint32_t dq = sb + kOffQ + qb * 4096;
+          mbar_expect_tx(bar(B_QFULL0 + qb), 4096);
+          tma_load_3d(dq, &tmQ, 0, g * kGroup, i, bar(B_QFULL0 + qb), pol);
+          tma_load_3d(dq + 2048, &tmQ, 64, g * kGroup, i, bar(B_QFULL0 + qb), pol);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      for (int k = 0; k < nb && ok; ++k, ++item) {
+        const int b = block_at(mine, k);
+        if (lane == 0) {
+          // one box per tensor: the whole 128 x 128 block, both halves of each 256-byte row
+          // fetched together, laid out [key / 8][D half][key % 8][64].  A slot is reused once
+          // the MMA that read it (S for K, P V for V) is done; slots free in ring order.
+#pragma unroll
+          for (int t = 0; t < 2 && ok; ++t) {
+            const int n = 2 * item + t, sl = n % kSlots;
+            if (n >= kSlots) ok = mbar_wait(bar(B_EMPTY0 + sl), ((n / kSlots) - 1) & 1);
+            if (ok) {
+              const uint32_t fb = bar(B_FULL0 + sl);
+              mbar_expect_tx(fb, kSlotBytes);
+              tma_load_5d(sb + kOffKV + sl * kSlotBytes, t ? &tmV : &tmK, 0, 0, 0, g, b * (kBlock / 8), fb, pol);
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      ++nu;
+    }
+    if (!ok && lane == 0) flag_timeout(p.hdr_w);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    // S^T: M 128 keys, N 16 heads, both operands K-major (128-byte swizzle)
+    constexpr uint32_t idesc_s = idesc_f16(128, 16, 1, 1, 0, 0);
+    // O^T: M 128 (D), N 16 heads; A = V_b read MN-major, B = P^T K-major
+    constexpr uint32_t idesc_o = idesc_f16(128, 16, 1, 1, 1, 0);
+    bool ok = true;
+    int item = 0, nu = 0, pending = -1;
+    auto issue_pv = [&](int x) -> bool {
+      const int vn = 2 * x + 1, vs = vn % kSlots;
+      if (!mbar_wait(bar(B_FULL0 + vs), (vn / kSlots) & 1)) return false;
+      if (!mbar_wait(bar(B_PREADY), x & 1)) return false;
+      tc_fence_after();
+      const uint32_t va = sb + kOffKV + vs * kSlotBytes;
+      const uint32_t pa = sb + kOffP;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mma_f16_ss(tmem + 32, smem_desc(va + k * 4096, 1024, 2048, 2),
+                   smem_desc(pa + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024, 2), idesc_o, k > 0);
+      mma_commit(bar(B_PVDONE));
+      mma_commit(bar(B_EMPTY0 + vs));
+      return true;
+    };
+    for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      UnitIds mine;
+      const int nb = unit_blocks(p, u, lane, mine);
+      if (nb == 0) continue;
+      const int qb = nu & 1;
+      if (lane == 0) {
+        ok = mbar_wait(bar(B_QFULL0 + qb), (nu >> 1) & 1);
+        for (int k = 0; k < nb && ok; ++k, ++item) {
+          const int kn = 2 * item, ks = kn % kSlots, s = item & 1;
+          if (!(ok = mbar_wait(bar(B_FULL0 + ks), (kn / kSlots) & 1))) break;
+          // S[s] is reused: the softmax warps must have read S of item - 2
+          if (item >= 2 && !(ok = mbar_wait(bar(B_SFREE0 + s), ((item >> 1) - 1) & 1))) break;
+          tc_fence_after();
+          const uint32_t ka = sb + kOffKV + ks * kSlotBytes, qa = sb + kOffQ + qb * 4096;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ss(tmem + s * 16, smem_desc(ka + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048, 2),
+                       smem_desc(qa + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024, 2), idesc_s, kk > 0);
+          mma_commit(bar(B_SFULL0 + s));
+          mma_commit(bar(B_EMPTY0 + ks));
+          if (k == nb - 1) mma_commit(bar(B_QEMPTY0 + qb));
+          if (pending >= 0 && !(ok = issue_pv(pending))) break;
+          pending = item;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ++nu;
+    }
+    if (lane == 0 && ok && pending >= 0) ok = issue_pv(pending);
+    if (!ok && lane == 0) flag_timeout(p.hdr_w);
+  } else {
+    // ------------------------------------------------------------ softmax + output (warps 2-5)
+    const int q4 = warp & 3;           // TMEM lane quadrant of this warp
+    const int key = 32 * q4 + lane;    // TMEM lane = key of S^T and d of O^T
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+    const uint32_t bar_id = 1;
+    const float kLn2 = 0.6931471805599453f;
+    bool ok = true;
+    int item = 0;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+      UnitIds mine;
+      const int nb = unit_blocks(p, u, lane, mine);
+      const int i = static_cast<int>(u / p.Hkv), g = static_cast<int>(u % p.Hkv);
+      __nv_bfloat16* Orow = p.O + (static_cast<int64_t>(i) * p.Hq + g * kGroup) * kHeadDim;
+      if (nb == 0) {
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) Orow[h * kHeadDim + key] = __float2bfloat16(0.f);
+        if (p.LSE && key < kGroup) p.LSE[static_cast<int64_t>(i) * p.Hq + g * kGroup + key] = -INFINITY;
+        continue;
+      }
+      const int pos = p.Lkv - p.N + i;
+      float m[kGroup], l[kGroup], o[kGroup], aprev[kGroup];
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+        o[h] = 0.f;
+        aprev[h] = 0.f;
+      }
+      for (int k = 0; k < nb; ++k, ++item) {
+        const int b = block_at(mine, k);
+        const int s = item & 1;
+        ok = mbar_wait(bar(B_SFULL0 + s), (item >> 1) & 1);
+        if (!named_bar_and(bar_id, 128, ok)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sv[16];
+        tmem_ld16(tmem + lane_base + s * 16, sv);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(bar(B_SFREE0 + s));
+        const bool vis = b * kBlock + key <= pos;
+        float x[kGroup];
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) x[h] = vis ? __uint_as_float(sv[h]) * p.sl2 : -INFINITY;
+        // per-head maximum over the 128 keys: within the warp, then across the 4 warps
+        const float mx = warp_reduce16<true>(x, lane);
+        float* rb = red + (k & 1) * 64;
+        if (!(lane & 1)) rb[(lane >> 1) * 4 + q4] = mx;  // [head][warp]
+        named_bar_sync(bar_id, 128);
+        float alpha[kGroup], pv[kGroup], mn[kGroup];
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+          const float4 w4 = reinterpret_cast<const float4*>(rb)[h];
+          const float bm = fmaxf(fmaxf(w4.x, w4.y), fmaxf(w4.z, w4.w));
+          mn[h] = fmaxf(m[h], bm);  // finite: the block holds at least one visible key
+          alpha[h] = ex2(m[h] - mn[h]);
+          pv[h] = vis ? ex2(x[h] - mn[h]) : 0.f;
+        }
+        // per-head sum of P over the 128 keys
+        const float sm = warp_reduce16<false>(pv, lane);
+        float* rs = red + 128 + (k & 1) * 64;
+        if (!(lane & 1)) rs[(lane >> 1) * 4 + q4] = sm;
+        // the previous block's P V: accumulate it (relative to the previous maximum), then
+        // the P buffer is free for this block
+        if (k > 0) {
+          ok = mbar_wait(bar(B_PVDONE), (item - 1) & 1);
+          if (!named_bar_and(bar_id, 128, ok)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t ov[16];
+          tmem_ld16(tmem + lane_base + 32, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < kGroup; ++h) o[h] = fmaf(o[h], aprev[h], __uint_as_float(ov[h]));
+        } else {
+          named_bar_sync(bar_id, 128);
+        }
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+          const float4 w4 = reinterpret_cast<const float4*>(rs)[h];
+          const float bs = (w4.x + w4.y) + (w4.z + w4.w);
+          l[h] = fmaf(l[h], alpha[h], bs);
+          m[h] = mn[h];
+          aprev[h] = alpha[h];
+        }
+        // P^T[h][key] (bf16) in the K-major 128-byte-swizzled B layout: keys 0-63 and
+        // 64-127 in two 2 KB halves of 16 rows
+        {
+          const int half = key >> 6, kk = key & 63;
+          uint8_t* pb = smem + kOffP + half * 2048 + (kk & 7) * 2;
+#pragma unroll
+          for (int h = 0; h < kGroup; ++h)
+            *reinterpret_cast<__nv_bfloat16*>(pb + h * 128 + (((kk >> 3) ^ (h & 7)) << 4)) = __float2bfloat16(pv[h]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(B_PREADY));
+      }
+      if (!ok) break;
+      // the unit's last P V
+      ok = mbar_wait(bar(B_PVDONE), (item - 1) & 1);
+      if (!named_bar_and(bar_id, 128, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t ov[16];
+      tmem_ld16(tmem + lane_base + 32, ov);
+      tmem_ld_wait();
+      tc_fence_before();
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) {
+        o[h] = fmaf(o[h], aprev[h], __uint_as_float(ov[h]));
+        Orow[h * kHeadDim + key] = __float2bfloat16(o[h] / l[h]);
+      }
+      if (p.LSE && key < kGroup) {
+        float mk = m[0], lk = l[0];
+#pragma unroll
+        for (int h = 1; h < kGroup; ++h)
+          if (key == h) { mk = m[h]; lk = l[h]; }
+        p.LSE[static_cast<int64_t>(i) * p.Hq + g * kGroup + key] = (mk + lg2(lk)) * kLn2;
+      }
+      // all 128 threads are past this unit's reads of `red` before the next unit writes it
+      named_bar_sync(bar_id, 128);
+    }
+    if (!ok && tid == 64) flag_timeout(p.hdr_w);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -263,6 +410,28 @@ cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, 
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  CUtensorMap tmQ, tmK, tmV;
+  {
+    // Q [N][Hq][128] bf16: box = 64 columns of the 16 heads of one group of one query
+    const uint64_t dims[3] = {kHeadDim, static_cast<uint64_t>(Hq), static_cast<uint64_t>(s->N)};
+    const uint64_t strides[2] = {kHeadDim * 2, static_cast<uint64_t>(Hq) * kHeadDim * 2};
+    const uint32_t box[3] = {64, kGroup, 1};
+    if (!encode_tmap(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, Q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    // K, V [Lkv][Hkv][128] bf16 viewed as (d % 64, key % 8, d / 64, group, key / 8): one box =
+    // one 128-key block of one group (32 KB), laid out [key / 8][d / 64][key % 8][64]: 8-row
+    // groups of 128-byte rows 2048 bytes apart, the second D half 1024 bytes after the first
+    const uint64_t row = static_cast<uint64_t>(s->Hkv) * kHeadDim * 2;  // bytes per key
+    const uint64_t dims[5] = {64, 8, 2, static_cast<uint64_t>(s->Hkv), static_cast<uint64_t>(s->nblocks) * (kBlock / 8)};
+    const uint64_t strides[4] = {row, 128, kHeadDim * 2, 8 * row};
+    const uint32_t box[5] = {64, 8, 2, 1, kBlock / 8};
+    if (!encode_tmap(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, K, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, V, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(q_outer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -270,11 +439,9 @@ cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, 
     attr_set = true;
   }
   QoParams p;
-  p.Q = static_cast<const __nv_bfloat16*>(Q);
-  p.K = static_cast<const __nv_bfloat16*>(K);
-  p.V = static_cast<const __nv_bfloat16*>(V);
   p.blist = s->d.blist;
   p.hdr = s->d.hdr;
+  p.hdr_w = s->d.hdr;
   p.O = static_cast<__nv_bfloat16*>(O);
   p.LSE = LSE;
   p.N = s->N;
@@ -282,12 +449,13 @@ cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, 
   p.Hq = Hq;
   p.Hkv = s->Hkv;
   p.topK = s->topK;
+  p.nblocks = s->nblocks;
   p.sl2 = scale * 1.4426950408889634f;
   p.force_path = force_path;
   const int64_t units = static_cast<int64_t>(s->N) * s->Hkv;
   int64_t grid = sms;
   if (grid > units) grid = units;
-  q_outer_kernel<<<static_cast<int>(grid), kThreads, kSmemBytes, st>>>(p);
+  q_outer_kernel<<<static_cast<int>(grid), kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }
 
