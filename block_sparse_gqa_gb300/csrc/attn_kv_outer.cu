@@ -68,6 +68,13 @@ namespace msa {
 namespace {
 
 constexpr int kThreads = 512;
+// setmaxnreg shares per warpgroup (control, each of the two softmax, output).  An
+// increase is granted only from registers the block already holds, so the shares must
+// add up to no more than the launch allocation (512 threads x 128 registers); a larger
+// sum would leave setmaxnreg.inc waiting forever.
+constexpr uint32_t kRegCtl = 72, kRegSoftmax = 176, kRegOut = 88;
+static_assert(kThreads == 512 && 128 * (kRegCtl + 2 * kRegSoftmax + kRegOut) <= 512 * 128,
+              "setmaxnreg shares exceed the launch allocation");
 constexpr int kChunkTiles = 8;  // tiles per claimed chunk
 constexpr int kRing = 8;        // tile-info ring slots
 constexpr int kQStages = 3;
@@ -292,7 +299,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    regs_dec<72>();
+    regs_dec<kRegCtl>();
     if (warp == 0) {
       // ---------------------------------------------------------- producer (whole warp)
       int* counter = &p.hdr->pad[0];
@@ -538,7 +545,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       }
     }
   } else if (warp < 12) {
-    regs_inc<176>();
+    regs_inc<kRegSoftmax>();
     // ------------------------------------------------------------ softmax
     const int wg = (warp - 4) >> 2;  // 0 or 1: the stage (tile parity) handled
     const uint32_t bar_id = 1 + wg;
@@ -614,7 +621,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       if (!gather(it + 3)) { flag_timeout(p.hdr); break; }
     }
   } else {
-    regs_dec<88>();
+    regs_dec<kRegOut>();
     // ------------------------------------------------------------ output (raw O -> bf16 -> TMA store)
     const uint32_t bar_id = 3;
     const int row = 32 * (warp & 3) + lane;
