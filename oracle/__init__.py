@@ -58,6 +58,8 @@ def _load():
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
         lib.oracle_dispatch.restype = i32
         lib.oracle_dispatch.argtypes = [ctypes.c_int32, i32]
+        lib.oracle_select_r1.restype = i32
+        lib.oracle_select_r1.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, P, P]
         _lib = lib
     return _lib
 
@@ -168,3 +170,26 @@ def e4m3_decode(byte: int) -> float:
 def dispatch(nsb: int, N: int) -> int:
     """1 = KV-outer, 2 = Q-outer (crossover nsb/N < 2.85)."""
     return _load().oracle_dispatch(int(nsb), int(N))
+
+
+def select_r1(Q, K, *, Lkv, topK, block=128, tile=128):
+    """Block selector R1 ("Sparse Attention", Chapter 4): (indices [N, Hkv, topK] int32,
+    scores [ntiles, Hkv, nblocks] float64 with +inf for the tile's own blocks and -inf
+    for blocks after the tile).  Q [N, Hq, D], K [Lkv, Hkv, D] as bf16 bit patterns
+    (uint16) or float64."""
+    lib = _load()
+    Q = np.ascontiguousarray(Q); K = np.ascontiguousarray(K)
+    fmt = _fmt_of(Q)
+    if _fmt_of(K) != fmt:
+        raise TypeError("Q and K must share one storage format")
+    N, Hq, D = Q.shape
+    Hkv = K.shape[1]
+    assert K.shape == (Lkv, Hkv, D)
+    nblocks = Lkv // block
+    ntiles = -(-N // tile)
+    idx = np.zeros((N, Hkv, topK), np.int32)
+    scores = np.zeros((ntiles, Hkv, nblocks), np.float64)
+    st = lib.oracle_select_r1(_ptr(Q), _ptr(K), fmt, N, Lkv, Hq, Hkv, D, block, tile, topK, _ptr(idx), _ptr(scores))
+    if st < 0:
+        raise ValueError("oracle_select_r1 rejected its arguments")
+    return idx, scores

@@ -309,3 +309,90 @@ void oracle_lse_merge(int n, int D, const double* O_parts, const double* lse_par
 int oracle_dispatch(int32_t nsb, int N) {
   return ((int64_t)nsb * 100 < (int64_t)N * 285) ? 1 : 2;
 }
+
+/* Block selector R1 ("Sparse Attention" (dinara-dl), Chapter 4, "R1: One
+ * Representative"): for each tile of 128 consecutive queries and each GQA group,
+ * every query head of the group is summarised by the mean of its 128 query vectors
+ * and every KV block of the group by the mean of its 128 key vectors; the block's
+ * score is the largest, over the group's heads, of the dot product of the two means;
+ * the tile keeps the topK best blocks ("TopK16" in the chapter).
+ * Readings where the chapter is silent (also in the design notes):
+ *  - a tile is queries [128 t, min(128 t + 128, N)); its mean is over the queries it
+ *    holds;
+ *  - candidates are the blocks b <= lb(last query of the tile) (causal for at least one
+ *    query of the tile); the blocks holding the tile's own queries (lb(first) ..
+ *    lb(last)) are always kept (score +inf), as every list of the method holds the
+ *    query's own block;
+ *  - order of the list: score descending, ties by smaller block id; fewer candidates
+ *    than topK -> padded with -1;
+ *  - every query of the tile gets the tile's list for that group.
+ * Outputs: indices [N, Hkv, topK] and scores [ntiles, Hkv, nblocks] (+inf forced,
+ * -inf for non-candidates).  Returns 0, or -1 on bad arguments. */
+int oracle_select_r1(const void* Q, const void* K, int fmt, int N, int Lkv, int Hq, int Hkv, int D, int block,
+                     int tile, int topK, int32_t* indices, double* scores) {
+  if (N < 1 || Lkv < block || Lkv % block || Hq % Hkv || topK < 1 || tile < 1 || N > Lkv) return -1;
+  const int G = Hq / Hkv, nblocks = Lkv / block, ntiles = (N + tile - 1) / tile;
+  double* kbar = (double*)calloc((size_t)Hkv * nblocks * D, sizeof(double));
+  double* qbar = (double*)calloc((size_t)Hq * D, sizeof(double));
+  int* used = (int*)calloc((size_t)nblocks, sizeof(int));
+  if (!kbar || !qbar || !used) {
+    free(kbar); free(qbar); free(used);
+    return -1;
+  }
+  /* block means of the keys, per group */
+  for (int g = 0; g < Hkv; ++g)
+    for (int b = 0; b < nblocks; ++b)
+      for (int d = 0; d < D; ++d) {
+        double s = 0.0;
+        for (int j = 0; j < block; ++j) s += load_elem(K, fmt, ((size_t)(b * block + j) * Hkv + g) * D + d);
+        kbar[((size_t)g * nblocks + b) * D + d] = s / block;
+      }
+  for (int t = 0; t < ntiles; ++t) {
+    const int i0 = t * tile, i1 = (i0 + tile < N) ? i0 + tile : N;
+    /* query means of the tile, per head */
+    for (int h = 0; h < Hq; ++h)
+      for (int d = 0; d < D; ++d) {
+        double s = 0.0;
+        for (int i = i0; i < i1; ++i) s += load_elem(Q, fmt, ((size_t)i * Hq + h) * D + d);
+        qbar[(size_t)h * D + d] = s / (i1 - i0);
+      }
+    const int lb_first = (Lkv - N + i0) / block, lb_last = (Lkv - N + i1 - 1) / block;
+    for (int g = 0; g < Hkv; ++g) {
+      double* sc = scores + ((size_t)t * Hkv + g) * nblocks;
+      for (int b = 0; b < nblocks; ++b) {
+        if (b > lb_last) {
+          sc[b] = -INFINITY;
+        } else if (b >= lb_first) {
+          sc[b] = INFINITY;
+        } else {
+          double best = -INFINITY;
+          for (int h = g * G; h < (g + 1) * G; ++h) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += qbar[(size_t)h * D + d] * kbar[((size_t)g * nblocks + b) * D + d];
+            if (dot > best) best = dot;
+          }
+          sc[b] = best;
+        }
+      }
+      /* topK by repeated selection of the best unused candidate (ties: smaller id) */
+      memset(used, 0, sizeof(int) * nblocks);
+      int32_t list[256];
+      const int K = topK < 256 ? topK : 256;
+      for (int k = 0; k < K; ++k) {
+        int arg = -1;
+        for (int b = 0; b < nblocks; ++b) {
+          if (used[b] || sc[b] == -INFINITY) continue;
+          if (arg < 0 || sc[b] > sc[arg]) arg = b;
+        }
+        list[k] = arg;
+        if (arg >= 0) used[arg] = 1;
+      }
+      for (int i = i0; i < i1; ++i)
+        for (int k = 0; k < topK; ++k) indices[((size_t)i * Hkv + g) * topK + k] = k < K ? list[k] : -1;
+    }
+  }
+  free(kbar);
+  free(qbar);
+  free(used);
+  return 0;
+}

@@ -339,3 +339,93 @@ def test_bf16_path_equals_decoded_f64():
     O, L, _ = oracle.attn_fwd(*(t.to(torch.float64).numpy() for t in ts), idx, Lkv=Lkv,
                               block=block, scale=0.3)
     assert np.array_equal(Ob, O) and np.array_equal(Lb, L)
+
+
+# ---------------------------------------------------------------------------------
+# Block selector R1 ("Sparse Attention", Chapter 4, "R1: One Representative"): pinned
+# by closed forms on inputs built for them, by an invariance, and by the list rules.
+
+def _r1(Q, K, Lkv, topK, block=32, tile=32):
+    return oracle.select_r1(Q, K, Lkv=Lkv, topK=topK, block=block, tile=tile)
+
+
+def test_select_r1_zero_queries_tie_rule():
+    """Q = 0: every candidate scores 0, so after the forced own block the list is the
+    candidates in ascending id order, padded with -1 when they run out."""
+    N = Lkv = 128
+    Q = np.zeros((N, 4, 8))
+    K = np.random.default_rng(1).standard_normal((Lkv, 2, 8))
+    idx, sc = _r1(Q, K, Lkv, topK=3)
+    for t in range(4):  # tile t holds block t
+        assert np.all(idx[32 * t:32 * t + 32, :, 0] == t)
+        rest = [b for b in range(t)][:2]
+        want = rest + [-1] * (2 - len(rest))
+        assert np.all(idx[32 * t:32 * t + 32, :, 1:] == np.array(want))
+        assert np.all(sc[t, :, :t] == 0.0) and np.all(np.isposinf(sc[t, :, t]))
+        assert np.all(np.isneginf(sc[t, :, t + 1:]))
+
+
+def test_select_r1_block_mean_and_head_max_closed_form():
+    """Keys of block b of group 0 are j * (b + 1) * e0 (j = 0..31): the block mean is
+    15.5 * (b + 1) * e0.  Only head 1 of the group has queries, all equal to 2 * e0, so
+    its tile mean is 2 * e0 and the block score is max(0 (the other heads),
+    31 * (b + 1)); group 1 has negative keys, so its scores are all 0."""
+    N = Lkv = 128
+    D, block = 4, 32
+    Q = np.zeros((N, 4, D))
+    Q[:, 1, 0] = 2.0
+    K = np.zeros((Lkv, 2, D))
+    for b in range(4):
+        for j in range(32):
+            K[b * 32 + j, 0, 0] = j * (b + 1)
+            K[b * 32 + j, 1, 0] = -j * (b + 1)
+    idx, sc = _r1(Q, K, Lkv, topK=4, block=block)
+    t = 3  # the last tile sees blocks 0..2 as candidates
+    np.testing.assert_allclose(sc[t, 0, :3], [31.0, 62.0, 93.0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sc[t, 1, :3], [0.0, 0.0, 0.0], atol=1e-12)
+    assert list(idx[100, 0]) == [3, 2, 1, 0]
+    assert list(idx[100, 1]) == [3, 0, 1, 2]
+
+
+def test_select_r1_planted_block_is_chosen():
+    """A block whose keys all equal a large multiple of the tile's mean query is chosen
+    right after the forced own block, whatever the other blocks hold."""
+    rng = np.random.default_rng(2)
+    N = Lkv = 256
+    D = 8
+    Q = rng.standard_normal((N, 2, D)) * 0.1
+    Q[192:224, 0, :] += 1.0  # tile 6: head 0 mean ~ ones
+    K = rng.standard_normal((Lkv, 1, D)) * 0.1
+    K[64:96, 0, :] = 10.0  # block 2
+    idx, _ = _r1(Q, K, Lkv, topK=3)
+    assert list(idx[200, 0, :2]) == [6, 2]
+
+
+def test_select_r1_block_swap_equivariance():
+    """Exchanging the keys of two candidate blocks exchanges their ids in every list."""
+    rng = np.random.default_rng(3)
+    N = Lkv = 256
+    Q = rng.standard_normal((N, 4, 8))
+    K = rng.standard_normal((Lkv, 2, 8))
+    idx, _ = _r1(Q, K, Lkv, topK=5)
+    K2 = K.copy()
+    K2[32:64], K2[96:128] = K[96:128].copy(), K[32:64].copy()  # blocks 1 and 3
+    idx2, _ = _r1(Q, K2, Lkv, topK=5)
+    sw = idx.copy()
+    sw[idx == 1], sw[idx == 3] = 3, 1
+    # tiles 4.. see both blocks as candidates: the lists must match after the exchange
+    assert np.array_equal(idx2[128:], sw[128:])
+
+
+def test_select_r1_tail_queries_and_two_own_blocks():
+    """Queries at the tail (N < Lkv) with a tile straddling two blocks: both blocks are
+    forced, later blocks are never listed, a partial last tile uses its own mean."""
+    rng = np.random.default_rng(4)
+    N, Lkv = 80, 256  # positions 176..255; tiles of 32: [176..207] holds blocks 5 and 6
+    Q = rng.standard_normal((N, 2, 8))
+    K = rng.standard_normal((Lkv, 1, 8))
+    idx, sc = _r1(Q, K, Lkv, topK=4)
+    assert set(idx[0, 0, :2]) == {5, 6} and np.all(idx[0, 0] <= 6)
+    assert np.all(np.isneginf(sc[0, 0, 7:]))
+    # the last tile (queries 64..79, 16 queries) sees blocks 0..7
+    assert idx[79, 0, 0] == 7 and np.all(idx[64:80] == idx[79])
