@@ -78,6 +78,10 @@ def lib() -> ctypes.CDLL:
         L.msa_last_cuda_error.argtypes = []
         L.msa_version.restype = I
         L.msa_version.argtypes = []
+        L.msa_select_workspace_bytes.restype = ctypes.c_size_t
+        L.msa_select_workspace_bytes.argtypes = [I, I, I, I]
+        L.msa_select_blocks_r1.restype = I
+        L.msa_select_blocks_r1.argtypes = [Tensor, Tensor, I, P, P, ctypes.c_size_t, P]
         _lib = L
     return _lib
 
@@ -191,6 +195,26 @@ def sparse_attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, schedule:
                                    LSE.data_ptr(), float(scale), ctypes.byref(opts))
     _check(st, "msa_sparse_attn_fwd")
     return O, LSE
+
+
+def select_blocks_r1(Q: torch.Tensor, K: torch.Tensor, topK: int, indices: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """msa_select_blocks_r1: int32 block lists [N, Hkv, topK] (device) for bf16 Q [N, Hq, 128]
+    and K [Lkv, Hkv, 128]; the workspace is allocated here unless given."""
+    N, Hq, _ = Q.shape
+    Lkv, Hkv, _ = K.shape
+    if indices is None:
+        indices = torch.empty((N, Hkv, topK), dtype=torch.int32, device=Q.device)
+    need = lib().msa_select_workspace_bytes(N, Hq, Hkv, Lkv // 128)
+    if workspace is None:
+        workspace = torch.empty(need + 256, dtype=torch.uint8, device=Q.device)
+    ptr = workspace.data_ptr()
+    aligned = (ptr + 255) // 256 * 256
+    usable = max(0, workspace.numel() * workspace.element_size() - (aligned - ptr))
+    st = lib().msa_select_blocks_r1(_tensor(Q), _tensor(K), int(topK), indices.data_ptr(), aligned, usable,
+                                    _stream_ptr(stream))
+    _check(st, "msa_select_blocks_r1")
+    return indices
 
 
 def version() -> int:

@@ -289,6 +289,29 @@ msa_status_t msa_schedule_export(msa_schedule_t s, int32_t* counts, int32_t* off
   return st;
 }
 
+size_t msa_select_workspace_bytes(int N, int Hq, int Hkv, int nblocks) {
+  if (N < 1 || Hq < 1 || Hkv < 1 || nblocks < 1) return 0;
+  return msa::select_workspace_bytes(N, Hq, Hkv, nblocks);
+}
+
+msa_status_t msa_select_blocks_r1(msa_tensor_t Q, msa_tensor_t K, int topK, int32_t* indices, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+  if (!Q.ptr || !K.ptr || !indices || !workspace) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(Q.ptr) || !aligned16(K.ptr) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MSA_ERR_INVALID_ARG;
+  if (Q.n < 1 || K.n < msa::kBlock || K.n % msa::kBlock || Q.n > K.n || Q.h < 1 || K.h < 1 || topK < 1)
+    return MSA_ERR_INVALID_ARG;
+  if (Q.d != K.d) return MSA_ERR_INVALID_ARG;
+  if (Q.d != msa::kHeadDim || Q.h != msa::kGroup * K.h || Q.dtype != MSA_BF16 || K.dtype != MSA_BF16 || topK > 64)
+    return MSA_ERR_UNSUPPORTED;
+  if (Q.n > INT32_MAX || K.n > INT32_MAX || static_cast<int64_t>(Q.n) * K.h * topK > INT32_MAX) return MSA_ERR_CAPACITY;
+  const int N = static_cast<int>(Q.n), Lkv = static_cast<int>(K.n), Hq = static_cast<int>(Q.h),
+            Hkv = static_cast<int>(K.h);
+  if (Lkv / msa::kBlock > 40960) return MSA_ERR_UNSUPPORTED;
+  if (workspace_bytes < msa::select_workspace_bytes(N, Hq, Hkv, Lkv / msa::kBlock)) return MSA_ERR_INVALID_ARG;
+  return from_cuda(msa::launch_select_r1(Q.ptr, K.ptr, N, Lkv, Hq, Hkv, topK, indices, workspace, stream));
+}
+
 const char* msa_status_string(msa_status_t st) {
   switch (st) {
     case MSA_OK: return "ok";

@@ -100,6 +100,12 @@ cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, f
 cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, const void* V, int Hq,
                            float scale, void* O, float* LSE, int force_path, cudaStream_t st);
 
+// select.cu: block selector R1
+size_t select_workspace_bytes(int N, int Hq, int Hkv, int nblocks);
+uint32_t select_smem_bytes(int nblocks);
+cudaError_t launch_select_r1(const void* Q, const void* K, int N, int Lkv, int Hq, int Hkv, int topK, int32_t* indices,
+                             void* workspace, cudaStream_t st);
+
 // tensor maps (msa_api.cpp)
 bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
                  const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz);

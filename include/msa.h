@@ -196,6 +196,35 @@ msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int N, int Hkv,
                                          msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, void* O, float* LSE,
                                          float scale, const msa_fwd_opts_t* opts);
 
+/*
+ * Block selector R1 ("Sparse Attention" (dinara-dl), Chapter 4, "R1: One
+ * Representative") -- the step that produces the block lists the forward reads.
+ *
+ * For every tile of 128 consecutive queries and every GQA group: each query head of
+ * the group is summarised by the mean of its query vectors over the tile, each KV
+ * block of the group by the mean of its 128 key vectors; a block's score is the
+ * largest, over the group's heads, of the dot product of the two means.  The tile
+ * keeps its topK best blocks: first the blocks holding the tile's own queries
+ * (ascending), then by score descending, ties to the smaller block id; blocks after
+ * the tile's last query are never chosen; if fewer than topK blocks are candidates the
+ * list is padded with -1.  Every query of the tile gets the tile's list.
+ *
+ * Q: bf16 [N, Hq, 128]; K: bf16 [Lkv, Hkv, 128], Lkv a multiple of 128, N <= Lkv
+ * (queries are the last N positions); Hq = 16 * Hkv.  indices: device int32
+ * [N, Hkv, topK], written completely.  workspace: device memory of at least
+ * msa_select_workspace_bytes(N, Hq, Hkv, Lkv / 128) bytes, 256-byte aligned, owned by
+ * the caller; its contents are scratch.  Arithmetic is fp32 (means, dot products).
+ * Asynchronous on `stream`; nothing is allocated.
+ *
+ * Returns MSA_ERR_INVALID_ARG for null or misaligned pointers, inconsistent shapes,
+ * topK < 1 or a workspace that is too small; MSA_ERR_UNSUPPORTED for D != 128,
+ * Hq != 16 * Hkv, non-bf16 inputs, topK > 64 or more than 40960 blocks; MSA_ERR_CUDA
+ * on launch failure.
+ */
+size_t msa_select_workspace_bytes(int N, int Hq, int Hkv, int nblocks);
+msa_status_t msa_select_blocks_r1(msa_tensor_t Q, msa_tensor_t K, int topK, int32_t* indices, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+
 /* Human-readable text for a status code (static storage). */
 const char* msa_status_string(msa_status_t st);
 
