@@ -80,6 +80,9 @@ def lib() -> ctypes.CDLL:
         L.msa_version.argtypes = []
         L.msa_select_workspace_bytes.restype = ctypes.c_size_t
         L.msa_select_workspace_bytes.argtypes = [I, I, I, I]
+        L.msa_sparse_attn_fwd_tiles.restype = I
+        L.msa_sparse_attn_fwd_tiles.argtypes = [Tensor, Tensor, Tensor, P, I, I, P, P, ctypes.c_float, P,
+                                                ctypes.POINTER(FwdOpts)]
         L.msa_select_blocks_r1.restype = I
         L.msa_select_blocks_r1.argtypes = [Tensor, Tensor, I, P, P, ctypes.c_size_t, P]
         _lib = L
@@ -215,6 +218,31 @@ def select_blocks_r1(Q: torch.Tensor, K: torch.Tensor, topK: int, indices: torch
                                     _stream_ptr(stream))
     _check(st, "msa_select_blocks_r1")
     return indices
+
+
+def sparse_attn_fwd_tiles(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, tile_lists: torch.Tensor, tile: int,
+                          scale: float | None = None, O: torch.Tensor | None = None, LSE: torch.Tensor | None = None,
+                          status: torch.Tensor | None = None, num_ctas: int = 0, stream=None):
+    """msa_sparse_attn_fwd_tiles: (O bf16 [N,Hq,D], LSE fp32 [N,Hq]) for int32 lists
+    [ceil(N / tile), Hkv, topK] shared by `tile` consecutive queries."""
+    N, Hq, D = Q.shape
+    if scale is None:
+        scale = D ** -0.5
+    if O is None:
+        O = torch.empty((N, Hq, D), dtype=torch.bfloat16, device=Q.device)
+    if LSE is None:
+        LSE = torch.empty((N, Hq), dtype=torch.float32, device=Q.device)
+    if tile_lists.dtype != torch.int32 or not tile_lists.is_contiguous() or tile_lists.dim() != 3:
+        raise ValueError("tile_lists must be a contiguous int32 tensor [ceil(N / tile), Hkv, topK]")
+    opts = FwdOpts()
+    lib().msa_fwd_opts_init(ctypes.byref(opts))
+    opts.stream = _stream_ptr(stream)
+    opts.num_ctas = int(num_ctas)
+    st = lib().msa_sparse_attn_fwd_tiles(_tensor(Q), _tensor(K), _tensor(V), tile_lists.data_ptr(), int(tile),
+                                         int(tile_lists.shape[2]), O.data_ptr(), LSE.data_ptr(), float(scale),
+                                         status.data_ptr() if status is not None else None, ctypes.byref(opts))
+    _check(st, "msa_sparse_attn_fwd_tiles")
+    return O, LSE
 
 
 def version() -> int:

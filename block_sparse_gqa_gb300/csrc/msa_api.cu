@@ -312,6 +312,29 @@ msa_status_t msa_select_blocks_r1(msa_tensor_t Q, msa_tensor_t K, int topK, int3
   return from_cuda(msa::launch_select_r1(Q.ptr, K.ptr, N, Lkv, Hq, Hkv, topK, indices, workspace, stream));
 }
 
+msa_status_t msa_sparse_attn_fwd_tiles(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, const int32_t* tile_lists,
+                                       int tile, int topK, void* O, float* LSE, float scale, int32_t* status,
+                                       const msa_fwd_opts_t* opts) {
+  msa_fwd_opts_t def;
+  if (!opts) {
+    msa_fwd_opts_init(&def);
+    opts = &def;
+  }
+  if (!Q.ptr || !K.ptr || !V.ptr || !O || !tile_lists) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(Q.ptr) || !aligned16(K.ptr) || !aligned16(V.ptr) || !aligned16(O)) return MSA_ERR_INVALID_ARG;
+  if (Q.n < 1 || K.n < msa::kBlock || K.n % msa::kBlock || V.n != K.n || Q.n > K.n) return MSA_ERR_INVALID_ARG;
+  if (K.h < 1 || V.h != K.h || Q.h < 1 || Q.d != K.d || K.d != V.d) return MSA_ERR_INVALID_ARG;
+  if (tile < 16 || tile % 16 || topK < 1 || !std::isfinite(scale)) return MSA_ERR_INVALID_ARG;
+  if (Q.d != msa::kHeadDim || Q.h != msa::kGroup * K.h || topK > 64) return MSA_ERR_UNSUPPORTED;
+  if (Q.dtype != MSA_BF16 || K.dtype != MSA_BF16 || V.dtype != MSA_BF16) return MSA_ERR_UNSUPPORTED;
+  if (K.n > INT32_MAX || static_cast<int64_t>(Q.n) * Q.h > INT32_MAX) return MSA_ERR_CAPACITY;
+  const int ctas = opts->num_ctas > 0 ? opts->num_ctas : device_sms();
+  if (ctas < 1) return MSA_ERR_CUDA;
+  return from_cuda(msa::launch_tiles(Q.ptr, K.ptr, V.ptr, static_cast<int>(Q.n), static_cast<int>(K.n),
+                                     static_cast<int>(Q.h), static_cast<int>(K.h), tile_lists, tile, topK, scale, O, LSE,
+                                     status, ctas, opts->stream));
+}
+
 const char* msa_status_string(msa_status_t st) {
   switch (st) {
     case MSA_OK: return "ok";

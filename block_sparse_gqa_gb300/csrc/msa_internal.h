@@ -106,6 +106,11 @@ uint32_t select_smem_bytes(int nblocks);
 cudaError_t launch_select_r1(const void* Q, const void* K, int N, int Lkv, int Hq, int Hkv, int topK, int32_t* indices,
                              void* workspace, cudaStream_t st);
 
+// attn_tiles.cu: forward for lists shared by tiles of consecutive queries
+cudaError_t launch_tiles(const void* Q, const void* K, const void* V, int N, int Lkv, int Hq, int Hkv,
+                         const int32_t* lists, int tile, int topK, float scale, void* O, float* LSE, int32_t* status,
+                         int num_ctas, cudaStream_t st);
+
 // tensor maps (msa_api.cpp)
 bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
                  const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz);

@@ -225,6 +225,36 @@ size_t msa_select_workspace_bytes(int N, int Hq, int Hkv, int nblocks);
 msa_status_t msa_select_blocks_r1(msa_tensor_t Q, msa_tensor_t K, int topK, int32_t* indices, void* workspace,
                                   size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * msa_sparse_attn_fwd_tiles -- the forward main branch when consecutive queries share
+ * their block lists ("Sparse Attention" (dinara-dl), Chapter 4: the selectors choose
+ * the blocks of a whole 128-query tile per GQA group; Chapter 3: a query tile stays on
+ * chip while its blocks stream past).  No schedule, no partial outputs, no combine:
+ * each group of 8 consecutive queries x 16 heads walks its list's blocks with an online
+ * softmax and writes O and LSE directly.
+ *
+ * Q: bf16 [N, Hq, 128]; K, V: bf16 [Lkv, Hkv, 128], Lkv a multiple of 128, N <= Lkv
+ * (queries are the last N positions); Hq = 16 * Hkv.  tile_lists: device int32
+ * [ceil(N / tile), Hkv, topK]: query i of group g uses list tile_lists[i / tile][g];
+ * tile a multiple of 16.  The semantics per query are those of msa_sparse_attn_fwd
+ * on the expanded per-query lists: -1 is padding, a repeated id counts once, keys
+ * after the query are masked (ids after the last query of a 16-query group are
+ * skipped), ids >= Lkv / 128 or < -1 are ignored and set bit 0 of *status.  O: bf16
+ * [N, Hq, 128]; LSE: fp32 [N, Hq] (may be NULL); a query with no visible key gets
+ * O = 0, LSE = -inf.  status: device int32 (may be NULL), bits OR-ed in: 1 bad id,
+ * 2 a device wait timed out; the caller zeroes it.  opts: stream and num_ctas are
+ * used (path, descales and stage events are ignored).  Asynchronous; nothing is
+ * allocated.
+ *
+ * Returns MSA_ERR_INVALID_ARG for null or misaligned pointers, inconsistent shapes,
+ * tile not a positive multiple of 16, topK < 1 or a non-finite scale;
+ * MSA_ERR_UNSUPPORTED for D != 128, Hq != 16 * Hkv, non-bf16 inputs or topK > 64;
+ * MSA_ERR_CUDA on launch failure.
+ */
+msa_status_t msa_sparse_attn_fwd_tiles(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, const int32_t* tile_lists,
+                                       int tile, int topK, void* O, float* LSE, float scale, int32_t* status,
+                                       const msa_fwd_opts_t* opts);
+
 /* Human-readable text for a status code (static storage). */
 const char* msa_status_string(msa_status_t st);
 
