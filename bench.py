@@ -50,6 +50,11 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="m3", choices=["tiny", "m3", "long", "lowreuse", "fp8"])
+    ap.add_argument("--lists", default="workload", choices=["workload", "r1"],
+                    help="block lists: the workload's own, or chosen by the R1 selector (once, before timing)")
+    ap.add_argument("--mode", default="general", choices=["general", "tiles"],
+                    help="general: schedule + attention + combine; tiles: the shared-list forward "
+                         "(lists shared by 128 queries for r1, by the workload's query runs otherwise)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -57,13 +62,13 @@ def parse_args():
 
 
 # ----------------------------------------------------------------------------- helpers
-def load_peaks():
+def load_peaks(kind="hbm_gbs"):
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return float(d[kind]), "measured"
+    return (6800.0 if kind == "hbm_gbs" else 1700.0), "fallback"
 
 
 def kernel_source_hash():
@@ -158,7 +163,7 @@ def barrier(pg):
 
 
 # ----------------------------------------------------------------------------- oracle timing
-def time_oracle(wl, seconds, seed=0):
+def time_oracle(wl, seconds, seed=0, indices=None):
     """Run the oracle on a seeded query sample sized for ~`seconds` of CPU time.
     Returns (TFLOP/s of useful work, sample description, threads)."""
     import numpy as np
@@ -167,7 +172,7 @@ def time_oracle(wl, seconds, seed=0):
     cfg = wl.cfg
     threads = os.cpu_count() or 1
     Qn, Kn, Vn = wl.np_inputs()
-    idx = wl.indices.numpy()
+    idx = wl.indices.numpy() if indices is None else indices
     rng = np.random.default_rng(seed)
 
     def run(nq):
@@ -229,8 +234,21 @@ def run_ours(args, world, rank, local, pg):
     wl = workloads.make_workload(cfg, seed=cfg.seed + 1000 * rank)
     stream = torch.cuda.current_stream()
 
-    idx_d = wl.indices.to(dev)
     Q, K, V = (t.to(dev) for t in (wl.Q, wl.K, wl.V))
+    if args.lists == "r1":
+        if cfg.dtype != "bf16":
+            raise SystemExit("the R1 selector takes bf16 inputs")
+        idx_d = msa.select_blocks_r1(Q, K, cfg.topK)  # an input of the step, chosen once
+        torch.cuda.synchronize()
+    else:
+        idx_d = wl.indices.to(dev)
+    tiles = args.mode == "tiles"
+    tstatus = torch.zeros(1, dtype=torch.int32, device=dev)  # device flags of the shared-list kernel
+    if tiles:
+        tile = 128 if args.lists == "r1" else cfg.run
+        tile_lists = idx_d[::tile].contiguous()
+        if tile % 16 or not torch.equal(torch.repeat_interleave(tile_lists, tile, 0)[:cfg.N], idx_d):
+            raise SystemExit(f"workload {cfg.name}: lists are not shared by tiles of a multiple of 16 queries")
     O = torch.empty((cfg.N, cfg.Hq, cfg.D), dtype=torch.bfloat16, device=dev)
     LSE = torch.empty((cfg.N, cfg.Hq), dtype=torch.float32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -245,6 +263,14 @@ def run_ours(args, world, rank, local, pg):
     descales = (wl.q_descale, wl.k_descale, wl.v_descale)
 
     def step(stage):
+        if tiles:
+            if stage:
+                stage[0].record(stream)
+            msa.sparse_attn_fwd_tiles(Q, K, V, tile_lists, tile, scale=cfg.scale, O=O, LSE=LSE, status=tstatus)
+            if stage:
+                stage[1].record(stream)
+                stage[2].record(stream)
+            return
         msa.build_schedule(idx_d, cfg.nblocks, schedule=sched)
         msa.sparse_attn_fwd(Q, K, V, sched, scale=cfg.scale, O=O, LSE=LSE, descales=descales,
                             stage_events=[e.cuda_event for e in stage] if stage else None)
@@ -254,7 +280,7 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.synchronize()
     info = sched.query()
     assert info["status"] == 0, info
-    kv_path = info["path"] == 1  # else the Q-outer kernel runs (inside the third stage)
+    kv_path = info["path"] == 1 or tiles  # else the Q-outer kernel runs (inside the third stage)
 
     starts, ends = new_events(args.steps), new_events(args.steps)
     stages = [new_events(3) for _ in range(args.steps)]
@@ -273,6 +299,8 @@ def run_ours(args, world, rank, local, pg):
     barrier(pg)
     clock_info = clocks.stop()
     after = sched.query()  # the device's sticky flags after the timed steps
+    if tiles:
+        after = {"status": int(tstatus.item())}
     if after["status"] != 0:
         raise SystemExit(f"device status {after['status']} after the timed steps (1 bad index, 2 wait timed out)")
 
@@ -308,14 +336,29 @@ def run_ours(args, world, rank, local, pg):
         achieved = attn_bytes / (attn_mean * 1e-3) / 1e9
         traffic = None
         step_bytes = attn_bytes + cfg.N * cfg.Hkv * cfg.topK * 4 * 3
+    roof = {"kernel": "kv_outer_kernel" if kv_path else "q_outer_kernel", "bound": "hbm", "achieved": achieved,
+            "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic, "algorithmic_bytes": attn_bytes,
+            "peak_source": f"{peak_kind} MEASURED_PEAKS.json hbm_gbs" if peak_kind == "measured"
+            else "fallback 6.8 TB/s", "launch_ms": attn_mean}
+    if tiles:
+        # the shared-list kernel moves Q, the distinct K/V blocks (re-read from L2 per
+        # 16-query pair) and O: it is bound by the tensor pipe and the softmax, not HBM
+        flops = 4.0 * 128 * D * G * E
+        tpeak, tkind = load_peaks("bf16_tflops_sustained")
+        achieved_t = flops / (attn_mean * 1e-3) / 1e12
+        roof = {"kernel": "tiles_kernel", "bound": "tensor", "achieved": achieved_t, "peak": tpeak,
+                "unit": "TFLOP/s", "frac": achieved_t / tpeak, "traffic": None, "algorithmic_flops": flops,
+                "peak_source": f"{tkind} MEASURED_PEAKS.json bf16_tflops_sustained", "launch_ms": attn_mean}
+        step_bytes = q_bytes + kv_bytes + cfg.N * cfg.Hq * (2 * D + 4) + tile_lists.numel() * 4
 
     e2e = None
     if not args.no_e2e:
         pin = lambda t: t.pin_memory()
-        hQ, hK, hV, hI = (pin(t) for t in (wl.Q, wl.K, wl.V, wl.indices))
+        lists_h = (tile_lists if tiles else idx_d).cpu()  # the step's block lists, as an input
+        hQ, hK, hV, hI = (pin(t) for t in (wl.Q, wl.K, wl.V, lists_h))
         hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
         hL = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
-        dQ, dK, dV, dI = (torch.empty_like(t, device=dev) for t in (wl.Q, wl.K, wl.V, wl.indices))
+        dQ, dK, dV, dI = (torch.empty_like(t, device=dev) for t in (wl.Q, wl.K, wl.V, lists_h))
         dO, dL = torch.empty_like(O), torch.empty_like(LSE)
         e_sched = None
 
@@ -323,8 +366,11 @@ def run_ours(args, world, rank, local, pg):
             nonlocal e_sched
             dQ.copy_(hQ, non_blocking=True); dK.copy_(hK, non_blocking=True)
             dV.copy_(hV, non_blocking=True); dI.copy_(hI, non_blocking=True)
-            e_sched = msa.build_schedule(dI, cfg.nblocks, schedule=e_sched)
-            msa.sparse_attn_fwd(dQ, dK, dV, e_sched, scale=cfg.scale, O=dO, LSE=dL, descales=descales)
+            if tiles:
+                msa.sparse_attn_fwd_tiles(dQ, dK, dV, dI, tile, scale=cfg.scale, O=dO, LSE=dL)
+            else:
+                e_sched = msa.build_schedule(dI, cfg.nblocks, schedule=e_sched)
+                msa.sparse_attn_fwd(dQ, dK, dV, e_sched, scale=cfg.scale, O=dO, LSE=dL, descales=descales)
             hO.copy_(dO, non_blocking=True); hL.copy_(dL, non_blocking=True)
 
         for _ in range(max(1, args.warmup)):
@@ -344,11 +390,12 @@ def run_ours(args, world, rank, local, pg):
         d2h = hO.numel() * hO.element_size() + hL.numel() * hL.element_size()
         e2e = {"value": world * cfg.nominal_flops() / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-        e_sched.close()
+        if e_sched is not None:
+            e_sched.close()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, threads, _ = time_oracle(wl, args.cpu_seconds)
+        v, sample, threads, _ = time_oracle(wl, args.cpu_seconds, indices=idx_d.cpu().numpy())
         cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample}
 
     sched.close()
@@ -363,18 +410,16 @@ def run_ours(args, world, rank, local, pg):
                                f"topK={cfg.topK}, causal, own block + up to {cfg.topK - 1} {cfg.picks} earlier blocks",
                    "l2": "flushed (256 MiB write) before every timed step, outside the step events",
                    "parallelism": f"independent problem per GPU x{world}",
-                   "path": "kv_outer" if kv_path else "q_outer",
+                   "path": "tiles" if tiles else ("kv_outer" if kv_path else "q_outer"),
+                   "lists": "R1 selector (chosen once, before timing)" if args.lists == "r1" else "workload",
                    "entries": E, "nsb": nsb, "tiles": T},
-        "roofline": {"kernel": "kv_outer_kernel" if kv_path else "q_outer_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                     "algorithmic_bytes": attn_bytes, "peak_source": f"{peak_kind} MEASURED_PEAKS.json hbm_gbs"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s", "launch_ms": attn_mean},
+        "roofline": roof,
         "path_roofline": {"bytes_per_step": step_bytes, "achieved_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
                           "frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak},
         "stage_ms": {"schedule": statistics.mean(sched_ms), "attention": statistics.mean(attn_ms),
                      "combine": statistics.mean(comb_ms)},
         "selected_pair_tflops": world * 4.0 * 128 * D * G * E / (ms_per_step * 1e-3) / 1e12,
-        "gpu_launches": kernels_per_step(cfg) * args.steps,
+        "gpu_launches": (1 if tiles else kernels_per_step(cfg)) * args.steps,
         "clocks": clock_info,
         "e2e": e2e,
         "cpu_baseline": cpu,
