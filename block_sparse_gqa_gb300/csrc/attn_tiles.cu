@@ -142,20 +142,22 @@ __device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
 // negations when the scale is negative.
 template <bool kMasked>
 __device__ __forceinline__ float row_max(const uint32_t (&v)[128], int lim, bool neg) {
-  float a0 = -FLT_MAX, a1 = -FLT_MAX;
+  // eight independent chains of 3-input maxima (short dependency chains)
+  float a[8];
 #pragma unroll
-  for (int e = 0; e < 128; e += 4) {
-    float x[4];
+  for (int q = 0; q < 8; ++q) a[q] = -FLT_MAX;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float sv = __uint_as_float(v[e + q]);
-      x[q] = neg ? -sv : sv;
-      if (kMasked && e + q > lim) x[q] = -FLT_MAX;
+  for (int e = 0; e < 128; e += 16) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float x0 = __uint_as_float(v[e + 2 * q]), x1 = __uint_as_float(v[e + 2 * q + 1]);
+      if (neg) { x0 = -x0; x1 = -x1; }
+      if (kMasked && e + 2 * q > lim) x0 = -FLT_MAX;
+      if (kMasked && e + 2 * q + 1 > lim) x1 = -FLT_MAX;
+      a[q] = max3(a[q], x0, x1);
     }
-    a0 = max3(a0, x[0], x[1]);
-    a1 = max3(a1, x[2], x[3]);
   }
-  return fmaxf(a0, a1);
+  return fmaxf(fmaxf(max3(a[0], a[1], a[2]), max3(a[3], a[4], a[5])), fmaxf(a[6], a[7]));
 }
 
 // P = 2^(s * sl2 - m_ref) written over S as bf16 pairs (keys c > lim get 0 when
@@ -163,7 +165,7 @@ __device__ __forceinline__ float row_max(const uint32_t (&v)[128], int lim, bool
 template <bool kMasked>
 __device__ __forceinline__ float row_exp(const uint32_t (&v)[128], int lim, float sl2, float m_ref, uint32_t tS) {
   const uint64_t sl2x2 = pack2(sl2, sl2), negm2 = pack2(-m_ref, -m_ref);
-  uint64_t s0 = 0, s1 = 0;
+  uint64_t sa[4] = {0, 0, 0, 0};  // four independent packed sums
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     uint32_t pk[8];
@@ -177,8 +179,7 @@ __device__ __forceinline__ float row_exp(const uint32_t (&v)[128], int lim, floa
         if (col > lim) p0 = 0.f;
         if (col + 1 > lim) p1 = 0.f;
       }
-      if ((e >> 1) & 1) s1 = fadd2(s1, pack2(p0, p1));
-      else s0 = fadd2(s0, pack2(p0, p1));
+      sa[(e >> 1) & 3] = fadd2(sa[(e >> 1) & 3], pack2(p0, p1));
       pk[e >> 1] = pack_bf16x2(p0, p1);
     }
     asm volatile(
@@ -186,10 +187,10 @@ __device__ __forceinline__ float row_exp(const uint32_t (&v)[128], int lim, floa
         "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7])
         : "memory");
   }
-  float l0, l1, l2, l3;
-  unpack2(s0, l0, l1);
-  unpack2(s1, l2, l3);
-  return (l0 + l1) + (l2 + l3);
+  float l[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) unpack2(sa[q], l[2 * q], l[2 * q + 1]);
+  return ((l[0] + l[1]) + (l[2] + l[3])) + ((l[4] + l[5]) + (l[6] + l[7]));
 }
 
 template <uint32_t N>
