@@ -58,6 +58,9 @@ def _load():
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
         lib.oracle_dispatch.restype = i32
         lib.oracle_dispatch.argtypes = [ctypes.c_int32, i32]
+        lib.oracle_attn_bwd.restype = i32
+        lib.oracle_attn_bwd.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f64,
+                                        P, i32, P, P, i32, P, P, i32]
         lib.oracle_select_r1.restype = i32
         lib.oracle_select_r1.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, P, P]
         _lib = lib
@@ -110,6 +113,49 @@ def attn_fwd(Q, K, V, indices, *, Lkv, block=128, scale, q_descale=1.0, k_descal
     if st < 0:
         raise ValueError("oracle_attn_fwd rejected its arguments")
     return O, LSE, st
+
+
+def attn_bwd(Q, K, V, dO, indices, *, Lkv, block=128, scale, qids=None, rows=None, nthreads=None):
+    """Gradients of the forward's O contracted with dO (float64).
+
+    Q, dO [N,Hq,D], K/V [Lkv,Hkv,D] as bf16 bit patterns (uint16) or float64;
+    indices [N,Hkv,topK] int32.  Returns (dQ, dK, dV, status): dQ [nq,Hq,D] for the
+    queries ``qids`` (default all; ``qids=()`` skips dQ); dK and dV for the schedule
+    rows ``rows`` (row r = g * nblocks + b, default all; ``rows=()`` skips them) as
+    [nrows, block, D], or as [Lkv, Hkv, D] when ``rows`` is None.
+    """
+    lib = _load()
+    Q, K, V, dO = (np.ascontiguousarray(a) for a in (Q, K, V, dO))
+    fmt = _fmt_of(Q)
+    if any(_fmt_of(a) != fmt for a in (K, V, dO)) or fmt == FMT_E4M3:
+        raise TypeError("Q, K, V and dO must share one storage format (bf16 bits or float64)")
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    N, Hq, D = Q.shape
+    Hkv = K.shape[1]
+    topK = indices.shape[2]
+    nblocks = Lkv // block
+    assert K.shape == (Lkv, Hkv, D) and V.shape == K.shape and dO.shape == Q.shape
+    assert indices.shape == (N, Hkv, topK)
+    full_rows = rows is None
+    qids = np.arange(N, dtype=np.int32) if qids is None else np.ascontiguousarray(qids, dtype=np.int32)
+    rows = np.arange(Hkv * nblocks, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    nq, nr = len(qids), len(rows)
+    dQ = np.zeros((nq, Hq, D), np.float64)
+    dK = np.zeros((nr, block, D), np.float64)
+    dV = np.zeros((nr, block, D), np.float64)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    st = lib.oracle_attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), fmt, _ptr(indices), N, Lkv, Hq, Hkv, D,
+                             topK, block, float(scale), _ptr(qids), nq, _ptr(dQ) if nq else None,
+                             _ptr(rows), nr, _ptr(dK) if nr else None, _ptr(dV) if nr else None,
+                             int(nthreads))
+    if st < 0:
+        raise ValueError("oracle_attn_bwd rejected its arguments")
+    if full_rows:
+        # row r = g * nblocks + b holds keys b*block.. of group g
+        dK = dK.reshape(Hkv, nblocks, block, D).transpose(1, 2, 0, 3).reshape(Lkv, Hkv, D)
+        dV = dV.reshape(Hkv, nblocks, block, D).transpose(1, 2, 0, 3).reshape(Lkv, Hkv, D)
+    return dQ, dK, dV, st
 
 
 def schedule(indices, *, Lkv, block=128):

@@ -396,3 +396,197 @@ int oracle_select_r1(const void* Q, const void* K, int fmt, int N, int Lkv, int 
   free(used);
   return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * Backward of the forward above.  "Flash-MSA: accelerating million-token training
+ * with sparse attention", order of operations: the forward keeps its block indices and
+ * its log-sum-exp for the backward, which computes the main-attention gradients over
+ * the same cached blocks.  The page gives no formula; the oracle takes the plain
+ * reading: the exact gradients of the forward's O with respect to Q, K and V,
+ * contracted with a given dL/dO.  For one (query i, head h) with visible key set J
+ * (built exactly as in the forward) and softmax weights p_j over J:
+ *   dp_j = dO[i,h] . v_j,   c = sum_j p_j dp_j,   ds_j = p_j (dp_j - c)
+ *   dQ[i,h] = scale * sum_j ds_j k_j,   dK_j += scale * ds_j q[i,h],   dV_j += p_j dO[i,h].
+ * The softmax is recomputed here from Q and K (the oracle takes no LSE).  bf16 or
+ * float64 inputs (no E4M3).
+ *
+ * dQ is returned for the queries qids[0..nq) ([nq,Hq,D]); dK and dV for the schedule
+ * rows rows[0..nrows) (row r = g * nblocks + b: keys b*block .. b*block+block-1 of
+ * group g), as [nrows, block, D].  Either part may be skipped with a NULL output.
+ * Work is split statically over threads, and per-thread dK/dV sums are added in
+ * thread order, so results do not depend on timing. */
+typedef struct {
+  const void *Q, *K, *V, *dO;
+  int fmt;
+  const int32_t* indices;
+  int N, Lkv, Hq, Hkv, D, topK, block;
+  double scale;
+  const int32_t* qids;
+  int nq;
+  double* dQ;
+  const int32_t* rows;
+  int nrows;
+  int32_t* row_of; /* [Hkv*nblocks] -> index into rows, or -1 */
+  int nthreads;
+  int bad;
+} bwd_job;
+
+typedef struct {
+  bwd_job* J;
+  int t;
+  double *dK, *dV; /* thread-private [nrows, block, D] */
+} bwd_worker_arg;
+
+/* Visible keys of (i, g) over the union of its selected blocks (as in attn_one). */
+static int bwd_keys(bwd_job* J, int i, int g, int* keys) {
+  const int nblocks = J->Lkv / J->block;
+  const long pos = (long)J->Lkv - J->N + i;
+  const long lb = pos / J->block;
+  const int32_t* lst = J->indices + ((size_t)i * J->Hkv + g) * J->topK;
+  int nkeys = 0;
+  for (int k = 0; k < J->topK; ++k) {
+    int b = lst[k];
+    if (b < -1 || b >= nblocks) { J->bad = 1; continue; }
+    if (b == -1 || b > lb) continue;
+    int dup = 0;
+    for (int k2 = 0; k2 < k; ++k2) if (lst[k2] == b) { dup = 1; break; }
+    if (dup) continue;
+    for (int t = 0; t < J->block; ++t) {
+      long j = (long)b * J->block + t;
+      if (j <= pos) keys[nkeys++] = (int)j;
+    }
+  }
+  return nkeys;
+}
+
+/* p_j and ds_j of (i, h) over its visible keys; q and dO of (i, h) are loaded too. */
+static void bwd_row(bwd_job* J, int i, int h, const int* keys, int nkeys, double* q, double* go,
+                    double* p, double* ds) {
+  const int G = J->Hq / J->Hkv, g = h / G, D = J->D;
+  for (int d = 0; d < D; ++d) {
+    q[d] = load_elem(J->Q, J->fmt, ((size_t)i * J->Hq + h) * D + d);
+    go[d] = load_elem(J->dO, J->fmt, ((size_t)i * J->Hq + h) * D + d);
+  }
+  double m = -INFINITY;
+  for (int t = 0; t < nkeys; ++t) {
+    size_t kb = ((size_t)keys[t] * J->Hkv + g) * D;
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d) acc += q[d] * load_elem(J->K, J->fmt, kb + d);
+    p[t] = J->scale * acc;
+    if (p[t] > m) m = p[t];
+  }
+  double l = 0.0;
+  for (int t = 0; t < nkeys; ++t) { p[t] = exp(p[t] - m); l += p[t]; }
+  double c = 0.0;
+  for (int t = 0; t < nkeys; ++t) {
+    p[t] /= l;
+    size_t vb = ((size_t)keys[t] * J->Hkv + g) * D;
+    double acc = 0.0;
+    for (int d = 0; d < D; ++d) acc += go[d] * load_elem(J->V, J->fmt, vb + d);
+    ds[t] = acc; /* dp_j for now */
+    c += p[t] * acc;
+  }
+  for (int t = 0; t < nkeys; ++t) ds[t] = p[t] * (ds[t] - c);
+}
+
+static void* bwd_worker(void* arg) {
+  bwd_worker_arg* A = (bwd_worker_arg*)arg;
+  bwd_job* J = A->J;
+  const int G = J->Hq / J->Hkv, D = J->D, maxkeys = J->topK * J->block;
+  double* q = (double*)malloc(sizeof(double) * D);
+  double* go = (double*)malloc(sizeof(double) * D);
+  double* p = (double*)malloc(sizeof(double) * maxkeys);
+  double* ds = (double*)malloc(sizeof(double) * maxkeys);
+  int* keys = (int*)malloc(sizeof(int) * maxkeys);
+  /* dQ of the requested queries */
+  if (J->dQ)
+    for (int r = A->t; r < J->nq; r += J->nthreads) {
+      const int i = J->qids[r];
+      for (int h = 0; h < J->Hq; ++h) {
+        const int g = h / G;
+        int nkeys = bwd_keys(J, i, g, keys);
+        double* out = J->dQ + ((size_t)r * J->Hq + h) * D;
+        for (int d = 0; d < D; ++d) out[d] = 0.0;
+        if (nkeys == 0) continue;
+        bwd_row(J, i, h, keys, nkeys, q, go, p, ds);
+        for (int t = 0; t < nkeys; ++t) {
+          size_t kb = ((size_t)keys[t] * J->Hkv + g) * D;
+          for (int d = 0; d < D; ++d) out[d] += J->scale * ds[t] * load_elem(J->K, J->fmt, kb + d);
+        }
+      }
+    }
+  /* dK / dV of the requested rows: every query (statically split) adds what its
+   * visible keys in those rows receive */
+  if (A->dK)
+    for (int i = A->t; i < J->N; i += J->nthreads)
+      for (int g = 0; g < J->Hkv; ++g) {
+        int nkeys = bwd_keys(J, i, g, keys);
+        int any = 0;
+        for (int t = 0; t < nkeys && !any; ++t) any = J->row_of[g * (J->Lkv / J->block) + keys[t] / J->block] >= 0;
+        if (!any) continue;
+        for (int h = g * G; h < (g + 1) * G; ++h) {
+          bwd_row(J, i, h, keys, nkeys, q, go, p, ds);
+          for (int t = 0; t < nkeys; ++t) {
+            const int b = keys[t] / J->block, ro = J->row_of[g * (J->Lkv / J->block) + b];
+            if (ro < 0) continue;
+            const size_t o = ((size_t)ro * J->block + (keys[t] - b * J->block)) * D;
+            for (int d = 0; d < D; ++d) {
+              A->dK[o + d] += J->scale * ds[t] * q[d];
+              A->dV[o + d] += p[t] * go[d];
+            }
+          }
+        }
+      }
+  free(q); free(go); free(p); free(ds); free(keys);
+  return NULL;
+}
+
+/* Returns 0, 1 if an invalid block id was seen (ignored), or -1 on bad arguments. */
+int oracle_attn_bwd(const void* Q, const void* K, const void* V, const void* dO, int fmt,
+                    const int32_t* indices, int N, int Lkv, int Hq, int Hkv, int D, int topK,
+                    int block, double scale, const int32_t* qids, int nq, double* dQ,
+                    const int32_t* rows, int nrows, double* dK, double* dV, int nthreads) {
+  if (!Q || !K || !V || !dO || !indices || fmt == ORC_IN_E4M3) return -1;
+  if (N < 0 || Lkv <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || topK <= 0 || block <= 0) return -1;
+  if (Hq % Hkv != 0 || Lkv % block != 0 || N > Lkv) return -1;
+  if ((dQ && (!qids || nq < 0)) || ((dK != NULL) != (dV != NULL)) || (dK && (!rows || nrows < 0))) return -1;
+  const int R = Hkv * (Lkv / block);
+  for (int r = 0; dQ && r < nq; ++r)
+    if (qids[r] < 0 || qids[r] >= N) return -1;
+  bwd_job J;
+  memset(&J, 0, sizeof J);
+  J.Q = Q; J.K = K; J.V = V; J.dO = dO; J.fmt = fmt; J.indices = indices;
+  J.N = N; J.Lkv = Lkv; J.Hq = Hq; J.Hkv = Hkv; J.D = D; J.topK = topK; J.block = block;
+  J.scale = scale; J.qids = qids; J.nq = dQ ? nq : 0; J.dQ = dQ; J.rows = rows; J.nrows = dK ? nrows : 0;
+  J.row_of = (int32_t*)malloc(sizeof(int32_t) * R);
+  for (int r = 0; r < R; ++r) J.row_of[r] = -1;
+  for (int k = 0; k < J.nrows; ++k) {
+    if (rows[k] < 0 || rows[k] >= R || J.row_of[rows[k]] >= 0) { free(J.row_of); return -1; }
+    J.row_of[rows[k]] = k;
+  }
+  if (nthreads < 1) nthreads = 1;
+  J.nthreads = nthreads;
+  const size_t per = (size_t)J.nrows * block * D;
+  bwd_worker_arg* args = (bwd_worker_arg*)calloc(nthreads, sizeof(bwd_worker_arg));
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
+  for (int t = 0; t < nthreads; ++t) {
+    args[t].J = &J;
+    args[t].t = t;
+    if (dK) {
+      args[t].dK = (double*)calloc(per > 0 ? per : 1, sizeof(double));
+      args[t].dV = (double*)calloc(per > 0 ? per : 1, sizeof(double));
+    }
+    pthread_create(&th[t], NULL, bwd_worker, &args[t]);
+  }
+  for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+  if (dK) {
+    for (size_t e = 0; e < per; ++e) { dK[e] = 0.0; dV[e] = 0.0; }
+    for (int t = 0; t < nthreads; ++t) {
+      for (size_t e = 0; e < per; ++e) { dK[e] += args[t].dK[e]; dV[e] += args[t].dV[e]; }
+      free(args[t].dK);
+      free(args[t].dV);
+    }
+  }
+  free(args); free(th); free(J.row_of);
+  return J.bad ? 1 : 0;
+}
