@@ -66,6 +66,9 @@ def lib() -> ctypes.CDLL:
         L.msa_build_schedule.argtypes = [P, I, I, I, I, P, ctypes.POINTER(P)]
         L.msa_sparse_attn_fwd.restype = I
         L.msa_sparse_attn_fwd.argtypes = [Tensor, Tensor, Tensor, P, P, P, ctypes.c_float, ctypes.POINTER(FwdOpts)]
+        L.msa_sparse_attn_bwd.restype = I
+        L.msa_sparse_attn_bwd.argtypes = [Tensor, Tensor, Tensor, P, P, P, P, P, P, P, ctypes.c_float,
+                                          ctypes.POINTER(FwdOpts)]
         L.msa_schedule_destroy.restype = I
         L.msa_schedule_destroy.argtypes = [P]
         L.msa_schedule_query.restype = I
@@ -172,6 +175,34 @@ def build_schedule(indices: torch.Tensor, nblocks: int, schedule: Schedule | Non
     if schedule is not None:
         return schedule
     return Schedule(h.value, N, Hkv, topK, nblocks)
+
+
+def sparse_attn_bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor, dO: torch.Tensor,
+                    LSE: torch.Tensor, schedule: Schedule, scale: float | None = None, dQ: torch.Tensor | None = None,
+                    dK: torch.Tensor | None = None, dV: torch.Tensor | None = None, num_ctas: int = 0, stream=None):
+    """msa_sparse_attn_bwd; returns (dQ bf16 [N,Hq,D], dK bf16 [Lkv,Hkv,D], dV bf16 [Lkv,Hkv,D])."""
+    N, Hq, D = Q.shape
+    if scale is None:
+        scale = D ** -0.5
+    for name, t, shape, dt in (("O", O, Q.shape, torch.bfloat16), ("dO", dO, Q.shape, torch.bfloat16),
+                               ("LSE", LSE, (N, Hq), torch.float32)):
+        if not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(shape) or t.dtype != dt:
+            raise ValueError(f"{name} must be a contiguous {dt} CUDA tensor of shape {tuple(shape)}")
+    if dQ is None:
+        dQ = torch.empty_like(Q, dtype=torch.bfloat16)
+    if dK is None:
+        dK = torch.empty(K.shape, dtype=torch.bfloat16, device=K.device)
+    if dV is None:
+        dV = torch.empty(V.shape, dtype=torch.bfloat16, device=V.device)
+    opts = FwdOpts()
+    lib().msa_fwd_opts_init(ctypes.byref(opts))
+    opts.stream = _stream_ptr(stream)
+    opts.num_ctas = int(num_ctas)
+    st = lib().msa_sparse_attn_bwd(_tensor(Q), _tensor(K), _tensor(V), O.data_ptr(), dO.data_ptr(), LSE.data_ptr(),
+                                   schedule.handle, dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), float(scale),
+                                   ctypes.byref(opts))
+    _check(st, "msa_sparse_attn_bwd")
+    return dQ, dK, dV
 
 
 def sparse_attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, schedule: Schedule, scale: float | None = None,

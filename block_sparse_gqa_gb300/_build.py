@@ -12,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmsa.so")
 SOURCES = ["msa_api.cu", "schedule.cu", "attn_kv_outer.cu", "combine.cu", "attn_q_outer.cu", "msa_noalloc.cu",
-           "select.cu", "attn_tiles.cu"]
+           "select.cu", "attn_tiles.cu", "attn_bwd.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("ptx.cuh", "msa_internal.h")] + [os.path.join(ROOT, "include", "msa.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -234,10 +234,48 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
   return MSA_OK;
 }
 
+msa_status_t msa_sparse_attn_bwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, const void* O, const void* dO,
+                                 const float* LSE, msa_schedule_t s, void* dQ, void* dK, void* dV, float scale,
+                                 const msa_fwd_opts_t* opts) {
+  msa_fwd_opts_t def;
+  if (!opts) {
+    msa_fwd_opts_init(&def);
+    opts = &def;
+  }
+  if (!s || !Q.ptr || !K.ptr || !V.ptr || !O || !dO || !LSE || !dQ || !dK || !dV) return MSA_ERR_INVALID_ARG;
+  for (const void* p : {Q.ptr, K.ptr, V.ptr, O, dO, static_cast<const void*>(LSE), static_cast<const void*>(dQ),
+                        static_cast<const void*>(dK), static_cast<const void*>(dV)})
+    if (!aligned16(p)) return MSA_ERR_INVALID_ARG;
+  if (Q.n != s->N || K.n != static_cast<int64_t>(s->nblocks) * msa::kBlock || V.n != K.n) return MSA_ERR_INVALID_ARG;
+  if (K.h != s->Hkv || V.h != s->Hkv || Q.h < 1 || Q.h % K.h != 0) return MSA_ERR_INVALID_ARG;
+  if (Q.d != K.d || K.d != V.d) return MSA_ERR_INVALID_ARG;
+  if (Q.dtype != MSA_BF16 || K.dtype != MSA_BF16 || V.dtype != MSA_BF16) return MSA_ERR_UNSUPPORTED;
+  if (Q.d != msa::kHeadDim || Q.h / K.h != msa::kGroup) return MSA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return MSA_ERR_INVALID_ARG;
+  if (opts->path == MSA_PATH_Q_OUTER) return MSA_ERR_UNSUPPORTED;
+  if (opts->path != MSA_PATH_AUTO && opts->path != MSA_PATH_KV_OUTER) return MSA_ERR_INVALID_ARG;
+  msa_status_t st = ensure_partials(s, msa::kGroup);
+  if (st != MSA_OK) return st;
+  if (!s->bwd_ws) {
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, msa::bwd_workspace_bytes(s));
+    if (e != cudaSuccess) return from_cuda(e);
+    s->bwd_ws = p;
+  }
+  const int ctas = opts->num_ctas > 0 ? opts->num_ctas : device_sms();
+  if (ctas < 1) return MSA_ERR_CUDA;
+  msa::BwdArgs a{s, Q.ptr, K.ptr, V.ptr, O, dO, LSE, dQ, dK, dV, s->bwd_ws, static_cast<int>(Q.h),
+                 s->nblocks * msa::kBlock, scale, ctas};
+  cudaError_t e = msa::launch_bwd(a, opts->stream);
+  s->last_stream = opts->stream;
+  return from_cuda(e);
+}
+
 msa_status_t msa_schedule_destroy(msa_schedule_t s) {
   if (!s) return MSA_ERR_INVALID_ARG;
   cudaError_t e = cudaStreamSynchronize(s->last_stream);
   if (s->partial) cudaFree(s->partial);
+  if (s->bwd_ws) cudaFree(s->bwd_ws);
   if (s->dev_base) cudaFree(s->dev_base);
   delete s;
   return from_cuda(e);

@@ -61,6 +61,7 @@ struct msa_schedule {
   void* partial;       // bf16 [cap_entries * G, D]: raw P V of each (entry, head) row
   float2* pstat;       // [cap_entries * G]: (m, l) of each partial row, m in base-2 units
   int partial_G;
+  void* bwd_ws;  // backward workspace (first backward call)
   cudaStream_t last_stream;
 };
 
@@ -110,6 +111,28 @@ cudaError_t launch_select_r1(const void* Q, const void* K, int N, int Lkv, int H
 cudaError_t launch_tiles(const void* Q, const void* K, const void* V, int N, int Lkv, int Hq, int Hkv,
                          const int32_t* lists, int tile, int topK, float scale, void* O, float* LSE, int32_t* status,
                          int num_ctas, cudaStream_t st);
+
+// attn_bwd.cu: backward (dQ, dK, dV) over the schedule of the forward
+constexpr int kUnitEntries = 256;  // entries per KV-stationary backward unit (32 tiles)
+struct BwdArgs {
+  const msa_schedule* s;
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* O;
+  const void* dO;
+  const float* LSE;
+  void* dQ;
+  void* dK;
+  void* dV;
+  void* workspace;  // bwd_workspace_bytes(s), 256-byte aligned
+  int Hq, Lkv;
+  float scale;
+  int num_ctas;
+};
+int64_t bwd_unit_capacity(const msa_schedule* s);
+size_t bwd_workspace_bytes(const msa_schedule* s);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st);
 
 // tensor maps (msa_api.cpp)
 bool encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,

@@ -138,6 +138,46 @@ msa_status_t msa_build_schedule(const int32_t* indices, int N, int Hkv, int topK
 msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, msa_schedule_t s,
                                  void* O, float* LSE, float scale, const msa_fwd_opts_t* opts);
 
+/*
+ * msa_sparse_attn_bwd -- gradients of the forward main branch over the same schedule.
+ *
+ * "Flash-MSA: accelerating million-token training with sparse attention", order of
+ * operations: the forward keeps its block indices and its log-sum-exp for the
+ * backward, which computes the main-attention gradients over the cached blocks.  For
+ * each (query i, head h) with visible keys J (the union of its selected blocks,
+ * causal): P_j = exp(scale * q.k_j - LSE[i,h]), D = dO[i,h] . O[i,h],
+ * dS_j = P_j (dO[i,h] . v_j - D); dQ[i,h] = scale * sum_j dS_j k_j,
+ * dK_j += scale * dS_j q[i,h], dV_j += P_j dO[i,h].  Keys no query sees get 0.
+ *
+ * Kernels, all on opts->stream with no host synchronisation: D = rowsum(dO * O);
+ * units of at most 256 entries of one (group, block) row of the schedule; a
+ * KV-stationary tcgen05 kernel that holds K_b, V_b, gathers Q and dO of 8 queries x 16
+ * heads per tile, forms P and dS on chip, accumulates dK_b, dV_b in tensor memory and
+ * writes each entry's dQ contribution (bf16) to the schedule's partial workspace;
+ * a reduction of the units' dK/dV (fp32) and a gather of each query's dQ
+ * contributions, both in a fixed order (results are deterministic).
+ *
+ * Q, dO: bf16 [N, Hq, D]; K, V: bf16 [Lkv, Hkv, D]; O: bf16 [N, Hq, D] and LSE: fp32
+ * [N, Hq] (natural log) from msa_sparse_attn_fwd on the same inputs and schedule (s
+ * must still hold the lists the forward used).  Outputs dQ: bf16 [N, Hq, D]; dK, dV:
+ * bf16 [Lkv, Hkv, D]; all device pointers, 16-byte aligned, caller-owned.  scale is the
+ * forward's.  opts may be NULL; opts->stream and opts->num_ctas are used, opts->path
+ * must be AUTO or KV_OUTER.
+ *
+ * The first call allocates the schedule's partial-output workspace (if the forward
+ * has not) and a backward workspace (cudaMalloc, synchronous): N*Hq*4 bytes for D,
+ * and 128 KiB of fp32 dK/dV per unit for at most min(Hkv*nblocks, N*Hkv*topK) +
+ * N*Hkv*topK/256 units.  Later calls allocate nothing.
+ *
+ * Returns MSA_ERR_INVALID_ARG on null or misaligned pointers or shapes inconsistent
+ * with the schedule; MSA_ERR_UNSUPPORTED for E4M3, D != 128, G != 16 or a forced
+ * Q-outer path; MSA_ERR_OOM / MSA_ERR_CUDA on allocation or launch failure.  A device
+ * wait that exceeds its bound sets the schedule's timeout flag (msa_schedule_query).
+ */
+msa_status_t msa_sparse_attn_bwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, const void* O, const void* dO,
+                                 const float* LSE, msa_schedule_t s, void* dQ, void* dK, void* dV, float scale,
+                                 const msa_fwd_opts_t* opts);
+
 /* Frees the schedule's device memory (synchronises its last stream first). */
 msa_status_t msa_schedule_destroy(msa_schedule_t s);
 

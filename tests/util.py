@@ -51,3 +51,12 @@ def check_worklist(exp, ref, N):
     assert np.all(win_of_q[ent] == np.repeat(w, cnt))
     key = (w * (R + 1) + row) * (E + 1) + first
     assert np.all(np.diff(key) > 0)
+
+# Backward (bf16 inputs and outputs, fp32 accumulation, bf16 P / dS operands and bf16
+# per-block dQ contributions) against the fp64 oracle: relative L2 per gradient tensor.
+BWD_REL_L2 = 2e-2
+
+
+def rel_l2(x, ref):
+    x = np.asarray(x, np.float64)
+    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-30))
