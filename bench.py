@@ -32,6 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "sparse-attn fwd useful TFLOP/s and % HBM roofline, M3 shape top16, 1 GB300"
+METRIC_BWD = "sparse-attn bwd useful TFLOP/s (dQ, dK, dV; 2.5x the forward's nominal FLOPs), M3 shape top16, 1 GB300"
 
 
 def kernels_per_step(cfg):
@@ -52,9 +53,10 @@ def parse_args():
     ap.add_argument("--workload", default="m3", choices=["tiny", "m3", "long", "lowreuse", "fp8"])
     ap.add_argument("--lists", default="workload", choices=["workload", "r1"],
                     help="block lists: the workload's own, or chosen by the R1 selector (once, before timing)")
-    ap.add_argument("--mode", default="general", choices=["general", "tiles"],
+    ap.add_argument("--mode", default="general", choices=["general", "tiles", "bwd"],
                     help="general: schedule + attention + combine; tiles: the shared-list forward "
-                         "(lists shared by 128 queries for r1, by the workload's query runs otherwise)")
+                         "(lists shared by 128 queries for r1, by the workload's query runs otherwise); "
+                         "bwd: the backward (dQ, dK, dV) over the forward's schedule, O and LSE")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -188,6 +190,35 @@ def time_oracle(wl, seconds, seed=0, indices=None):
     t = run(nq)
     flops = 4.0 * nq * cfg.Hq * cfg.topK * 128 * cfg.D
     sample = f"{nq} of {cfg.N} queries (seeded uniform sample), all {cfg.Hq} heads, {cfg.name} lists"
+    return flops / t / 1e12, sample, threads, t
+
+
+def time_oracle_bwd(wl, dO_bits, seconds, seed=0):
+    """The oracle's backward for the dQ of a seeded query sample sized for ~`seconds`:
+    per (query, head) it forms S, dP and dQ over the selected keys, 3 of the 5 products
+    of the backward, so the useful FLOPs counted are 6 * nq * Hq * topK * 128 * D."""
+    import numpy as np
+    import oracle
+    cfg = wl.cfg
+    threads = os.cpu_count() or 1
+    Qn, Kn, Vn = wl.np_inputs()
+    idx = wl.indices.numpy()
+    rng = np.random.default_rng(seed)
+
+    def run(nq):
+        qids = np.sort(rng.choice(cfg.N, size=nq, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.attn_bwd(Qn, Kn, Vn, dO_bits, idx, Lkv=cfg.Lkv, scale=cfg.scale, qids=qids, rows=(),
+                        nthreads=threads)
+        return time.perf_counter() - t0
+
+    probe_n = min(16, cfg.N)
+    tp = run(probe_n)
+    nq = int(min(cfg.N, max(probe_n, probe_n * seconds / max(tp, 1e-6))))
+    t = run(nq)
+    flops = 6.0 * nq * cfg.Hq * cfg.topK * 128 * cfg.D
+    sample = (f"dQ of {nq} of {cfg.N} queries (seeded uniform sample), all {cfg.Hq} heads, {cfg.name} lists; "
+              "S, dP and dQ products counted")
     return flops / t / 1e12, sample, threads, t
 
 
@@ -374,6 +405,16 @@ def run_ours(args, world, rank, local, pg):
     LSE = torch.empty((cfg.N, cfg.Hq), dtype=torch.float32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     sched = msa.build_schedule(idx_d, cfg.nblocks)
+    bwd = args.mode == "bwd"
+    if bwd:
+        if cfg.dtype != "bf16" or args.lists != "workload":
+            raise SystemExit("--mode bwd takes the bf16 workloads with their own lists")
+        gen = torch.Generator().manual_seed(cfg.seed + 77 + 1000 * rank)
+        dO_h = torch.randn((cfg.N, cfg.Hq, cfg.D), generator=gen).to(torch.bfloat16)
+        dO = dO_h.to(dev)
+        # the forward whose schedule, O and LSE the backward takes (outside the timed steps)
+        msa.sparse_attn_fwd(Q, K, V, sched, scale=cfg.scale, O=O, LSE=LSE)
+        dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
 
     def new_events(n):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -384,6 +425,10 @@ def run_ours(args, world, rank, local, pg):
     descales = (wl.q_descale, wl.k_descale, wl.v_descale)
 
     def step(stage):
+        if bwd:
+            msa.sparse_attn_bwd(Q, K, V, O, dO, LSE, sched, scale=cfg.scale, dQ=dQ, dK=dK, dV=dV,
+                                stage_events=[e.cuda_event for e in stage] if stage else None)
+            return
         if tiles:
             if stage:
                 stage[0].record(stream)
@@ -401,7 +446,7 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.synchronize()
     info = sched.query()
     assert info["status"] == 0, info
-    kv_path = info["path"] == 1 or tiles  # else the Q-outer kernel runs (inside the third stage)
+    kv_path = info["path"] == 1 or tiles or bwd  # else the Q-outer kernel runs (inside the third stage)
 
     starts, ends = new_events(args.steps), new_events(args.steps)
     stages = [new_events(3) for _ in range(args.steps)]
@@ -431,7 +476,8 @@ def run_ours(args, world, rank, local, pg):
     sched_ms = [s.elapsed_time(st[0]) for s, st in zip(starts, stages)]
     total_ms = max_over_ranks(pg, sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
-    value = world * cfg.nominal_flops() / (ms_per_step * 1e-3) / 1e12
+    nominal = cfg.nominal_flops() * (2.5 if bwd else 1.0)  # the backward runs 5 products to the forward's 2
+    value = world * nominal / (ms_per_step * 1e-3) / 1e12
 
     # algorithmic bytes ("Roofline"): attention kernel and whole step
     E, nsb, T = info["entries"], info["nsb"], info["ntiles"]
@@ -471,14 +517,33 @@ def run_ours(args, world, rank, local, pg):
                 "unit": "TFLOP/s", "frac": achieved_t / tpeak, "traffic": None, "algorithmic_flops": flops,
                 "peak_source": f"{tkind} MEASURED_PEAKS.json bf16_tflops_sustained", "launch_ms": attn_mean}
         step_bytes = q_bytes + kv_bytes + cfg.N * cfg.Hq * (2 * D + 4) + tile_lists.numel() * 4
+    if bwd:
+        # the KV-stationary backward kernel: five 128 x 128 x 128 products per tile (S, dP,
+        # dV, dK, dQ) over the selected pairs; bound by the tensor pipe and the chain
+        # between them.  Step bytes: Q, dO and O read once, LSE and D, the selected K/V
+        # blocks, the dQ contributions written and re-read, the units' fp32 dK/dV written
+        # and re-read, dQ, dK, dV written, the lists.
+        flops = 10.0 * 128 * D * G * E
+        tpeak, tkind = load_peaks("bf16_tflops_sustained")
+        achieved_t = flops / (attn_mean * 1e-3) / 1e12
+        roof = {"kernel": "bwd_kv_kernel", "bound": "tensor", "achieved": achieved_t, "peak": tpeak,
+                "unit": "TFLOP/s", "frac": achieved_t / tpeak, "traffic": None, "algorithmic_flops": flops,
+                "peak_source": f"{tkind} MEASURED_PEAKS.json bf16_tflops_sustained", "launch_ms": attn_mean}
+        counts = sched.export()["counts"]
+        units = int(((counts + 255) // 256).sum())
+        step_bytes = (3 * q_bytes + cfg.N * cfg.Hq * 12 + kv_bytes + 2 * E * G * D * 2 + 2 * units * 2 * 128 * D * 4
+                      + q_bytes + 2 * cfg.Lkv * cfg.Hkv * D * 2 + E * 4 + cfg.N * cfg.Hkv * cfg.topK * 4)
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not bwd:
         e2e = time_e2e(args, msa, cfg, wl, dev, stream, tiles, tile_lists if tiles else idx_d,
                        tile if tiles else None, descales, flush, pg, world)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and bwd:
+        v, sample, threads, _ = time_oracle_bwd(wl, dO_h.view(torch.int16).numpy().view("uint16"), args.cpu_seconds)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample}
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, sample, threads, _ = time_oracle(wl, args.cpu_seconds, indices=idx_d.cpu().numpy())
         cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample}
 
@@ -486,7 +551,8 @@ def run_ours(args, world, rank, local, pg):
     if rank != 0:
         return
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)" if es == 1 else "bf16",
         "data": f"synthetic (seeded N(0,1) Q/K/V{', per-tensor E4M3' if es == 1 else ''}, {cfg.picks} block picks)",
@@ -494,16 +560,18 @@ def run_ours(args, world, rank, local, pg):
                                f"topK={cfg.topK}, causal, own block + up to {cfg.topK - 1} {cfg.picks} earlier blocks",
                    "l2": "flushed (256 MiB write) before every timed step, outside the step events",
                    "parallelism": f"independent problem per GPU x{world}",
-                   "path": "tiles" if tiles else ("kv_outer" if kv_path else "q_outer"),
+                   "path": "bwd" if bwd else "tiles" if tiles else ("kv_outer" if kv_path else "q_outer"),
                    "lists": "R1 selector (chosen once, before timing)" if args.lists == "r1" else "workload",
                    "entries": E, "nsb": nsb, "tiles": T},
         "roofline": roof,
         "path_roofline": {"bytes_per_step": step_bytes, "achieved_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
                           "frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak},
-        "stage_ms": {"schedule": statistics.mean(sched_ms), "attention": statistics.mean(attn_ms),
-                     "combine": statistics.mean(comb_ms)},
-        "selected_pair_tflops": world * 4.0 * 128 * D * G * E / (ms_per_step * 1e-3) / 1e12,
-        "gpu_launches": (1 if tiles else kernels_per_step(cfg)) * args.steps,
+        "stage_ms": ({"prep+units": statistics.mean(sched_ms), "bwd_kv": statistics.mean(attn_ms),
+                      "reduce+dq": statistics.mean(comb_ms)} if bwd else
+                     {"schedule": statistics.mean(sched_ms), "attention": statistics.mean(attn_ms),
+                      "combine": statistics.mean(comb_ms)}),
+        "selected_pair_tflops": world * (10.0 if bwd else 4.0) * 128 * D * G * E / (ms_per_step * 1e-3) / 1e12,
+        "gpu_launches": (5 if bwd else 1 if tiles else kernels_per_step(cfg)) * args.steps,
         "clocks": clock_info,
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -179,7 +179,8 @@ def build_schedule(indices: torch.Tensor, nblocks: int, schedule: Schedule | Non
 
 def sparse_attn_bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor, dO: torch.Tensor,
                     LSE: torch.Tensor, schedule: Schedule, scale: float | None = None, dQ: torch.Tensor | None = None,
-                    dK: torch.Tensor | None = None, dV: torch.Tensor | None = None, num_ctas: int = 0, stream=None):
+                    dK: torch.Tensor | None = None, dV: torch.Tensor | None = None, num_ctas: int = 0,
+                    stage_events=None, stream=None):
     """msa_sparse_attn_bwd; returns (dQ bf16 [N,Hq,D], dK bf16 [Lkv,Hkv,D], dV bf16 [Lkv,Hkv,D])."""
     N, Hq, D = Q.shape
     if scale is None:
@@ -198,6 +199,9 @@ def sparse_attn_bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.
     lib().msa_fwd_opts_init(ctypes.byref(opts))
     opts.stream = _stream_ptr(stream)
     opts.num_ctas = int(num_ctas)
+    if stage_events is not None:
+        for k, ev in enumerate(stage_events[:3]):
+            opts.stage_events[k] = ev
     st = lib().msa_sparse_attn_bwd(_tensor(Q), _tensor(K), _tensor(V), O.data_ptr(), dO.data_ptr(), LSE.data_ptr(),
                                    schedule.handle, dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), float(scale),
                                    ctypes.byref(opts))

@@ -22,16 +22,27 @@
 //   bwd_dq_kernel       dQ[i, g heads] = scale * sum of the entry partials of (i, g)
 // Every reduction runs in a fixed order, so results do not depend on scheduling.
 //
-// bwd_kv_kernel, one CTA of 256 threads per SM (persistent; units claimed with an
-// atomicAdd).  Shared memory (bf16 128 x 128 tiles, two 64-column halves with the
-// 128-byte swizzle): K_b, V_b (TMA), Q and dO of the tile (cp.async gathers), P and
-// dS (written by the threads).  The same physical tile layout is K-major for a matrix
-// and MN-major for its transpose, so P and dS serve both as P^T / dS^T (M = keys) and
-// as dS (M = rows); K_b is read K-major for S and MN-major for dQ.  TMEM (512
-// columns): S [0, 128) (later dQ), dP [128, 256), dV [256, 384), dK [384, 512).
-// Per tile: gather -> S, dP MMAs -> P, dS -> dV, dK, dQ MMAs -> dQ rows to global.
-// Thread (warp w, lane) owns MMA row / TMEM lane 32 (w % 4) + lane and the column
-// half w / 4.
+// bwd_kv_kernel, one CTA of 512 threads per SM, persistent (units claimed with an
+// atomicAdd).  It works on the transposed products so that the block's keys sit on the
+// TMEM lanes: S^T = K_b Q^T and dP^T = V_b dO^T (M = keys, N = the tile's 128 rows);
+// P^T = exp2(S^T * scale * log2 e - LSE * log2 e) and dS^T = P^T (dP^T - D) are written
+// back to TMEM as bf16 and feed dV += P^T dO and dK += dS^T Q directly as the A operand
+// (A read from TMEM); dS also goes to shared memory (rows contiguous per key, i.e. the
+// MN-major A layout of dS with M = rows) for dQ = dS K_b, which lands in the columns
+// dP^T held.  TMEM (512 columns): [0, 128) S^T -> P^T / dS^T (bf16 pairs), [128, 256)
+// dP^T -> dQ, [256, 384) dV, [384, 512) dK.  Shared memory: K_b, V_b (TMA), Q and dO in
+// two stages (TMA: one 2 KB box per query and D half), dS; bf16 128 x 128 tiles of two
+// 64-column halves with the 128-byte swizzle, so one tile is K-major for a matrix and
+// MN-major for its transpose.  Warp roles:
+//   warp 0      producer: claims units, loads K_b / V_b and gathers Q / dO of each tile
+//               into the stage the tile uses, publishes tiles in a 4-slot ring
+//   warp 1      TMEM allocation and MMA issue (one thread)
+//   warps 4-11  two warpgroups, one per half of the tile's rows: thread = key (TMEM
+//               lane); P^T, dS^T for its 64 rows, dS to shared memory
+//   warps 12-15 evacuation: dQ rows of each tile (bf16 partial rows) and, at the end
+//               of a unit, its dK / dV (fp32, thread = key)
+// The MMAs of tile t + 1 start once dQ of tile t has left TMEM; the gathers run two
+// tiles ahead of the MMAs.
 #include <cuda_bf16.h>
 
 #include "msa_internal.h"
@@ -40,18 +51,38 @@
 namespace msa {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+// setmaxnreg shares (control, each compute warpgroup, evacuation): their sum over the
+// four warpgroups must stay within the launch allocation (512 threads x 128 registers)
+constexpr uint32_t kRegCtl = 72, kRegCompute = 160, kRegEvac = 112;
+static_assert(kThreads == 512 && 128 * (kRegCtl + 2 * kRegCompute + kRegEvac) <= 512 * 128,
+              "setmaxnreg shares exceed the launch allocation");
+constexpr int kRing = 4;
 constexpr uint32_t kTile = 32768;  // bf16 128 x 128
-constexpr uint32_t kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 3 * kTile, kOffP = 4 * kTile,
-                   kOffDS = 5 * kTile, kOffCtl = 6 * kTile;
-constexpr uint32_t kSmemBytes = kOffCtl + 1024 + 1024;  // + control + alignment slack
-enum { B_KV = 0, B_MMA1 = 1, B_MMA2 = 2 };
+// control area at the (16-byte aligned) start of shared memory, tiles after it at the
+// next 1024-byte boundary
+constexpr uint32_t kCtlBytes = 2048;
+constexpr uint32_t kOffRing = 512, kOffLD = 1024;  // ring: kRing x 64 B; LD: 2 x 64 float2
+constexpr uint32_t kOffK = 0, kOffV = kTile, kOffQ0 = 2 * kTile, kOffDO0 = 4 * kTile, kOffDS = 6 * kTile;
+constexpr uint32_t kTilesBytes = 7 * kTile;
+constexpr uint32_t kSmemBytes = kCtlBytes + 1024 + kTilesBytes;
+static_assert(kSmemBytes <= 232448, "shared memory");
+enum {
+  B_TFULL0 = 0, B_TEMPTY0 = kRing, B_QFULL0 = 2 * kRing, B_QFREE0 = 2 * kRing + 2, B_KVFULL = 2 * kRing + 4,
+  B_KVFREE, B_SFULL, B_PFULL, B_MMA2, B_DQFREE, B_DKVFREE, B_COUNT
+};
+static_assert(8 * B_COUNT + 4 <= kOffRing, "control area");
+
+// One published tile: its first CSR position, entry count (0 = no more work), schedule
+// row, flags (bit 0 first tile of its unit, bit 1 last), unit id, query ids.
+struct BTile {
+  int e0, cnt, row, flags, uid, pad[3];
+  int q[kTileQ];
+};
+static_assert(sizeof(BTile) == 64, "ring entry");
 
 struct BwdParams {
-  const uint8_t* Q;
-  const uint8_t* dO;
-  const float* LSE;
-  const float* Dv;
+  const float2* LD;  // [N * Hq]: (LSE * log2 e, D)
   const int4* units;
   const int32_t* qlist;
   int32_t* counter;
@@ -67,39 +98,50 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 
 __global__ void __launch_bounds__(kThreads, 1)
-bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
+bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+              const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* ctl = smem_raw;
   const uint32_t raw_u = smem_u32(smem_raw);
-  const uint32_t pad = (1024u - (raw_u & 1023u)) & 1023u;
-  uint8_t* smem = smem_raw + pad;
-  const uint32_t sb = raw_u + pad;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffCtl);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffCtl + 64);
-  int4* unit_slot = reinterpret_cast<int4*>(smem + kOffCtl + 128);
-  int* flag_slot = reinterpret_cast<int*>(smem + kOffCtl + 192);
+  const uint32_t sb = (raw_u + kCtlBytes + 1023u) & ~1023u;  // tiles, 1024-byte aligned
+  uint8_t* smem = smem_raw + (sb - raw_u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ctl);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 8 * B_COUNT);
+  BTile* ring = reinterpret_cast<BTile*>(ctl + kOffRing);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rr = 32 * (warp & 3) + lane;  // MMA row / TMEM lane
-  const int hc = warp >> 2;               // column half
-  const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-
-  // rows of a partly filled tile keep earlier (finite) data; zero everything once so
-  // that 0-weighted rows never meet NaN bit patterns in the MMAs
-  for (uint32_t o = tid * 16; o < 6 * kTile; o += kThreads * 16)
-    *reinterpret_cast<uint4*>(smem + o) = make_uint4(0, 0, 0, 0);
+  // stale rows of a partly filled tile are weighted 0; zero the Q / dO stages once so
+  // that they never hold NaN bit patterns
+  for (uint32_t o = tid * 16; o < 4 * kTile; o += kThreads * 16)
+    *reinterpret_cast<uint4*>(smem + kOffQ0 + o) = make_uint4(0, 0, 0, 0);
+  if (tid < 64) reinterpret_cast<uint4*>(ctl + kOffLD)[tid] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (tid == 0) {
-    mbar_init(bar(B_KV), 1);
-    mbar_init(bar(B_MMA1), 1);
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(bar(B_TFULL0 + r), 1);
+      mbar_init(bar(B_TEMPTY0 + r), 4);  // MMA thread, two compute warpgroups, evacuation
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_QFULL0 + s), 1);
+      mbar_init(bar(B_QFREE0 + s), 1);
+    }
+    mbar_init(bar(B_KVFULL), 1);
+    mbar_init(bar(B_KVFREE), 1);
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_PFULL), 2);
     mbar_init(bar(B_MMA2), 1);
+    mbar_init(bar(B_DQFREE), 1);
+    mbar_init(bar(B_DKVFREE), 1);
     mbar_fence_init();
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
   }
-  if (warp == 0) {
+  if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -107,195 +149,279 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint64_t pol_kv = policy_evict_last();
-  constexpr uint32_t idesc_kk = idesc_f16(128, 128, 1, 1, 0, 0);  // A, B K-major
-  constexpr uint32_t idesc_tt = idesc_f16(128, 128, 1, 1, 1, 1);  // A, B MN-major
-  constexpr uint32_t idesc_kt = idesc_f16(128, 128, 1, 1, 0, 1);  // A K-major, B MN-major
-  const int nunits = *p.nunits;
-  uint32_t kv_ph = 0, m1_ph = 0, m2_ph = 0;
-  bool ok = true;
 
-  for (;;) {
-    if (tid == 0) {
-      const int u = atomicAdd(p.counter, 1);
-      *unit_slot = u < nunits ? p.units[u] : make_int4(-1, 0, 0, 0);
-      flag_slot[0] = u;
-    }
-    __syncthreads();
-    const int4 un = *unit_slot;
-    const int uid = flag_slot[0];
-    if (un.x < 0) break;
-    const int g = un.x / p.nblocks, b = un.x - g * p.nblocks;
-    if (tid == 0) {
-      mbar_expect_tx(bar(B_KV), 2 * kTile);
-      tma_load_3d(sb + kOffK, &tmK, 0, g, b * kBlock, bar(B_KV), pol_kv);
-      tma_load_3d(sb + kOffK + 16384, &tmK, 64, g, b * kBlock, bar(B_KV), pol_kv);
-      tma_load_3d(sb + kOffV, &tmV, 0, g, b * kBlock, bar(B_KV), pol_kv);
-      tma_load_3d(sb + kOffV + 16384, &tmV, 64, g, b * kBlock, bar(B_KV), pol_kv);
-    }
-    const int ntile = (un.z + kTileQ - 1) / kTileQ;
-    for (int t = 0; t < ntile && ok; ++t) {
-      const int e0 = un.y + t * kTileQ;
-      const int cnt = min(kTileQ, un.z - t * kTileQ);
-      // gather Q and dO rows of the tile: chunk c (8 elements) of query j, head h
-      for (int idx = tid; idx < cnt * 256; idx += kThreads) {
-        const int j = idx >> 8, h = (idx >> 4) & 15, c = idx & 15;
-        const int r = j * 16 + h;
-        const size_t src = ((static_cast<size_t>(__ldg(p.qlist + e0 + j)) * p.Hq + g * kGroup + h) * kHeadDim + c * 8) * 2;
-        const uint32_t dst = (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-        cp_async16(sb + kOffQ + dst, p.Q + src);
-        cp_async16(sb + kOffDO + dst, p.dO + src);
-      }
-      const int j = rr >> 4, h = rr & 15;
-      const bool valid = j < cnt;
-      float lse2 = 0.f, dv = 0.f;
-      int lim = -1;  // keys c <= lim of the block are visible to this row
-      if (valid) {
-        const int qi = __ldg(p.qlist + e0 + j);
-        const size_t o = static_cast<size_t>(qi) * p.Hq + g * kGroup + h;
-        lse2 = __ldg(p.LSE + o) * 1.4426950408889634f;
-        dv = __ldg(p.Dv + o);
-        lim = min(p.Lkv - p.N + qi - b * kBlock, kBlock - 1);
-      }
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        if (t == 0) {
-          ok = mbar_wait(bar(B_KV), kv_ph);
-          kv_ph ^= 1;
-        }
-        if (ok) {
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-            mma_f16_ss(tmem, smem_desc(sb + kOffQ + off, 16, 1024, 2), smem_desc(sb + kOffK + off, 16, 1024, 2),
-                       idesc_kk, k > 0);
+  if (warp < 4) {
+    regs_dec<kRegCtl>();
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------ producer
+      tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmDO);
+      const uint64_t pol_kv = policy_evict_last(), pol_q = policy_evict_normal();
+      const int nunits = *p.nunits;
+      int it = 0, nu = 0;
+      bool ok = true;
+      // waits for ring slot `it`; false on timeout
+      auto slot_free = [&](int t) {
+        return t < kRing || mbar_wait(bar(B_TEMPTY0 + t % kRing), ((t / kRing) & 1) ^ 1);
+      };
+      while (ok) {
+        const int u = atomicAdd(p.counter, 1);
+        if (u >= nunits) {
+          if ((ok = slot_free(it))) {
+            ring[it % kRing].cnt = 0;
+            mbar_arrive(bar(B_TFULL0 + it % kRing));
           }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-            mma_f16_ss(tmem + 128, smem_desc(sb + kOffDO + off, 16, 1024, 2),
-                       smem_desc(sb + kOffV + off, 16, 1024, 2), idesc_kk, k > 0);
-          }
-          mma_commit(bar(B_MMA1));
+          break;
         }
-        flag_slot[1] = ok;
-      }
-      __syncthreads();
-      ok = flag_slot[1] != 0;
-      if (!ok) break;
-      ok = __syncthreads_and(mbar_wait(bar(B_MMA1), m1_ph));
-      m1_ph ^= 1;
-      if (!ok) break;
-      tc_fence_after();
-      {
-        // P = 2^(S * scale * log2 e - LSE * log2 e) on visible keys, dS = P (dP - D)
-        uint32_t s[64], d[64];
-        const uint32_t tS = tmem + lane_base + 64 * hc;
-        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-        tmem_ld32(tS + 128, *reinterpret_cast<uint32_t(*)[32]>(&d[0]));
-        tmem_ld32(tS + 160, *reinterpret_cast<uint32_t(*)[32]>(&d[32]));
-        tmem_ld_wait();
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t pw[4], dw[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int c0 = ch * 8 + 2 * q, key0 = 64 * hc + c0;
-            const float p0 = key0 <= lim ? ex2(fmaf(__uint_as_float(s[c0]), p.sl2, -lse2)) : 0.f;
-            const float p1 = key0 + 1 <= lim ? ex2(fmaf(__uint_as_float(s[c0 + 1]), p.sl2, -lse2)) : 0.f;
-            pw[q] = pack_bf16x2(p0, p1);
-            dw[q] = pack_bf16x2(p0 * (__uint_as_float(d[c0]) - dv), p1 * (__uint_as_float(d[c0 + 1]) - dv));
+        const int4 un = p.units[u];
+        const int g = un.x / p.nblocks, b = un.x - g * p.nblocks;
+        const int ntile = (un.z + kTileQ - 1) / kTileQ;
+        for (int t = 0; t < ntile && ok; ++t, ++it) {
+          const int slot = it % kRing, s = it & 1;
+          if (!(ok = slot_free(it))) break;
+          if (it >= 2 && !(ok = mbar_wait(bar(B_QFREE0 + s), ((it - 2) >> 1) & 1))) break;
+          const int e0 = un.y + t * kTileQ, cnt = min(kTileQ, un.z - t * kTileQ);
+          BTile& tl = ring[slot];
+          tl.e0 = e0;
+          tl.cnt = cnt;
+          tl.row = un.x;
+          tl.flags = (t == 0 ? 1 : 0) | (t == ntile - 1 ? 2 : 0);
+          tl.uid = u;
+          const uint32_t bq = bar(B_QFULL0 + s);
+          mbar_expect_tx(bq, static_cast<uint32_t>(cnt) * 8192u);
+          const uint32_t dq = sb + kOffQ0 + s * kTile, ddo = sb + kOffDO0 + s * kTile;
+          for (int j = 0; j < cnt; ++j) {
+            const int q = __ldg(p.qlist + e0 + j);
+            tl.q[j] = q;
+            tma_load_3d(dq + j * 2048, &tmQ, 0, g * kGroup, q, bq, pol_q);
+            tma_load_3d(dq + 16384 + j * 2048, &tmQ, 64, g * kGroup, q, bq, pol_q);
+            tma_load_3d(ddo + j * 2048, &tmDO, 0, g * kGroup, q, bq, pol_q);
+            tma_load_3d(ddo + 16384 + j * 2048, &tmDO, 64, g * kGroup, q, bq, pol_q);
           }
-          const uint32_t off = hc * 16384 + rr * 128 + ((ch ^ (rr & 7)) << 4);
-          *reinterpret_cast<uint4*>(smem + kOffP + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-          *reinterpret_cast<uint4*>(smem + kOffDS + off) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+          if (t == 0) {
+            // K_b, V_b: their buffers are free once the previous unit's MMAs are done
+            if (nu > 0 && !(ok = mbar_wait(bar(B_KVFREE), (nu - 1) & 1))) break;
+            mbar_expect_tx(bar(B_KVFULL), 2 * kTile);
+            tma_load_3d(sb + kOffK, &tmK, 0, g, b * kBlock, bar(B_KVFULL), pol_kv);
+            tma_load_3d(sb + kOffK + 16384, &tmK, 64, g, b * kBlock, bar(B_KVFULL), pol_kv);
+            tma_load_3d(sb + kOffV, &tmV, 0, g, b * kBlock, bar(B_KVFULL), pol_kv);
+            tma_load_3d(sb + kOffV + 16384, &tmV, 64, g, b * kBlock, bar(B_KVFULL), pol_kv);
+          }
+          mbar_arrive(bar(B_TFULL0 + slot));
         }
+        ++nu;
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      if (tid == 0) {
+      if (!ok) atomicOr(&p.hdr->status, kStatusTimeout);
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------------------------------------ MMA issue
+      constexpr uint32_t idesc_kk = idesc_f16(128, 128, 1, 1, 0, 0);  // A, B K-major
+      constexpr uint32_t idesc_ts = idesc_f16(128, 128, 1, 1, 0, 1);  // A from TMEM, B MN-major
+      constexpr uint32_t idesc_tt = idesc_f16(128, 128, 1, 1, 1, 1);  // A, B MN-major
+      bool ok = true;
+      int nu = 0;
+      for (int it = 0;; ++it) {
+        const int slot = it % kRing, s = it & 1;
+        if (!(ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1))) break;
+        const int cnt = ring[slot].cnt, flags = ring[slot].flags;
+        if (cnt == 0) break;
+        mbar_arrive(bar(B_TEMPTY0 + slot));
+        if ((flags & 1) && !(ok = mbar_wait(bar(B_KVFULL), nu & 1))) break;
+        if (!(ok = mbar_wait(bar(B_QFULL0 + s), (it >> 1) & 1))) break;
+        // TMEM [0, 256) is reused: dQ of the previous tile has been read out (which also
+        // means its MMAs, the readers of P^T / dS^T, are done)
+        if (it > 0 && !(ok = mbar_wait(bar(B_DQFREE), (it - 1) & 1))) break;
         tc_fence_after();
-        // dV += P^T dO and dK += dS^T Q: A = P^T / dS^T (M = keys, K = rows), B = dO / Q
-        // (K = rows, N = d), both MN-major; 16 rows per MMA = 2 KB of the tile
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_f16_ss(tmem + 256, smem_desc(sb + kOffP + k * 2048, 16384, 1024, 2),
-                     smem_desc(sb + kOffDO + k * 2048, 16384, 1024, 2), idesc_tt, (t > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_f16_ss(tmem + 384, smem_desc(sb + kOffDS + k * 2048, 16384, 1024, 2),
-                     smem_desc(sb + kOffQ + k * 2048, 16384, 1024, 2), idesc_tt, (t > 0 || k > 0) ? 1u : 0u);
-        // dQ part = dS K_b: A = dS (M = rows, K = keys) K-major, B = K_b (K = keys, N = d) MN-major
+        const uint32_t qa = sb + kOffQ0 + s * kTile, oa = sb + kOffDO0 + s * kTile;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_f16_ss(tmem, smem_desc(sb + kOffDS + off, 16, 1024, 2), smem_desc(sb + kOffK + k * 2048, 16384, 1024, 2),
-                     idesc_kt, k > 0);
+          mma_f16_ss(tmem, smem_desc(sb + kOffK + off, 16, 1024, 2), smem_desc(qa + off, 16, 1024, 2), idesc_kk, k > 0);
         }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_f16_ss(tmem + 128, smem_desc(sb + kOffV + off, 16, 1024, 2), smem_desc(oa + off, 16, 1024, 2), idesc_kk,
+                     k > 0);
+        }
+        mma_commit(bar(B_SFULL));
+        if (!(ok = mbar_wait(bar(B_PFULL), it & 1))) break;
+        // the first tile of a unit starts dK / dV afresh: the previous unit's must be out
+        if ((flags & 1) && nu > 0 && !(ok = mbar_wait(bar(B_DKVFREE), (nu - 1) & 1))) break;
+        tc_fence_after();
+        const uint32_t acc0 = (flags & 1) ? 0u : 1u;
+        // 16 rows per MMA: rows 0-63 of P^T at columns 0-31, rows 64-127 at 64-95; dS^T 32 further
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t col = (k < 4 ? 0 : 64) + 8 * (k & 3);
+          mma_f16_ts(tmem + 256, tmem + col, smem_desc(oa + k * 2048, 16384, 1024, 2), idesc_ts, k > 0 ? 1u : acc0);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t col = (k < 4 ? 32 : 96) + 8 * (k & 3);
+          mma_f16_ts(tmem + 384, tmem + col, smem_desc(qa + k * 2048, 16384, 1024, 2), idesc_ts, k > 0 ? 1u : acc0);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_f16_ss(tmem + 128, smem_desc(sb + kOffDS + k * 2048, 16384, 1024, 2),
+                     smem_desc(sb + kOffK + k * 2048, 16384, 1024, 2), idesc_tt, k > 0);
+        mma_commit(bar(B_QFREE0 + s));
         mma_commit(bar(B_MMA2));
-      }
-      ok = __syncthreads_and(mbar_wait(bar(B_MMA2), m2_ph));
-      m2_ph ^= 1;
-      if (!ok) break;
-      tc_fence_after();
-      {
-        uint32_t v[64];
-        const uint32_t tQ = tmem + lane_base + 64 * hc;
-        tmem_ld32(tQ, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld32(tQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-        tmem_ld_wait();
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dq_part + ((static_cast<size_t>(e0 + j) * kGroup + h) * kHeadDim + 64 * hc));
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[8 * ch + 0]), __uint_as_float(v[8 * ch + 1]));
-            w.y = pack_bf16x2(__uint_as_float(v[8 * ch + 2]), __uint_as_float(v[8 * ch + 3]));
-            w.z = pack_bf16x2(__uint_as_float(v[8 * ch + 4]), __uint_as_float(v[8 * ch + 5]));
-            w.w = pack_bf16x2(__uint_as_float(v[8 * ch + 6]), __uint_as_float(v[8 * ch + 7]));
-            dst[ch] = w;
-          }
+        if (flags & 2) {
+          mma_commit(bar(B_KVFREE));
+          ++nu;
         }
       }
-      tc_fence_before();
-      __syncthreads();
+      if (!ok) atomicOr(&p.hdr->status, kStatusTimeout);
     }
-    if (!ok) break;
-    // the unit's dK, dV (TMEM lane = key of the block) -> fp32 partials of the unit
-    tc_fence_after();
-    float* dk = p.dkv + static_cast<size_t>(uid) * 2 * kBlock * kHeadDim;
+  } else if (warp < 12) {
+    regs_inc<kRegCompute>();
+    // -------------------------------------------------------------- P^T, dS^T
+    const int wg = (warp - 4) >> 2;  // rows [64 wg, 64 wg + 64) of each tile
+    const uint32_t bar_id = 1 + wg;
+    const int kk = 32 * (warp & 3) + lane;  // key of the block = TMEM lane
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const int gtid = tid - 128 - 128 * wg;
+    float2* ld = reinterpret_cast<float2*>(ctl + kOffLD + 512 * wg);  // [4 queries][16 heads]
+    for (int it = 0;; ++it) {
+      const int slot = it % kRing;
+      bool ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1);
+      if (!named_bar_and(bar_id, 128, ok)) { atomicOr(&p.hdr->status, kStatusTimeout); break; }
+      const BTile& t = ring[slot];
+      const int cnt = t.cnt;
+      if (cnt == 0) break;
+      const int g = t.row / p.nblocks, b = t.row - g * p.nblocks;
+      // (LSE * log2 e, D) of this half's 4 queries x 16 heads: 128 contiguous bytes per query
+      if (gtid < 32) {
+        const int j = 4 * wg + (gtid >> 3);
+        if (j < cnt)
+          cp_async16(smem_u32(ld) + gtid * 16,
+                     reinterpret_cast<const uint8_t*>(p.LD + static_cast<size_t>(t.q[j]) * p.Hq + g * kGroup) +
+                         (gtid & 7) * 16);
+      }
+      int lim[4];  // keys kk <= lim[jj] are visible to query 4 wg + jj; -1 for rows past cnt
 #pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      uint32_t v[64];
-      const uint32_t tA = tmem + lane_base + (m == 0 ? 384 : 256) + 64 * hc;
-      tmem_ld32(tA, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tmem_ld32(tA + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = 4 * wg + jj;
+        lim[jj] = j < cnt ? p.Lkv - p.N + t.q[j] - b * kBlock : -1;
+      }
+      named_bar_sync(bar_id, 128);  // everyone has read the ring entry
+      if (gtid == 0) mbar_arrive(bar(B_TEMPTY0 + slot));
+      cp_async_wait_all();
+      ok = mbar_wait(bar(B_SFULL), it & 1);
+      if (!named_bar_and(bar_id, 128, ok)) { atomicOr(&p.hdr->status, kStatusTimeout); break; }
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld32(tl + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(tl + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       tmem_ld_wait();
-      float4* dst = reinterpret_cast<float4*>(dk + (static_cast<size_t>(m) * kBlock + rr) * kHeadDim + 64 * hc);
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
-        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
-                             __uint_as_float(v[4 * q + 3]));
+      for (int jj = 0; jj < 4; ++jj) {
+        uint32_t dv[16];
+        tmem_ld16(tl + 128 + 64 * wg + 16 * jj, dv);
+        tmem_ld_wait();
+        const bool vis = kk <= lim[jj];
+        uint32_t pp[8], dd[8];
+#pragma unroll
+        for (int h = 0; h < 16; h += 2) {
+          const float2 a = ld[jj * 16 + h], c = ld[jj * 16 + h + 1];
+          const float p0 = vis ? ex2(fmaf(__uint_as_float(sv[16 * jj + h]), p.sl2, -a.x)) : 0.f;
+          const float p1 = vis ? ex2(fmaf(__uint_as_float(sv[16 * jj + h + 1]), p.sl2, -c.x)) : 0.f;
+          pp[h >> 1] = pack_bf16x2(p0, p1);
+          dd[h >> 1] = vis ? pack_bf16x2(p0 * (__uint_as_float(dv[h]) - a.y), p1 * (__uint_as_float(dv[h + 1]) - c.y))
+                           : 0u;
+        }
+        tmem_st8(tl + 64 * wg + 8 * jj, pp);
+        tmem_st8(tl + 64 * wg + 32 + 8 * jj, dd);
+        // dS [rows][keys] for dQ: row kk of this half's tile holds the 64 rows' values of key kk
+        uint8_t* dsrow = smem + kOffDS + wg * 16384 + kk * 128;
+        *reinterpret_cast<uint4*>(dsrow + (((2 * jj) ^ (kk & 7)) << 4)) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+        *reinterpret_cast<uint4*>(dsrow + (((2 * jj + 1) ^ (kk & 7)) << 4)) = make_uint4(dd[4], dd[5], dd[6], dd[7]);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      fence_proxy_async_smem();
+      named_bar_sync(bar_id, 128);
+      if (gtid == 0) mbar_arrive(bar(B_PFULL));
     }
-    tc_fence_before();
-    __syncthreads();
+  } else {
+    regs_dec<kRegEvac>();
+    // -------------------------------------------------------------- evacuation
+    const uint32_t bar_id = 3;
+    const int rr = 32 * (warp & 3) + lane;  // TMEM lane: tile row for dQ, key for dK / dV
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const bool elected = tid == 384;
+    int nu = 0;
+    for (int it = 0;; ++it) {
+      const int slot = it % kRing;
+      bool ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1);
+      if (!named_bar_and(bar_id, 128, ok)) { atomicOr(&p.hdr->status, kStatusTimeout); break; }
+      const int cnt = ring[slot].cnt, e0 = ring[slot].e0, flags = ring[slot].flags, uid = ring[slot].uid;
+      if (cnt == 0) break;
+      ok = mbar_wait(bar(B_MMA2), it & 1);
+      if (!named_bar_and(bar_id, 128, ok)) { atomicOr(&p.hdr->status, kStatusTimeout); break; }
+      if (elected) mbar_arrive(bar(B_TEMPTY0 + slot));
+      tc_fence_after();
+      const int j = rr >> 4, h = rr & 15;
+      __nv_bfloat16* dst = p.dq_part + (static_cast<size_t>(e0 + j) * kGroup + h) * kHeadDim;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[64];
+        tmem_ld32(tl + 128 + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(tl + 128 + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_ld_wait();
+        if (half == 1) {
+          // dQ is out of TMEM: the next tile's MMAs may overwrite it
+          tc_fence_before();
+          named_bar_sync(bar_id, 128);
+          if (elected) mbar_arrive(bar(B_DQFREE));
+        }
+        if (j < cnt) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 64 * half);
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            d4[ch] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * ch + 0]), __uint_as_float(v[8 * ch + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * ch + 2]), __uint_as_float(v[8 * ch + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * ch + 4]), __uint_as_float(v[8 * ch + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * ch + 6]), __uint_as_float(v[8 * ch + 7])));
+        }
+      }
+      if (flags & 2) {
+        // the unit's dK (columns 384..) and dV (256..), thread = key -> fp32 partials
+        float* dk = p.dkv + static_cast<size_t>(uid) * 2 * kBlock * kHeadDim;
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t v[64];
+            const uint32_t ta = tl + (m == 0 ? 384 : 256) + 64 * half;
+            tmem_ld32(ta, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_ld_wait();
+            float4* d4 = reinterpret_cast<float4*>(dk + (static_cast<size_t>(m) * kBlock + rr) * kHeadDim + 64 * half);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                  __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          }
+        tc_fence_before();
+        named_bar_sync(bar_id, 128);
+        if (elected) mbar_arrive(bar(B_DKVFREE));
+        ++nu;
+      }
+    }
   }
-  if (!ok && tid == 0) atomicOr(&p.hdr->status, kStatusTimeout);
+
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, 512);
+  if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// D[i, h] = dO[i, h, :] . O[i, h, :] in fp32: 16 threads per row (8 elements each), two
-// rows per warp; the loop bound is warp-uniform so every lane joins the shuffles.
+// (LSE[i, h] * log2 e, D[i, h] = dO[i, h, :] . O[i, h, :]) in fp32: 16 threads per row
+// (8 elements each), two rows per warp; the loop bound is warp-uniform so every lane
+// joins the shuffles.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__ O, const uint4* __restrict__ dO,
-                                                       float* __restrict__ Dv, int64_t rows) {
+                                                       const float* __restrict__ LSE, float2* __restrict__ LD,
+                                                       int64_t rows) {
   const int sub = threadIdx.x & 15;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -313,7 +439,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
     }
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (sub == 0 && r < rows) Dv[r] = s;
+    if (sub == 0 && r < rows) LD[r] = make_float2(__ldg(LSE + r) * 1.4426950408889634f, s);
   }
 }
 
@@ -425,7 +551,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const int32_t* __restrict__
 size_t bwd_workspace_bytes(const msa_schedule* s) {
   const int64_t units = bwd_unit_capacity(s);
   size_t b = 0;
-  b += (static_cast<size_t>(s->N) * s->Hkv * kGroup * sizeof(float) + 255) / 256 * 256;  // D
+  b += (static_cast<size_t>(s->N) * s->Hkv * kGroup * sizeof(float2) + 255) / 256 * 256;  // (LSE log2 e, D)
   b += (static_cast<size_t>(units) * sizeof(int4) + 255) / 256 * 256;                     // units
   b += (static_cast<size_t>(s->R + 1) * sizeof(int32_t) + 255) / 256 * 256;               // unit_off
   b += 256;                                                                                // claim counter
@@ -448,7 +574,7 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
     return p;
   };
   const int64_t qrows = static_cast<int64_t>(s->N) * a.Hq;
-  float* Dv = reinterpret_cast<float*>(take(static_cast<size_t>(qrows) * sizeof(float)));
+  float2* LD = reinterpret_cast<float2*>(take(static_cast<size_t>(qrows) * sizeof(float2)));
   int4* units = reinterpret_cast<int4*>(take(static_cast<size_t>(cap_units) * sizeof(int4)));
   int32_t* unit_off = reinterpret_cast<int32_t*>(take(static_cast<size_t>(s->R + 1) * sizeof(int32_t)));
   int32_t* counter = reinterpret_cast<int32_t*>(take(256));
@@ -462,14 +588,24 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
     int64_t grid = (qrows * 16 + 255) / 256;
     if (grid > static_cast<int64_t>(sms) * 32) grid = static_cast<int64_t>(sms) * 32;
     bwd_prep_kernel<<<static_cast<int>(grid), 256, 0, st>>>(static_cast<const uint4*>(a.O),
-                                                            static_cast<const uint4*>(a.dO), Dv, qrows);
+                                                            static_cast<const uint4*>(a.dO), a.LSE, LD, qrows);
     if ((e = cudaGetLastError())) return e;
   }
   bwd_units_kernel<<<1, 1024, 0, st>>>(s->d.counts, s->d.offsets, s->R, units, unit_off);
   if ((e = cudaGetLastError())) return e;
   if ((e = cudaMemsetAsync(counter, 0, sizeof(int32_t), st))) return e;
 
-  CUtensorMap tmK, tmV;
+  CUtensorMap tmK, tmV, tmQ, tmDO;
+  {
+    // Q, dO [N][Hq][128]: one D half of the 16 heads of one query per box (2 KB)
+    const uint64_t dims[3] = {kHeadDim, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(s->N)};
+    const uint64_t strides[2] = {kHeadDim * 2, static_cast<uint64_t>(a.Hq) * kHeadDim * 2};
+    const uint32_t box[3] = {64u, kGroup, 1};
+    if (!encode_tmap(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap(&tmDO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.dO, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   {
     const uint64_t dims[3] = {kHeadDim, static_cast<uint64_t>(s->Hkv), static_cast<uint64_t>(a.Lkv)};
     const uint64_t strides[2] = {kHeadDim * 2, static_cast<uint64_t>(s->Hkv) * kHeadDim * 2};
@@ -480,10 +616,7 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
       return cudaErrorInvalidValue;
   }
   BwdParams p;
-  p.Q = static_cast<const uint8_t*>(a.Q);
-  p.dO = static_cast<const uint8_t*>(a.dO);
-  p.LSE = a.LSE;
-  p.Dv = Dv;
+  p.LD = LD;
   p.units = units;
   p.qlist = s->d.qlist;
   p.counter = counter;
@@ -501,8 +634,10 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
     if ((e = cudaFuncSetAttribute(bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes))) return e;
     attr_set = true;
   }
-  bwd_kv_kernel<<<a.num_ctas, kThreads, kSmemBytes, st>>>(tmK, tmV, p);
+  if (a.ev[0] && (e = cudaEventRecord(a.ev[0], st))) return e;
+  bwd_kv_kernel<<<a.num_ctas, kThreads, kSmemBytes, st>>>(tmK, tmV, tmQ, tmDO, p);
   if ((e = cudaGetLastError())) return e;
+  if (a.ev[1] && (e = cudaEventRecord(a.ev[1], st))) return e;
   bwd_reduce_kernel<<<s->R * 16, 256, 0, st>>>(reinterpret_cast<const float4*>(dkv), unit_off, s->R, s->nblocks,
                                                 s->Hkv, a.scale, static_cast<__nv_bfloat16*>(a.dK),
                                                 static_cast<__nv_bfloat16*>(a.dV));
@@ -514,8 +649,10 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
     bwd_dq_kernel<<<static_cast<int>(grid), 256, 0, st>>>(s->d.cmap, static_cast<const uint4*>(s->partial), s->N,
                                                           s->Hkv, s->topK, a.Hq, a.scale,
                                                           static_cast<__nv_bfloat16*>(a.dQ));
+    if ((e = cudaGetLastError())) return e;
   }
-  return cudaGetLastError();
+  if (a.ev[2] && (e = cudaEventRecord(a.ev[2], st))) return e;
+  return cudaSuccess;
 }
 
 }  // namespace msa

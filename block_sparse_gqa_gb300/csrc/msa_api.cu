@@ -265,7 +265,8 @@ msa_status_t msa_sparse_attn_bwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
   const int ctas = opts->num_ctas > 0 ? opts->num_ctas : device_sms();
   if (ctas < 1) return MSA_ERR_CUDA;
   msa::BwdArgs a{s, Q.ptr, K.ptr, V.ptr, O, dO, LSE, dQ, dK, dV, s->bwd_ws, static_cast<int>(Q.h),
-                 s->nblocks * msa::kBlock, scale, ctas};
+                 s->nblocks * msa::kBlock, scale, ctas,
+                 {opts->stage_events[0], opts->stage_events[1], opts->stage_events[2]}};
   cudaError_t e = msa::launch_bwd(a, opts->stream);
   s->last_stream = opts->stream;
   return from_cuda(e);

@@ -129,6 +129,7 @@ struct BwdArgs {
   int Hq, Lkv;
   float scale;
   int num_ctas;
+  cudaEvent_t ev[3];  // optional: before / after the tcgen05 kernel, after the last kernel
 };
 int64_t bwd_unit_capacity(const msa_schedule* s);
 size_t bwd_workspace_bytes(const msa_schedule* s);
