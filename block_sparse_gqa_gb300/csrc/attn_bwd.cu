@@ -25,15 +25,17 @@
 // bwd_kv_kernel, one CTA of 512 threads per SM, persistent (units claimed with an
 // atomicAdd).  It works on the transposed products so that the block's keys sit on the
 // TMEM lanes: S^T = K_b Q^T and dP^T = V_b dO^T (M = keys, N = the tile's 128 rows);
-// P^T = exp2(S^T * scale * log2 e - LSE * log2 e) and dS^T = P^T (dP^T - D) are written
-// back to TMEM as bf16 and feed dV += P^T dO and dK += dS^T Q directly as the A operand
-// (A read from TMEM); dS also goes to shared memory (rows contiguous per key, i.e. the
-// MN-major A layout of dS with M = rows) for dQ = dS K_b, which lands in the columns
-// dP^T held.  TMEM (512 columns): [0, 128) S^T -> P^T / dS^T (bf16 pairs), [128, 256)
-// dP^T -> dQ, [256, 384) dV, [384, 512) dK.  Shared memory: K_b, V_b (TMA), Q and dO in
-// two stages (TMA: one 2 KB box per query and D half), dS; bf16 128 x 128 tiles of two
-// 64-column halves with the 128-byte swizzle, so one tile is K-major for a matrix and
-// MN-major for its transpose.  Warp roles:
+// P^T = exp2(S^T * scale * log2 e - LSE * log2 e) is written back to TMEM as bf16 and
+// feeds dV += P^T dO as the A operand read from TMEM; dS^T = P^T (dP^T - D) goes to
+// shared memory, one 128-byte row per key, which serves dK += dS^T Q (read K-major) and
+// dQ = dS K_b (read MN-major, M = rows); dQ lands in the columns dP^T held.  TMEM (512
+// columns): [0, 128) S^T -> P^T (bf16 pairs), [128, 256) dP^T -> dQ, [256, 384) dV,
+// [384, 512) dK.  Shared memory, bf16 128 x 128 tiles with the
+// 128-byte swizzle: K_b, V_b (TMA) and dS as two 64-column halves, so one tile is K-major
+// for a matrix and MN-major for its transpose (dS serves dQ as A = dS, M = rows, and dK as
+// A = dS^T, M = keys); Q and dO in two stages, one TMA box of 4 KB per query laid out as
+// [8-row group][D half][8 rows] (K-major with 2 KB between row groups, MN-major with the
+// D halves 1 KB apart).  Warp roles:
 //   warp 0      producer: claims units, loads K_b / V_b and gathers Q / dO of each tile
 //               into the stage the tile uses, publishes tiles in a 4-slot ring
 //   warp 1      TMEM allocation and MMA issue (one thread)
@@ -54,7 +56,7 @@ namespace {
 constexpr int kThreads = 512;
 // setmaxnreg shares (control, each compute warpgroup, evacuation): their sum over the
 // four warpgroups must stay within the launch allocation (512 threads x 128 registers)
-constexpr uint32_t kRegCtl = 72, kRegCompute = 160, kRegEvac = 112;
+constexpr uint32_t kRegCtl = 96, kRegCompute = 168, kRegEvac = 80;
 static_assert(kThreads == 512 && 128 * (kRegCtl + 2 * kRegCompute + kRegEvac) <= 512 * 128,
               "setmaxnreg shares exceed the launch allocation");
 constexpr int kRing = 4;
@@ -62,14 +64,14 @@ constexpr uint32_t kTile = 32768;  // bf16 128 x 128
 // control area at the (16-byte aligned) start of shared memory, tiles after it at the
 // next 1024-byte boundary
 constexpr uint32_t kCtlBytes = 2048;
-constexpr uint32_t kOffRing = 512, kOffLD = 1024;  // ring: kRing x 64 B; LD: 2 x 64 float2
+constexpr uint32_t kOffRing = 512, kOffLD = 1024;  // ring: kRing x 64 B; per compute warpgroup 512 B of (LSE, D)
 constexpr uint32_t kOffK = 0, kOffV = kTile, kOffQ0 = 2 * kTile, kOffDO0 = 4 * kTile, kOffDS = 6 * kTile;
 constexpr uint32_t kTilesBytes = 7 * kTile;
 constexpr uint32_t kSmemBytes = kCtlBytes + 1024 + kTilesBytes;
 static_assert(kSmemBytes <= 232448, "shared memory");
 enum {
   B_TFULL0 = 0, B_TEMPTY0 = kRing, B_QFULL0 = 2 * kRing, B_QFREE0 = 2 * kRing + 2, B_KVFULL = 2 * kRing + 4,
-  B_KVFREE, B_SFULL, B_PFULL, B_MMA2, B_DQFREE, B_DKVFREE, B_COUNT
+  B_KVFREE, B_SFULL, B_DPFULL, B_PREADY, B_DSREADY, B_DVDONE, B_MMA2, B_DQFREE, B_DSFREE, B_DKVFREE, B_COUNT
 };
 static_assert(8 * B_COUNT + 4 <= kOffRing, "control area");
 
@@ -82,12 +84,12 @@ struct BTile {
 static_assert(sizeof(BTile) == 64, "ring entry");
 
 struct BwdParams {
-  const float2* LD;  // [N * Hq]: (LSE * log2 e, D)
+  const float* LSE2;  // [N * Hq]: LSE * log2 e
+  const float* Dv;    // [N * Hq]: D = dO . O
   const int4* units;
   const int32_t* qlist;
   int32_t* counter;
   const int32_t* nunits;
-  __nv_bfloat16* dq_part;  // [E * 16, 128]
   float* dkv;              // [units][2][128][128]: dK then dV
   SchedHeader* hdr;
   int N, Lkv, Hq, nblocks;
@@ -97,6 +99,9 @@ struct BwdParams {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void lds4(uint32_t addr, float& a, float& b, float& c, float& d) {
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(a), "=f"(b), "=f"(c), "=f"(d) : "r"(addr) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 template <uint32_t N>
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
@@ -105,7 +110,8 @@ __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.a
 
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-              const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
+              const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+              const __grid_constant__ CUtensorMap tmP128, const __grid_constant__ CUtensorMap tmP16, const BwdParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* ctl = smem_raw;
   const uint32_t raw_u = smem_u32(smem_raw);
@@ -135,7 +141,11 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     mbar_init(bar(B_KVFULL), 1);
     mbar_init(bar(B_KVFREE), 1);
     mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_PFULL), 2);
+    mbar_init(bar(B_DPFULL), 1);
+    mbar_init(bar(B_PREADY), 2);
+    mbar_init(bar(B_DSREADY), 2);
+    mbar_init(bar(B_DVDONE), 1);
+    mbar_init(bar(B_DSFREE), 1);
     mbar_init(bar(B_MMA2), 1);
     mbar_init(bar(B_DQFREE), 1);
     mbar_init(bar(B_DKVFREE), 1);
@@ -190,12 +200,12 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           mbar_expect_tx(bq, static_cast<uint32_t>(cnt) * 8192u);
           const uint32_t dq = sb + kOffQ0 + s * kTile, ddo = sb + kOffDO0 + s * kTile;
           for (int j = 0; j < cnt; ++j) {
+            // one 4 KB box per query and tensor: its 16 heads as two 8-row groups, each
+            // with both D halves ([group][D half][8 rows][128 B])
             const int q = __ldg(p.qlist + e0 + j);
             tl.q[j] = q;
-            tma_load_3d(dq + j * 2048, &tmQ, 0, g * kGroup, q, bq, pol_q);
-            tma_load_3d(dq + 16384 + j * 2048, &tmQ, 64, g * kGroup, q, bq, pol_q);
-            tma_load_3d(ddo + j * 2048, &tmDO, 0, g * kGroup, q, bq, pol_q);
-            tma_load_3d(ddo + 16384 + j * 2048, &tmDO, 64, g * kGroup, q, bq, pol_q);
+            tma_load_5d(dq + j * 4096, &tmQ, 0, 0, 0, 2 * g, q, bq, pol_q);
+            tma_load_5d(ddo + j * 4096, &tmDO, 0, 0, 0, 2 * g, q, bq, pol_q);
           }
           if (t == 0) {
             // K_b, V_b: their buffers are free once the previous unit's MMAs are done
@@ -226,44 +236,48 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         mbar_arrive(bar(B_TEMPTY0 + slot));
         if ((flags & 1) && !(ok = mbar_wait(bar(B_KVFULL), nu & 1))) break;
         if (!(ok = mbar_wait(bar(B_QFULL0 + s), (it >> 1) & 1))) break;
-        // TMEM [0, 256) is reused: dQ of the previous tile has been read out (which also
-        // means its MMAs, the readers of P^T / dS^T, are done)
-        if (it > 0 && !(ok = mbar_wait(bar(B_DQFREE), (it - 1) & 1))) break;
+        // S^T lands in TMEM [0, 128): P^T of the previous tile there has been read by its dV
+        if (it > 0 && !(ok = mbar_wait(bar(B_DVDONE), (it - 1) & 1))) break;
         tc_fence_after();
         const uint32_t qa = sb + kOffQ0 + s * kTile, oa = sb + kOffDO0 + s * kTile;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_f16_ss(tmem, smem_desc(sb + kOffK + off, 16, 1024, 2), smem_desc(qa + off, 16, 1024, 2), idesc_kk, k > 0);
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_f16_ss(tmem + 128, smem_desc(sb + kOffV + off, 16, 1024, 2), smem_desc(oa + off, 16, 1024, 2), idesc_kk,
-                     k > 0);
-        }
+        for (int k = 0; k < 8; ++k)
+          mma_f16_ss(tmem, smem_desc(sb + kOffK + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, 2),
+                     smem_desc(qa + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048, 2), idesc_kk, k > 0);
         mma_commit(bar(B_SFULL));
-        if (!(ok = mbar_wait(bar(B_PFULL), it & 1))) break;
+        // dP^T lands in TMEM [128, 256): dQ of the previous tile has been read out
+        if (it > 0 && !(ok = mbar_wait(bar(B_DQFREE), (it - 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_f16_ss(tmem + 128, smem_desc(sb + kOffV + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, 2),
+                     smem_desc(oa + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048, 2), idesc_kk, k > 0);
+        mma_commit(bar(B_DPFULL));
+        if (!(ok = mbar_wait(bar(B_PREADY), it & 1))) break;
         // the first tile of a unit starts dK / dV afresh: the previous unit's must be out
         if ((flags & 1) && nu > 0 && !(ok = mbar_wait(bar(B_DKVFREE), (nu - 1) & 1))) break;
         tc_fence_after();
         const uint32_t acc0 = (flags & 1) ? 0u : 1u;
-        // 16 rows per MMA: rows 0-63 of P^T at columns 0-31, rows 64-127 at 64-95; dS^T 32 further
+        // dV += P^T dO: P^T rows 0-63 at TMEM columns 0-31, rows 64-127 at 64-95 (16 rows per MMA)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t col = (k < 4 ? 0 : 64) + 8 * (k & 3);
-          mma_f16_ts(tmem + 256, tmem + col, smem_desc(oa + k * 2048, 16384, 1024, 2), idesc_ts, k > 0 ? 1u : acc0);
+          mma_f16_ts(tmem + 256, tmem + col, smem_desc(oa + k * 4096, 1024, 2048, 2), idesc_ts, k > 0 ? 1u : acc0);
         }
+        mma_commit(bar(B_DVDONE));
+        // dK += dS^T Q: the dS tile read K-major is dS^T (M = keys, K = rows); formed while dV runs
+        if (!(ok = mbar_wait(bar(B_DSREADY), it & 1))) break;
+        tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t col = (k < 4 ? 32 : 96) + 8 * (k & 3);
-          mma_f16_ts(tmem + 384, tmem + col, smem_desc(qa + k * 2048, 16384, 1024, 2), idesc_ts, k > 0 ? 1u : acc0);
-        }
+        for (int k = 0; k < 8; ++k)
+          mma_f16_ss(tmem + 384, smem_desc(sb + kOffDS + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, 2),
+                     smem_desc(qa + k * 4096, 1024, 2048, 2), idesc_ts, k > 0 ? 1u : acc0);
+        mma_commit(bar(B_QFREE0 + s));  // Q / dO of this stage are read no more
+        // dQ = dS K_b into TMEM [128, 256): A = dS (M = rows) MN-major, B = K_b MN-major
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           mma_f16_ss(tmem + 128, smem_desc(sb + kOffDS + k * 2048, 16384, 1024, 2),
                      smem_desc(sb + kOffK + k * 2048, 16384, 1024, 2), idesc_tt, k > 0);
-        mma_commit(bar(B_QFREE0 + s));
         mma_commit(bar(B_MMA2));
         if (flags & 2) {
           mma_commit(bar(B_KVFREE));
@@ -280,7 +294,8 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const int kk = 32 * (warp & 3) + lane;  // key of the block = TMEM lane
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     const int gtid = tid - 128 - 128 * wg;
-    float2* ld = reinterpret_cast<float2*>(ctl + kOffLD + 512 * wg);  // [4 queries][16 heads]
+    // LSE * log2 e [4 queries][16 heads], then D [4][16], of this half's queries
+    const uint32_t ld = smem_u32(ctl + kOffLD + 512 * wg);
     for (int it = 0;; ++it) {
       const int slot = it % kRing;
       bool ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1);
@@ -289,13 +304,13 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       const int cnt = t.cnt;
       if (cnt == 0) break;
       const int g = t.row / p.nblocks, b = t.row - g * p.nblocks;
-      // (LSE * log2 e, D) of this half's 4 queries x 16 heads: 128 contiguous bytes per query
       if (gtid < 32) {
-        const int j = 4 * wg + (gtid >> 3);
-        if (j < cnt)
-          cp_async16(smem_u32(ld) + gtid * 16,
-                     reinterpret_cast<const uint8_t*>(p.LD + static_cast<size_t>(t.q[j]) * p.Hq + g * kGroup) +
-                         (gtid & 7) * 16);
+        // 64 contiguous bytes per query and array: query jj = gtid / 8, array (gtid / 4) % 2, chunk gtid % 4
+        const int jj = gtid >> 3, arr = (gtid >> 2) & 1, j = 4 * wg + jj;
+        if (j < cnt) {
+          const float* src = (arr ? p.Dv : p.LSE2) + static_cast<size_t>(t.q[j]) * p.Hq + g * kGroup + (gtid & 3) * 4;
+          cp_async16(ld + arr * 256 + jj * 64 + (gtid & 3) * 16, src);
+        }
       }
       int lim[4];  // keys kk <= lim[jj] are visible to query 4 wg + jj; -1 for rows past cnt
 #pragma unroll
@@ -309,38 +324,69 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       ok = mbar_wait(bar(B_SFULL), it & 1);
       if (!named_bar_and(bar_id, 128, ok)) { atomicOr(&p.hdr->status, kStatusTimeout); break; }
       tc_fence_after();
-      uint32_t sv[64];
-      tmem_ld32(tl + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld32(tl + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-      tmem_ld_wait();
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        uint32_t dv[16];
-        tmem_ld16(tl + 128 + 64 * wg + 16 * jj, dv);
+      // P^T first (it needs S^T only; dP^T is still being computed), to TMEM for dV
+      float pv[64];
+      {
+        uint32_t sv[64];
+        tmem_ld32(tl + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(tl + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tmem_ld_wait();
-        const bool vis = kk <= lim[jj];
-        uint32_t pp[8], dd[8];
 #pragma unroll
-        for (int h = 0; h < 16; h += 2) {
-          const float2 a = ld[jj * 16 + h], c = ld[jj * 16 + h + 1];
-          const float p0 = vis ? ex2(fmaf(__uint_as_float(sv[16 * jj + h]), p.sl2, -a.x)) : 0.f;
-          const float p1 = vis ? ex2(fmaf(__uint_as_float(sv[16 * jj + h + 1]), p.sl2, -c.x)) : 0.f;
-          pp[h >> 1] = pack_bf16x2(p0, p1);
-          dd[h >> 1] = vis ? pack_bf16x2(p0 * (__uint_as_float(dv[h]) - a.y), p1 * (__uint_as_float(dv[h + 1]) - c.y))
-                           : 0u;
+        for (int jj = 0; jj < 4; ++jj) {
+          const bool vis = kk <= lim[jj];
+          float l2[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) lds4(ld + jj * 64 + q * 16, l2[4 * q], l2[4 * q + 1], l2[4 * q + 2], l2[4 * q + 3]);
+          uint32_t pp[8];
+#pragma unroll
+          for (int h = 0; h < 16; h += 2) {
+            const float p0 = vis ? ex2(fmaf(__uint_as_float(sv[16 * jj + h]), p.sl2, -l2[h])) : 0.f;
+            const float p1 = vis ? ex2(fmaf(__uint_as_float(sv[16 * jj + h + 1]), p.sl2, -l2[h + 1])) : 0.f;
+            pv[16 * jj + h] = p0;
+            pv[16 * jj + h + 1] = p1;
+            pp[h >> 1] = pack_bf16x2(p0, p1);
+          }
+          tmem_st8(tl + 64 * wg + 8 * jj, pp);
         }
-        tmem_st8(tl + 64 * wg + 8 * jj, pp);
-        tmem_st8(tl + 64 * wg + 32 + 8 * jj, dd);
-        // dS [rows][keys] for dQ: row kk of this half's tile holds the 64 rows' values of key kk
-        uint8_t* dsrow = smem + kOffDS + wg * 16384 + kk * 128;
-        *reinterpret_cast<uint4*>(dsrow + (((2 * jj) ^ (kk & 7)) << 4)) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
-        *reinterpret_cast<uint4*>(dsrow + (((2 * jj + 1) ^ (kk & 7)) << 4)) = make_uint4(dd[4], dd[5], dd[6], dd[7]);
       }
       tmem_st_wait();
       tc_fence_before();
+      named_bar_sync(bar_id, 128);
+      if (gtid == 0) mbar_arrive(bar(B_PREADY));
+      ok = mbar_wait(bar(B_DPFULL), it & 1);
+      // dS goes to the tile the previous tile's dQ was staged in: its store must have read it
+      if (it > 0) ok = mbar_wait(bar(B_DSFREE), (it - 1) & 1) && ok;
+      if (!named_bar_and(bar_id, 128, ok)) { atomicOr(&p.hdr->status, kStatusTimeout); break; }
+      tc_fence_after();
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {
+        uint32_t dv[32];  // dP^T of rows 32 hv .. 32 hv + 31 of this half
+        tmem_ld32(tl + 128 + 64 * wg + 32 * hv, dv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j2 = 0; j2 < 2; ++j2) {
+          const int jj = 2 * hv + j2;
+          const bool vis = kk <= lim[jj];
+          float dd0[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            lds4(ld + 256 + jj * 64 + q * 16, dd0[4 * q], dd0[4 * q + 1], dd0[4 * q + 2], dd0[4 * q + 3]);
+          uint32_t dd[8];
+#pragma unroll
+          for (int h = 0; h < 16; h += 2)
+            dd[h >> 1] = vis ? pack_bf16x2(pv[16 * jj + h] * (__uint_as_float(dv[16 * j2 + h]) - dd0[h]),
+                                           pv[16 * jj + h + 1] * (__uint_as_float(dv[16 * j2 + h + 1]) - dd0[h + 1]))
+                             : 0u;
+          // dS [rows][keys] for dQ (and, read K-major, dS^T for dK): row kk of this half's tile holds the 64 rows' values of key kk
+          uint8_t* dsrow = smem + kOffDS + wg * 16384 + kk * 128;
+          *reinterpret_cast<uint4*>(dsrow + (((2 * jj) ^ (kk & 7)) << 4)) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+          *reinterpret_cast<uint4*>(dsrow + (((2 * jj + 1) ^ (kk & 7)) << 4)) = make_uint4(dd[4], dd[5], dd[6], dd[7]);
+        }
+      }
+      tc_fence_before();
       fence_proxy_async_smem();
       named_bar_sync(bar_id, 128);
-      if (gtid == 0) mbar_arrive(bar(B_PFULL));
+      if (gtid == 0) mbar_arrive(bar(B_DSREADY));
     }
   } else {
     regs_dec<kRegEvac>();
@@ -349,6 +395,8 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     const int rr = 32 * (warp & 3) + lane;  // TMEM lane: tile row for dQ, key for dK / dV
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     const bool elected = tid == 384;
+    const uint64_t pol_st = policy_evict_normal();
+    if (elected) { tma_prefetch_desc(&tmP128); tma_prefetch_desc(&tmP16); }
     int nu = 0;
     for (int it = 0;; ++it) {
       const int slot = it % kRing;
@@ -360,29 +408,42 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
       if (!named_bar_and(bar_id, 128, ok)) { atomicOr(&p.hdr->status, kStatusTimeout); break; }
       if (elected) mbar_arrive(bar(B_TEMPTY0 + slot));
       tc_fence_after();
-      const int j = rr >> 4, h = rr & 15;
-      __nv_bfloat16* dst = p.dq_part + (static_cast<size_t>(e0 + j) * kGroup + h) * kHeadDim;
+      // dQ (TMEM lane = tile row) -> bf16 -> the dS tile (dQ, its last reader, is done), in
+      // the 128-byte-swizzled layout of the partial rows' tensor map -> TMA store
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[64];
-        tmem_ld32(tl + 128 + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld32(tl + 128 + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      for (int qt = 0; qt < 4; ++qt) {
+        uint32_t v[32];
+        tmem_ld32(tl + 128 + 32 * qt, v);
         tmem_ld_wait();
-        if (half == 1) {
-          // dQ is out of TMEM: the next tile's MMAs may overwrite it
-          tc_fence_before();
-          named_bar_sync(bar_id, 128);
-          if (elected) mbar_arrive(bar(B_DQFREE));
-        }
-        if (j < cnt) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 64 * half);
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            d4[ch] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * ch + 0]), __uint_as_float(v[8 * ch + 1])),
-                                pack_bf16x2(__uint_as_float(v[8 * ch + 2]), __uint_as_float(v[8 * ch + 3])),
-                                pack_bf16x2(__uint_as_float(v[8 * ch + 4]), __uint_as_float(v[8 * ch + 5])),
-                                pack_bf16x2(__uint_as_float(v[8 * ch + 6]), __uint_as_float(v[8 * ch + 7])));
+        for (int c = 0; c < 4; ++c) {
+          const int ch = 4 * qt + c;  // 8-column chunk 0..15
+          const uint32_t off = (ch >> 3) * 16384 + rr * 128 + (((ch & 7) ^ (rr & 7)) << 4);
+          *reinterpret_cast<uint4*>(smem + kOffDS + off) =
+              make_uint4(pack_bf16x2(__uint_as_float(v[8 * c + 0]), __uint_as_float(v[8 * c + 1])),
+                         pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
+                         pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
+                         pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
         }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      named_bar_sync(bar_id, 128);
+      if (elected) {
+        mbar_arrive(bar(B_DQFREE));  // dQ is out of TMEM: the next tile's dP^T may overwrite it
+        const uint32_t src = sb + kOffDS;
+        if (cnt == kTileQ) {
+          tma_store_2d(&tmP128, 0, e0 * kGroup, src, pol_st);
+          tma_store_2d(&tmP128, 64, e0 * kGroup, src + 16384, pol_st);
+        } else {
+          for (int q = 0; q < cnt; ++q) {
+            tma_store_2d(&tmP16, 0, (e0 + q) * kGroup, src + q * 2048, pol_st);
+            tma_store_2d(&tmP16, 64, (e0 + q) * kGroup, src + 16384 + q * 2048, pol_st);
+          }
+        }
+        bulk_commit();
+        bulk_wait_read0();
+        mbar_arrive(bar(B_DSFREE));  // the staging has been read: the next dS may be written
       }
       if (flags & 2) {
         // the unit's dK (columns 384..) and dV (256..), thread = key -> fp32 partials
@@ -408,6 +469,7 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         ++nu;
       }
     }
+    if (elected) bulk_wait_all0();
   }
 
   tc_fence_before();
@@ -416,12 +478,12 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// (LSE[i, h] * log2 e, D[i, h] = dO[i, h, :] . O[i, h, :]) in fp32: 16 threads per row
+// LSE[i, h] * log2 e and D[i, h] = dO[i, h, :] . O[i, h, :] in fp32: 16 threads per row
 // (8 elements each), two rows per warp; the loop bound is warp-uniform so every lane
 // joins the shuffles.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__ O, const uint4* __restrict__ dO,
-                                                       const float* __restrict__ LSE, float2* __restrict__ LD,
-                                                       int64_t rows) {
+                                                       const float* __restrict__ LSE, float* __restrict__ LSE2,
+                                                       float* __restrict__ Dv, int64_t rows) {
   const int sub = threadIdx.x & 15;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -439,7 +501,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
     }
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (sub == 0 && r < rows) LD[r] = make_float2(__ldg(LSE + r) * 1.4426950408889634f, s);
+    if (sub == 0 && r < rows) {
+      LSE2[r] = __ldg(LSE + r) * 1.4426950408889634f;
+      Dv[r] = s;
+    }
   }
 }
 
@@ -551,7 +616,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const int32_t* __restrict__
 size_t bwd_workspace_bytes(const msa_schedule* s) {
   const int64_t units = bwd_unit_capacity(s);
   size_t b = 0;
-  b += (static_cast<size_t>(s->N) * s->Hkv * kGroup * sizeof(float2) + 255) / 256 * 256;  // (LSE log2 e, D)
+  b += 2 * ((static_cast<size_t>(s->N) * s->Hkv * kGroup * sizeof(float) + 255) / 256 * 256);  // LSE log2 e, D
   b += (static_cast<size_t>(units) * sizeof(int4) + 255) / 256 * 256;                     // units
   b += (static_cast<size_t>(s->R + 1) * sizeof(int32_t) + 255) / 256 * 256;               // unit_off
   b += 256;                                                                                // claim counter
@@ -574,7 +639,8 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
     return p;
   };
   const int64_t qrows = static_cast<int64_t>(s->N) * a.Hq;
-  float2* LD = reinterpret_cast<float2*>(take(static_cast<size_t>(qrows) * sizeof(float2)));
+  float* LSE2 = reinterpret_cast<float*>(take(static_cast<size_t>(qrows) * sizeof(float)));
+  float* Dv = reinterpret_cast<float*>(take(static_cast<size_t>(qrows) * sizeof(float)));
   int4* units = reinterpret_cast<int4*>(take(static_cast<size_t>(cap_units) * sizeof(int4)));
   int32_t* unit_off = reinterpret_cast<int32_t*>(take(static_cast<size_t>(s->R + 1) * sizeof(int32_t)));
   int32_t* counter = reinterpret_cast<int32_t*>(take(256));
@@ -588,22 +654,38 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
     int64_t grid = (qrows * 16 + 255) / 256;
     if (grid > static_cast<int64_t>(sms) * 32) grid = static_cast<int64_t>(sms) * 32;
     bwd_prep_kernel<<<static_cast<int>(grid), 256, 0, st>>>(static_cast<const uint4*>(a.O),
-                                                            static_cast<const uint4*>(a.dO), a.LSE, LD, qrows);
+                                                            static_cast<const uint4*>(a.dO), a.LSE, LSE2, Dv,
+                                                            qrows);
     if ((e = cudaGetLastError())) return e;
   }
   bwd_units_kernel<<<1, 1024, 0, st>>>(s->d.counts, s->d.offsets, s->R, units, unit_off);
   if ((e = cudaGetLastError())) return e;
   if ((e = cudaMemsetAsync(counter, 0, sizeof(int32_t), st))) return e;
 
-  CUtensorMap tmK, tmV, tmQ, tmDO;
+  CUtensorMap tmK, tmV, tmQ, tmDO, tmP128, tmP16;
   {
-    // Q, dO [N][Hq][128]: one D half of the 16 heads of one query per box (2 KB)
-    const uint64_t dims[3] = {kHeadDim, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(s->N)};
-    const uint64_t strides[2] = {kHeadDim * 2, static_cast<uint64_t>(a.Hq) * kHeadDim * 2};
-    const uint32_t box[3] = {64u, kGroup, 1};
-    if (!encode_tmap(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.Q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    // dQ partial rows [E * 16][128] bf16: a full tile's 128 rows, or 16 rows per entry
+    const uint64_t dims[2] = {kHeadDim, static_cast<uint64_t>(s->cap_entries) * kGroup};
+    const uint64_t strides[1] = {kHeadDim * 2};
+    const uint32_t box128[2] = {64, 128}, box16[2] = {64, 16};
+    if (!encode_tmap(&tmP128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s->partial, dims, strides, box128,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-    if (!encode_tmap(&tmDO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.dO, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_tmap(&tmP16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s->partial, dims, strides, box16,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    // Q, dO [N][Hq][128] viewed as (64 elements of a D half, head within 8, D half, group of
+    // 8 heads, query): one box = the 16 heads of one query's GQA group, 4 KB, landing as
+    // [8-head group][D half][8 heads][128 B]
+    const uint64_t row = kHeadDim * 2;
+    const uint64_t dims[5] = {64, 8, 2, static_cast<uint64_t>(a.Hq) / 8, static_cast<uint64_t>(s->N)};
+    const uint64_t strides[4] = {row, 128, 8 * row, static_cast<uint64_t>(a.Hq) * row};
+    const uint32_t box[5] = {64, 8, 2, 2, 1};
+    if (!encode_tmap(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, a.Q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap(&tmDO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, a.dO, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   {
@@ -616,12 +698,12 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
       return cudaErrorInvalidValue;
   }
   BwdParams p;
-  p.LD = LD;
+  p.LSE2 = LSE2;
+  p.Dv = Dv;
   p.units = units;
   p.qlist = s->d.qlist;
   p.counter = counter;
   p.nunits = unit_off + s->R;
-  p.dq_part = static_cast<__nv_bfloat16*>(s->partial);
   p.dkv = dkv;
   p.hdr = s->d.hdr;
   p.N = s->N;
@@ -635,7 +717,7 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
     attr_set = true;
   }
   if (a.ev[0] && (e = cudaEventRecord(a.ev[0], st))) return e;
-  bwd_kv_kernel<<<a.num_ctas, kThreads, kSmemBytes, st>>>(tmK, tmV, tmQ, tmDO, p);
+  bwd_kv_kernel<<<a.num_ctas, kThreads, kSmemBytes, st>>>(tmK, tmV, tmQ, tmDO, tmP128, tmP16, p);
   if ((e = cudaGetLastError())) return e;
   if (a.ev[1] && (e = cudaEventRecord(a.ev[1], st))) return e;
   bwd_reduce_kernel<<<s->R * 16, 256, 0, st>>>(reinterpret_cast<const float4*>(dkv), unit_off, s->R, s->nblocks,
