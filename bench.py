@@ -57,6 +57,8 @@ def parse_args():
                     help="general: schedule + attention + combine; tiles: the shared-list forward "
                          "(lists shared by 128 queries for r1, by the workload's query runs otherwise); "
                          "bwd: the backward (dQ, dK, dV) over the forward's schedule, O and LSE")
+    ap.add_argument("--partials", default="bf16", choices=["bf16", "fp32"],
+                    help="format of the KV-outer partial outputs (the pages' bf16 vs fp32 study)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -439,7 +441,8 @@ def run_ours(args, world, rank, local, pg):
             return
         msa.build_schedule(idx_d, cfg.nblocks, schedule=sched)
         msa.sparse_attn_fwd(Q, K, V, sched, scale=cfg.scale, O=O, LSE=LSE, descales=descales,
-                            stage_events=[e.cuda_event for e in stage] if stage else None)
+                            stage_events=[e.cuda_event for e in stage] if stage else None,
+                            partials_fp32=args.partials == "fp32")
 
     for _ in range(args.warmup):
         step(None)
@@ -485,7 +488,7 @@ def run_ours(args, world, rank, local, pg):
     es = 1 if cfg.dtype == "e4m3" else 2  # bytes per input element
     q_bytes = cfg.N * cfg.Hq * D * es
     kv_bytes = nsb * 2 * 128 * D * es
-    part_bytes = E * G * (2 * D + 8)  # bf16 partial row + float2 (m, l)
+    part_bytes = E * G * ((4 if args.partials == "fp32" else 2) * D + 8)  # partial row + float2 (m, l)
     meta_attn = E * 4 + T * 16
     attn_bytes = q_bytes + kv_bytes + part_bytes + meta_attn
     comb_bytes = part_bytes + cfg.N * cfg.Hkv * cfg.topK * 4 + cfg.N * cfg.Hq * (2 * D + 4)
@@ -493,7 +496,7 @@ def run_ours(args, world, rank, local, pg):
     peak, peak_kind = load_peaks()
     attn_mean = statistics.mean(attn_ms)
     achieved = attn_bytes / (attn_mean * 1e-3) / 1e9
-    traffic = recorded_traffic(cfg.name)
+    traffic = recorded_traffic(cfg.name) if args.partials == "bf16" else None  # profiled with bf16 partials
     if not kv_path:
         # Q-outer: Q once, each distinct selected K/V block once (the pages' deduplicated
         # bytes), the block lists, O and LSE written; timed in the combine stage, where the
@@ -562,6 +565,7 @@ def run_ours(args, world, rank, local, pg):
                    "parallelism": f"independent problem per GPU x{world}",
                    "path": "bwd" if bwd else "tiles" if tiles else ("kv_outer" if kv_path else "q_outer"),
                    "lists": "R1 selector (chosen once, before timing)" if args.lists == "r1" else "workload",
+                   "partials": args.partials,
                    "entries": E, "nsb": nsb, "tiles": T},
         "roofline": roof,
         "path_roofline": {"bytes_per_step": step_bytes, "achieved_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,

@@ -244,7 +244,7 @@ __device__ __forceinline__ float2 softmax_row_any_scale(uint32_t (&v)[128], int 
   return make_float2(m2, l);
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kF32P>
 __global__ void __launch_bounds__(kThreads, 1)
 kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const __grid_constant__ CUtensorMap tmP128, const __grid_constant__ CUtensorMap tmP16,
@@ -645,39 +645,82 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       if (elected) mbar_arrive(bar(B_TEMPTY0 + slot));
       tc_fence_after();
       const uint32_t tO = tmem + lane_base + 256 + s * 128;
+      if constexpr (kF32P) {
+        // fp32 partials: one D half (64 columns, 32 KB for 128 rows) at a time through the
+        // staging tile, as two 32-column boxes of 128-byte rows
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tO + c * 32, v);
-        tmem_ld_wait();
+        for (int hh = 0; hh < 2; ++hh) {
+          if (hh == 1) {
+            // the first half's stores must have read the staging tile
+            if (elected) bulk_wait_read0();
+            named_bar_sync(bar_id, 128);
+          }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int ch = c * 4 + q;
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]), __uint_as_float(v[q * 8 + 1]));
-          w.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]), __uint_as_float(v[q * 8 + 3]));
-          w.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]), __uint_as_float(v[q * 8 + 5]));
-          w.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]), __uint_as_float(v[q * 8 + 7]));
-          const uint32_t off = (ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
-          *reinterpret_cast<uint4*>(stage + off) = w;
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(bar(B_OFREE0 + s));
-      fence_proxy_async_smem();
-      named_bar_sync(bar_id, 128);
-      if (elected) {
-        const uint32_t src = sb + L::kOffSt;
-        if (count == kTileQ) {
-          tma_store_2d(&tmP128, 0, first * kGroup, src, pol_st);
-          tma_store_2d(&tmP128, 64, first * kGroup, src + 16384, pol_st);
-        } else {
-          for (int q = 0; q < count; ++q) {
-            tma_store_2d(&tmP16, 0, (first + q) * kGroup, src + q * 2048, pol_st);
-            tma_store_2d(&tmP16, 64, (first + q) * kGroup, src + 16384 + q * 2048, pol_st);
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t v[32];
+            tmem_ld32(tO + 64 * hh + 32 * c2, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t off = c2 * 16384 + row * 128 + ((q ^ (row & 7)) << 4);
+              *reinterpret_cast<uint4*>(stage + off) = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+          }
+          if (hh == 1) {
+            tc_fence_before();
+            mbar_arrive(bar(B_OFREE0 + s));
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(bar_id, 128);
+          if (elected) {
+            const uint32_t src = sb + L::kOffSt;
+            if (count == kTileQ) {
+              tma_store_2d(&tmP128, 64 * hh, first * kGroup, src, pol_st);
+              tma_store_2d(&tmP128, 64 * hh + 32, first * kGroup, src + 16384, pol_st);
+            } else {
+              for (int q = 0; q < count; ++q) {
+                tma_store_2d(&tmP16, 64 * hh, (first + q) * kGroup, src + q * 2048, pol_st);
+                tma_store_2d(&tmP16, 64 * hh + 32, (first + q) * kGroup, src + 16384 + q * 2048, pol_st);
+              }
+            }
+            bulk_commit();
           }
         }
-        bulk_commit();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int ch = c * 4 + q;
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]), __uint_as_float(v[q * 8 + 1]));
+            w.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]), __uint_as_float(v[q * 8 + 3]));
+            w.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]), __uint_as_float(v[q * 8 + 5]));
+            w.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]), __uint_as_float(v[q * 8 + 7]));
+            const uint32_t off = (ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+            *reinterpret_cast<uint4*>(stage + off) = w;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B_OFREE0 + s));
+        fence_proxy_async_smem();
+        named_bar_sync(bar_id, 128);
+        if (elected) {
+          const uint32_t src = sb + L::kOffSt;
+          if (count == kTileQ) {
+            tma_store_2d(&tmP128, 0, first * kGroup, src, pol_st);
+            tma_store_2d(&tmP128, 64, first * kGroup, src + 16384, pol_st);
+          } else {
+            for (int q = 0; q < count; ++q) {
+              tma_store_2d(&tmP16, 0, (first + q) * kGroup, src + q * 2048, pol_st);
+              tma_store_2d(&tmP16, 64, (first + q) * kGroup, src + 16384 + q * 2048, pol_st);
+            }
+          }
+          bulk_commit();
+        }
       }
       stored_before = true;
     }
@@ -710,14 +753,17 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
       return cudaErrorInvalidValue;
   }
   {
+    // partial rows [E * 16][128], bf16 or fp32; boxes of 128-byte rows (64 bf16 or 32 fp32
+    // columns) for a full tile's 128 rows or one entry's 16 rows
+    const uint64_t pes = a.f32p ? 4 : 2;
     const uint64_t dims[2] = {kHeadDim, static_cast<uint64_t>(s->cap_entries) * kGroup};
-    const uint64_t strides[1] = {kHeadDim * 2};
-    const uint32_t box128[2] = {64, 128}, box16[2] = {64, 16};
-    if (!encode_tmap(&tmP128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s->partial, dims, strides, box128,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint64_t strides[1] = {kHeadDim * pes};
+    const uint32_t bw = static_cast<uint32_t>(128 / pes);
+    const uint32_t box128[2] = {bw, 128}, box16[2] = {bw, 16};
+    const CUtensorMapDataType pdt = a.f32p ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!encode_tmap(&tmP128, pdt, 2, s->partial, dims, strides, box128, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-    if (!encode_tmap(&tmP16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s->partial, dims, strides, box16,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_tmap(&tmP16, pdt, 2, s->partial, dims, strides, box16, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   KvParams p;
@@ -732,21 +778,25 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   p.nblocks = s->nblocks;
   p.sl2 = a.scale * a.qk_descale * 1.4426950408889634f;
   p.force_path = a.force_path;
-  static bool attr_set[2] = {false, false};
+  static bool attr_set[4] = {false, false, false, false};
+  const int inst = (fp8 ? 1 : 0) | (a.f32p ? 2 : 0);
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, KvParams);
+  switch (inst) {
+    case 0: kern = kv_outer_kernel<false, false>; break;
+    case 1: kern = kv_outer_kernel<true, false>; break;
+    case 2: kern = kv_outer_kernel<false, true>; break;
+    default: kern = kv_outer_kernel<true, true>; break;
+  }
   const uint32_t smem = fp8 ? Lay<true>::kSmemBytes : Lay<false>::kSmemBytes;
-  if (!attr_set[fp8]) {
-    cudaError_t e = fp8 ? cudaFuncSetAttribute(kv_outer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-                        : cudaFuncSetAttribute(kv_outer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (!attr_set[inst]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set[fp8] = true;
+    attr_set[inst] = true;
   }
   // the chunk counter this launch claims its work from starts at zero
   cudaError_t e = cudaMemsetAsync(&s->d.hdr->pad[0], 0, sizeof(int32_t), st);
   if (e != cudaSuccess) return e;
-  if (fp8)
-    kv_outer_kernel<true><<<a.num_ctas, kThreads, smem, st>>>(tmK, tmV, tmP128, tmP16, p);
-  else
-    kv_outer_kernel<false><<<a.num_ctas, kThreads, smem, st>>>(tmK, tmV, tmP128, tmP16, p);
+  kern<<<a.num_ctas, kThreads, smem, st>>>(tmK, tmV, tmP128, tmP16, p);
   return cudaGetLastError();
 }
 

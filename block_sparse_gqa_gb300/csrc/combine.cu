@@ -9,7 +9,7 @@
 // partial row.  It is bandwidth-bound and tolerant of gather latency.
 //
 // Partial k of (query i, group g, head h) is row 16 * cmap[i, g, k] + h of the
-// bf16 [E*16, 128] slab: O_k = sum_j 2^(x_j - m_k) V_j over the block's visible keys
+// bf16 (or, on request, fp32) [E*16, 128] slab: O_k = sum_j 2^(x_j - m_k) V_j over the block's visible keys
 // (x = score * scale * log2 e), with statistics (m_k, l_k = sum_j 2^(x_j - m_k)).
 // For E4M3 inputs the V descale multiplies the merged output (the partials hold P V
 // of the stored E4M3 values).
@@ -30,7 +30,6 @@ namespace msa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kKChunk = 8;
 
 __device__ __forceinline__ void acc8(float (&a)[8], const uint4& v, float w) {
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -41,11 +40,35 @@ __device__ __forceinline__ void acc8(float (&a)[8], const uint4& v, float w) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 4)
+// 8 consecutive columns of one partial row: bf16 (one 16-byte load) or fp32 (two)
+template <bool kF32>
+struct Part8;
+template <>
+struct Part8<false> {
+  uint4 a;
+};
+template <>
+struct Part8<true> {
+  uint4 a, b;
+};
+template <bool kF32>
+__device__ __forceinline__ void acc_part8(float (&a)[8], const Part8<kF32>& v, float w) {
+  if constexpr (kF32) {
+    const uint32_t u[8] = {v.a.x, v.a.y, v.a.z, v.a.w, v.b.x, v.b.y, v.b.z, v.b.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) a[q] = fmaf(w, __uint_as_float(u[q]), a[q]);
+  } else {
+    acc8(a, v.a, w);
+  }
+}
+
+template <bool kF32>
+__global__ void __launch_bounds__(kThreads, kF32 ? 3 : 4)
 combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ partial,
                const float2* __restrict__ pstat, int N, int Hkv, int topK, int Hq,
                __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, float v_descale,
                const SchedHeader* __restrict__ hdr, int force_path) {
+  constexpr int kKChunk = kF32 ? 4 : 8;  // partial loads in flight per thread
   const int path = force_path ? force_path : hdr->path;
   if (path != kPathKvOuter) return;
   const int h = threadIdx.x >> 4, c = threadIdx.x & 15;
@@ -59,12 +82,17 @@ combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ parti
 #pragma unroll
       for (int k = 0; k < kKChunk; ++k) pos[k] = (k0 + k < topK) ? __ldg(cm + k0 + k) : -1;
       float2 st[kKChunk];
-      uint4 v[kKChunk];
+      Part8<kF32> v[kKChunk];
 #pragma unroll
       for (int k = 0; k < kKChunk; ++k) {
         const int64_t r = static_cast<int64_t>(pos[k]) * kGroup + h;
         st[k] = pos[k] >= 0 ? __ldg(pstat + r) : make_float2(-INFINITY, 0.f);
-        v[k] = pos[k] >= 0 ? __ldg(partial + r * 16 + c) : make_uint4(0, 0, 0, 0);
+        if constexpr (kF32) {
+          v[k].a = pos[k] >= 0 ? __ldg(partial + r * 32 + 2 * c) : make_uint4(0, 0, 0, 0);
+          v[k].b = pos[k] >= 0 ? __ldg(partial + r * 32 + 2 * c + 1) : make_uint4(0, 0, 0, 0);
+        } else {
+          v[k].a = pos[k] >= 0 ? __ldg(partial + r * 16 + c) : make_uint4(0, 0, 0, 0);
+        }
       }
       float Mc = M;
 #pragma unroll
@@ -78,7 +106,7 @@ combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ parti
       for (int k = 0; k < kKChunk; ++k) {
         const float w = pos[k] >= 0 ? ex2(st[k].x - Mc) : 0.f;
         L = fmaf(w, st[k].y, L);
-        acc8(acc, v[k], w);
+        acc_part8<kF32>(acc, v[k], w);
       }
       M = Mc;
     }
@@ -105,16 +133,21 @@ combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ parti
 }  // namespace
 
 cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, float v_descale, int force_path,
-                           cudaStream_t st) {
+                           bool f32p, cudaStream_t st) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t units = static_cast<int64_t>(s->N) * s->Hkv;
   int64_t grid = sms * 16;
   if (grid > units) grid = units;
-  combine_kernel<<<static_cast<int>(grid), kThreads, 0, st>>>(
-      s->d.cmap, static_cast<const uint4*>(s->partial), s->pstat, s->N, s->Hkv, s->topK, Hq,
-      static_cast<__nv_bfloat16*>(O), LSE, v_descale, s->d.hdr, force_path);
+  if (f32p)
+    combine_kernel<true><<<static_cast<int>(grid), kThreads, 0, st>>>(
+        s->d.cmap, static_cast<const uint4*>(s->partial), s->pstat, s->N, s->Hkv, s->topK, Hq,
+        static_cast<__nv_bfloat16*>(O), LSE, v_descale, s->d.hdr, force_path);
+  else
+    combine_kernel<false><<<static_cast<int>(grid), kThreads, 0, st>>>(
+        s->d.cmap, static_cast<const uint4*>(s->partial), s->pstat, s->N, s->Hkv, s->topK, Hq,
+        static_cast<__nv_bfloat16*>(O), LSE, v_descale, s->d.hdr, force_path);
   return cudaGetLastError();
 }
 

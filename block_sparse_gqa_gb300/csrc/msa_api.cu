@@ -61,21 +61,22 @@ msa_status_t schedule_create(int N, int Hkv, int topK, int nblocks, msa_schedule
   return MSA_OK;
 }
 
-msa_status_t ensure_partials(msa_schedule* s, int G) {
-  if (s->partial && s->partial_G == G) return MSA_OK;
+msa_status_t ensure_partials(msa_schedule* s, int G, int elem = 2) {
+  if (s->partial && s->partial_G == G && s->partial_elem >= elem) return MSA_OK;
   if (s->partial) {
     cudaFree(s->partial);
     s->partial = nullptr;
     s->pstat = nullptr;
   }
   const size_t rows = static_cast<size_t>(s->cap_entries) * G;
-  const size_t obytes = align_up(rows * msa::kHeadDim * 2, 256);
+  const size_t obytes = align_up(rows * msa::kHeadDim * elem, 256);
   void* p = nullptr;
   cudaError_t e = cudaMalloc(&p, obytes + rows * sizeof(float2));
   if (e != cudaSuccess) return from_cuda(e);
   s->partial = p;
   s->pstat = reinterpret_cast<float2*>(static_cast<char*>(p) + obytes);
   s->partial_G = G;
+  s->partial_elem = elem;
   return MSA_OK;
 }
 
@@ -212,7 +213,9 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
                opts->q_descale > 0.f && opts->k_descale > 0.f && opts->v_descale > 0.f))
     return MSA_ERR_INVALID_ARG;
   if (fp8 && opts->path == MSA_PATH_Q_OUTER) return MSA_ERR_UNSUPPORTED;  // the Q-outer kernel is bf16 only
-  msa_status_t st = ensure_partials(s, msa::kGroup);
+  if (opts->partials_fp32 != 0 && opts->partials_fp32 != 1) return MSA_ERR_INVALID_ARG;
+  const bool f32p = opts->partials_fp32 == 1;
+  msa_status_t st = ensure_partials(s, msa::kGroup, f32p ? 4 : 2);
   if (st != MSA_OK) return st;
   // E4M3 inputs always take the KV-outer kernel (the only one with an E4M3 instance)
   const int force = fp8 ? msa::kPathKvOuter : opts->path == MSA_PATH_AUTO ? 0 : static_cast<int>(opts->path);
@@ -224,10 +227,10 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
   const int Hq = static_cast<int>(Q.h);
   cudaError_t e;
   if (opts->stage_events[0] && (e = cudaEventRecord(opts->stage_events[0], stream))) return from_cuda(e);
-  msa::KvOuterArgs a{s, Q.ptr, K.ptr, V.ptr, Hq, s->nblocks * msa::kBlock, scale, force, ctas, fp8, qk_descale};
+  msa::KvOuterArgs a{s, Q.ptr, K.ptr, V.ptr, Hq, s->nblocks * msa::kBlock, scale, force, ctas, fp8, qk_descale, f32p};
   if ((e = msa::launch_kv_outer(a, stream))) return from_cuda(e);
   if (opts->stage_events[1] && (e = cudaEventRecord(opts->stage_events[1], stream))) return from_cuda(e);
-  if ((e = msa::launch_combine(s, Hq, O, LSE, v_descale, force, stream))) return from_cuda(e);
+  if ((e = msa::launch_combine(s, Hq, O, LSE, v_descale, force, f32p, stream))) return from_cuda(e);
   if ((e = msa::launch_q_outer(s, Q.ptr, K.ptr, V.ptr, Hq, scale, O, LSE, force, stream))) return from_cuda(e);
   if (opts->stage_events[2] && (e = cudaEventRecord(opts->stage_events[2], stream))) return from_cuda(e);
   s->last_stream = stream;

@@ -58,9 +58,10 @@ struct msa_schedule {
   size_t dev_bytes;
   msa::SchedDev d;
   // partial-output workspace (first forward call)
-  void* partial;       // bf16 [cap_entries * G, D]: raw P V of each (entry, head) row
+  void* partial;       // bf16 or fp32 [cap_entries * G, D]: raw P V of each (entry, head) row
   float2* pstat;       // [cap_entries * G]: (m, l) of each partial row, m in base-2 units
   int partial_G;
+  int partial_elem;    // bytes per element the partial buffer was sized for (2 or 4)
   void* bwd_ws;  // backward workspace (first backward call)
   cudaStream_t last_stream;
 };
@@ -90,12 +91,13 @@ struct KvOuterArgs {
   int num_ctas;
   bool fp8;          // E4M3 inputs
   float qk_descale;  // q descale * k descale (1 for bf16)
+  bool f32p;         // fp32 partial outputs
 };
 cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st);
 
 // combine.cu
 cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, float v_descale, int force_path,
-                           cudaStream_t st);
+                           bool f32p, cudaStream_t st);
 
 // attn_q_outer.cu
 cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, const void* V, int Hq,

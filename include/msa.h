@@ -78,6 +78,11 @@ typedef struct {
    * [0] before the attention kernel, [1] after it, [2] after the combine. */
   cudaEvent_t stage_events[3];
   int num_ctas;          /* persistent grid size for the KV-outer kernel; 0 = #SMs */
+  /* KV-outer partial outputs: 0 = bf16 (default), 1 = fp32 ("Sparse Attention", Chapter 5,
+   * "Partial outputs and Combine": the partials' format is the main data-movement cost,
+   * 16x (bf16) or 32x (fp32) the final bf16 output).  fp32 doubles the partial bytes and
+   * keeps the per-block P V sums unrounded until the combine. */
+  int partials_fp32;
 } msa_fwd_opts_t;
 
 /* Fill *opts with the defaults: stream 0, AUTO, descales 1, no events, #SMs. */
@@ -127,9 +132,10 @@ msa_status_t msa_build_schedule(const int32_t* indices, int N, int Hkv, int topK
  * E4M3 inputs always run the KV-outer path (AUTO included): S = Q K^T on E4M3
  * tensor cores, V widened to f16 on chip, P V in f16, output bf16.
  *
- * The first call for a given head count allocates the partial-output workspace of
- * the schedule (cudaMalloc, synchronous): N*Hkv*topK*G*(2*D + 8) bytes at most (bf16 rows + float2 (m, l)).
- * Later calls allocate nothing.
+ * The first call for a given head count and partial format allocates the partial-output
+ * workspace of the schedule (cudaMalloc, synchronous): N*Hkv*topK*G*(2*D + 8) bytes at most
+ * for bf16 rows + float2 (m, l), N*Hkv*topK*G*(4*D + 8) with opts->partials_fp32.  A fp32
+ * workspace also serves bf16 calls; later calls allocate nothing.
  *
  * Returns MSA_ERR_INVALID_ARG on null pointers or shapes inconsistent with the
  * schedule or non-positive E4M3 descales; MSA_ERR_UNSUPPORTED for D != 128, G != 16,
@@ -161,8 +167,9 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
  * [N, Hq] (natural log) from msa_sparse_attn_fwd on the same inputs and schedule (s
  * must still hold the lists the forward used).  Outputs dQ: bf16 [N, Hq, D]; dK, dV:
  * bf16 [Lkv, Hkv, D]; all device pointers, 16-byte aligned, caller-owned.  scale is the
- * forward's.  opts may be NULL; opts->stream and opts->num_ctas are used, opts->path
- * must be AUTO or KV_OUTER.
+ * forward's.  opts may be NULL; opts->stream, opts->num_ctas and opts->stage_events
+ * ([0] before the tcgen05 kernel, [1] after it, [2] after the last kernel) are used;
+ * opts->path must be AUTO or KV_OUTER.
  *
  * The first call allocates the schedule's partial-output workspace (if the forward
  * has not) and a backward workspace (cudaMalloc, synchronous): N*Hq*4 bytes for D,
