@@ -63,6 +63,8 @@ def _load():
                                         P, i32, P, P, i32, P, P, i32]
         lib.oracle_select_r1.restype = i32
         lib.oracle_select_r1.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, P, P]
+        lib.oracle_select_r4.restype = i32
+        lib.oracle_select_r4.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32, P, P]
         _lib = lib
     return _lib
 
@@ -218,12 +220,21 @@ def dispatch(nsb: int, N: int) -> int:
     return _load().oracle_dispatch(int(nsb), int(N))
 
 
+def select_r4(Q, K, *, Lkv, topK, block=128, tile=128):
+    """Block selector R4 ("Sparse Attention", Chapter 4): as select_r1 with four
+    representatives (means of consecutive quarters) per query tile and per KV block."""
+    return _select(_load().oracle_select_r4, "oracle_select_r4", Q, K, Lkv, topK, block, tile)
+
+
 def select_r1(Q, K, *, Lkv, topK, block=128, tile=128):
     """Block selector R1 ("Sparse Attention", Chapter 4): (indices [N, Hkv, topK] int32,
     scores [ntiles, Hkv, nblocks] float64 with +inf for the tile's own blocks and -inf
     for blocks after the tile).  Q [N, Hq, D], K [Lkv, Hkv, D] as bf16 bit patterns
     (uint16) or float64."""
-    lib = _load()
+    return _select(_load().oracle_select_r1, "oracle_select_r1", Q, K, Lkv, topK, block, tile)
+
+
+def _select(fn, name, Q, K, Lkv, topK, block, tile):
     Q = np.ascontiguousarray(Q); K = np.ascontiguousarray(K)
     fmt = _fmt_of(Q)
     if _fmt_of(K) != fmt:
@@ -235,7 +246,7 @@ def select_r1(Q, K, *, Lkv, topK, block=128, tile=128):
     ntiles = -(-N // tile)
     idx = np.zeros((N, Hkv, topK), np.int32)
     scores = np.zeros((ntiles, Hkv, nblocks), np.float64)
-    st = lib.oracle_select_r1(_ptr(Q), _ptr(K), fmt, N, Lkv, Hq, Hkv, D, block, tile, topK, _ptr(idx), _ptr(scores))
+    st = fn(_ptr(Q), _ptr(K), fmt, N, Lkv, Hq, Hkv, D, block, tile, topK, _ptr(idx), _ptr(scores))
     if st < 0:
-        raise ValueError("oracle_select_r1 rejected its arguments")
+        raise ValueError(f"{name} rejected its arguments")
     return idx, scores

@@ -590,3 +590,93 @@ int oracle_attn_bwd(const void* Q, const void* K, const void* V, const void* dO,
   free(args); free(th); free(J.row_of);
   return J.bad ? 1 : 0;
 }
+
+/* Block selector R4 ("Sparse Attention" (dinara-dl), Chapter 4, "R4: Four
+ * Representatives"): as R1, but a 128-query tile and a 128-key block are each cut into
+ * four consecutive groups of 32 tokens, each summarised by its mean vector; for one
+ * (tile, block) pair the four query representatives of every head of the GQA group meet
+ * the block's four key representatives (16 dot products per head), and the largest of
+ * them is the block's score.  Candidates, forced own blocks, ordering and padding as in
+ * oracle_select_r1.  Reading where the chapter is silent: the groups of a tile are
+ * queries [i0 + 32 s, i0 + 32 s + 32) clipped to the tile's queries; a group holding no
+ * query (a short last tile) has no representative.  Outputs as oracle_select_r1. */
+int oracle_select_r4(const void* Q, const void* K, int fmt, int N, int Lkv, int Hq, int Hkv, int D, int block,
+                     int tile, int topK, int32_t* indices, double* scores) {
+  if (N < 1 || Lkv < block || Lkv % block || block % 4 || tile % 4 || Hq % Hkv || topK < 1 || tile < 1 || N > Lkv)
+    return -1;
+  const int G = Hq / Hkv, nblocks = Lkv / block, ntiles = (N + tile - 1) / tile;
+  const int kg = block / 4, qg = tile / 4; /* tokens per representative */
+  double* krep = (double*)calloc((size_t)Hkv * nblocks * 4 * D, sizeof(double));
+  double* qrep = (double*)calloc((size_t)Hq * 4 * D, sizeof(double));
+  int* used = (int*)calloc((size_t)nblocks, sizeof(int));
+  if (!krep || !qrep || !used) {
+    free(krep); free(qrep); free(used);
+    return -1;
+  }
+  /* four representatives per key block and group */
+  for (int g = 0; g < Hkv; ++g)
+    for (int b = 0; b < nblocks; ++b)
+      for (int r = 0; r < 4; ++r)
+        for (int d = 0; d < D; ++d) {
+          double s = 0.0;
+          for (int j = 0; j < kg; ++j) s += load_elem(K, fmt, ((size_t)(b * block + r * kg + j) * Hkv + g) * D + d);
+          krep[(((size_t)g * nblocks + b) * 4 + r) * D + d] = s / kg;
+        }
+  for (int t = 0; t < ntiles; ++t) {
+    const int i0 = t * tile, i1 = (i0 + tile < N) ? i0 + tile : N;
+    int has[4];
+    for (int q = 0; q < 4; ++q) {
+      const int a = i0 + q * qg, e = (a + qg < i1) ? a + qg : i1;
+      has[q] = e > a;
+      for (int h = 0; h < Hq; ++h)
+        for (int d = 0; d < D; ++d) {
+          double s = 0.0;
+          for (int i = a; i < e; ++i) s += load_elem(Q, fmt, ((size_t)i * Hq + h) * D + d);
+          qrep[((size_t)h * 4 + q) * D + d] = has[q] ? s / (e - a) : 0.0;
+        }
+    }
+    const int lb_first = (Lkv - N + i0) / block, lb_last = (Lkv - N + i1 - 1) / block;
+    for (int g = 0; g < Hkv; ++g) {
+      double* sc = scores + ((size_t)t * Hkv + g) * nblocks;
+      for (int b = 0; b < nblocks; ++b) {
+        if (b > lb_last) {
+          sc[b] = -INFINITY;
+        } else if (b >= lb_first) {
+          sc[b] = INFINITY;
+        } else {
+          double best = -INFINITY;
+          for (int h = g * G; h < (g + 1) * G; ++h)
+            for (int q = 0; q < 4; ++q) {
+              if (!has[q]) continue;
+              for (int r = 0; r < 4; ++r) {
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d)
+                  dot += qrep[((size_t)h * 4 + q) * D + d] * krep[(((size_t)g * nblocks + b) * 4 + r) * D + d];
+                if (dot > best) best = dot;
+              }
+            }
+          sc[b] = best;
+        }
+      }
+      /* topK by repeated selection of the best unused candidate (ties: smaller id) */
+      memset(used, 0, sizeof(int) * nblocks);
+      int32_t list[256];
+      const int K = topK < 256 ? topK : 256;
+      for (int k = 0; k < K; ++k) {
+        int arg = -1;
+        for (int b = 0; b < nblocks; ++b) {
+          if (used[b] || sc[b] == -INFINITY) continue;
+          if (arg < 0 || sc[b] > sc[arg]) arg = b;
+        }
+        list[k] = arg;
+        if (arg >= 0) used[arg] = 1;
+      }
+      for (int i = i0; i < i1; ++i)
+        for (int k = 0; k < topK; ++k) indices[((size_t)i * Hkv + g) * topK + k] = k < K ? list[k] : -1;
+    }
+  }
+  free(krep);
+  free(qrep);
+  free(used);
+  return 0;
+}

@@ -429,3 +429,70 @@ def test_select_r1_tail_queries_and_two_own_blocks():
     assert np.all(np.isneginf(sc[0, 0, 7:]))
     # the last tile (queries 64..79, 16 queries) sees blocks 0..7
     assert idx[79, 0, 0] == 7 and np.all(idx[64:80] == idx[79])
+
+
+# ----------------------------------------------------------------------------- selector R4
+# "Sparse Attention", Chapter 4, "R4: Four Representatives": consecutive quarters of a query
+# tile and of a key block are each summarised by their mean; the block score is the largest
+# of the 16 quarter-pair dot products over the group's heads.
+
+def _grid(rng, shape):
+    """Small multiples of 1/8: sums and means of a few of them are exact in float64."""
+    return rng.integers(-8, 9, size=shape).astype(np.float64) / 8
+
+
+def test_select_r4_equals_r1_when_blocks_are_constant():
+    rng = np.random.default_rng(21)
+    N, Lkv, Hq, Hkv, D = 512, 1024, 4, 2, 8
+    qv = _grid(rng, (N // 128, Hq, D))
+    kv = _grid(rng, (Lkv // 128, Hkv, D))
+    Q = np.repeat(qv, 128, axis=0)
+    K = np.repeat(kv, 128, axis=0)
+    i1, s1 = oracle.select_r1(Q, K, Lkv=Lkv, topK=5)
+    i4, s4 = oracle.select_r4(Q, K, Lkv=Lkv, topK=5)
+    assert np.array_equal(s1, s4) and np.array_equal(i1, i4)
+
+
+def test_select_r4_closed_form_quarter_constants_and_short_tile():
+    """Q constant over each 32-query quarter, K over each 32-key quarter: the representatives
+    are those constants, so the score is a maximum of explicit dot products.  N = 296: the
+    last tile holds 40 queries (quarters 0 and 1, the second with 8 queries)."""
+    rng = np.random.default_rng(22)
+    N, Lkv, Hq, Hkv, D, G = 296, 768, 4, 2, 8, 2
+    nq, nk = -(-N // 32), Lkv // 32
+    qv = _grid(rng, (nq, Hq, D))
+    kv = _grid(rng, (nk, Hkv, D))
+    Q = np.repeat(qv, 32, axis=0)[:N]
+    K = np.repeat(kv, 32, axis=0)
+    _, sc = oracle.select_r4(Q, K, Lkv=Lkv, topK=3)
+    for t in range(-(-N // 128)):
+        i0, i1 = 128 * t, min(128 * t + 128, N)
+        quarters = [i0 // 32 + q for q in range(4) if i0 + 32 * q < i1]
+        lb_first, lb_last = (Lkv - N + i0) // 128, (Lkv - N + i1 - 1) // 128
+        for g in range(Hkv):
+            for b in range(Lkv // 128):
+                if b > lb_last:
+                    assert sc[t, g, b] == -np.inf
+                elif b >= lb_first:
+                    assert sc[t, g, b] == np.inf
+                else:
+                    want = max(float(qv[q, h] @ kv[4 * b + r, g])
+                               for h in range(g * G, (g + 1) * G) for q in quarters for r in range(4))
+                    assert sc[t, g, b] == want, (t, g, b)
+
+
+def test_select_r4_finds_a_quarter_that_r1_averages_away():
+    """Block 2's mean key is zero, but its first 32 keys point along the queries: R1 scores it
+    0 and misses it, R4 scores it highest."""
+    rng = np.random.default_rng(23)
+    N, Lkv, Hq, Hkv, D = 128, 1024, 2, 1, 8
+    Q = np.zeros((N, Hq, D)); Q[:, :, 0] = 1.0
+    K = 0.01 * rng.standard_normal((Lkv, Hkv, D))
+    K[:, :, 0] = 0.1 * np.abs(rng.standard_normal((Lkv, Hkv)))  # every block mildly aligned
+    K[256:288, :, 0] = 6.0
+    K[288:384, :, 0] = -2.0                                       # block 2: mean 0 along e0
+    K[256:384, :, 1:] = 0.0
+    i1, _ = oracle.select_r1(Q, K, Lkv=Lkv, topK=3)
+    i4, s4 = oracle.select_r4(Q, K, Lkv=Lkv, topK=3)
+    assert 2 not in i1[0, 0].tolist()
+    assert i4[0, 0, 1] == 2 and abs(s4[0, 0, 2] - 6.0) < 1e-12  # after the forced own block 7
