@@ -51,8 +51,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="m3", choices=["tiny", "m3", "long", "lowreuse", "fp8"])
-    ap.add_argument("--lists", default="workload", choices=["workload", "r1"],
-                    help="block lists: the workload's own, or chosen by the R1 selector (once, before timing)")
+    ap.add_argument("--lists", default="workload", choices=["workload", "r1", "r4"],
+                    help="block lists: the workload's own, or chosen by the R1 / R4 selector (once, before timing)")
     ap.add_argument("--mode", default="general", choices=["general", "tiles", "bwd"],
                     help="general: schedule + attention + combine; tiles: the shared-list forward "
                          "(lists shared by 128 queries for r1, by the workload's query runs otherwise); "
@@ -389,17 +389,18 @@ def run_ours(args, world, rank, local, pg):
     stream = torch.cuda.current_stream()
 
     Q, K, V = (t.to(dev) for t in (wl.Q, wl.K, wl.V))
-    if args.lists == "r1":
+    if args.lists in ("r1", "r4"):
         if cfg.dtype != "bf16":
-            raise SystemExit("the R1 selector takes bf16 inputs")
-        idx_d = msa.select_blocks_r1(Q, K, cfg.topK)  # an input of the step, chosen once
+            raise SystemExit("the selectors take bf16 inputs")
+        select = msa.select_blocks_r1 if args.lists == "r1" else msa.select_blocks_r4
+        idx_d = select(Q, K, cfg.topK)  # an input of the step, chosen once
         torch.cuda.synchronize()
     else:
         idx_d = wl.indices.to(dev)
     tiles = args.mode == "tiles"
     tstatus = torch.zeros(1, dtype=torch.int32, device=dev)  # device flags of the shared-list kernel
     if tiles:
-        tile = 128 if args.lists == "r1" else cfg.run
+        tile = 128 if args.lists in ("r1", "r4") else cfg.run
         tile_lists = idx_d[::tile].contiguous()
         if tile % 16 or not torch.equal(torch.repeat_interleave(tile_lists, tile, 0)[:cfg.N], idx_d):
             raise SystemExit(f"workload {cfg.name}: lists are not shared by tiles of a multiple of 16 queries")
@@ -564,7 +565,8 @@ def run_ours(args, world, rank, local, pg):
                    "l2": "flushed (256 MiB write) before every timed step, outside the step events",
                    "parallelism": f"independent problem per GPU x{world}",
                    "path": "bwd" if bwd else "tiles" if tiles else ("kv_outer" if kv_path else "q_outer"),
-                   "lists": "R1 selector (chosen once, before timing)" if args.lists == "r1" else "workload",
+                   "lists": (f"{args.lists.upper()} selector (chosen once, before timing)" if args.lists != "workload"
+                             else "workload"),
                    "partials": args.partials,
                    "entries": E, "nsb": nsb, "tiles": T},
         "roofline": roof,

@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.msa_sparse_attn_fwd_tiles.restype = I
         L.msa_sparse_attn_fwd_tiles.argtypes = [Tensor, Tensor, Tensor, P, I, I, P, P, ctypes.c_float, P,
                                                 ctypes.POINTER(FwdOpts)]
+        L.msa_select_blocks_r4.restype = I
+        L.msa_select_blocks_r4.argtypes = [Tensor, Tensor, I, P, P, ctypes.c_size_t, P]
         L.msa_select_blocks_r1.restype = I
         L.msa_select_blocks_r1.argtypes = [Tensor, Tensor, I, P, P, ctypes.c_size_t, P]
         _lib = L
@@ -237,8 +239,15 @@ def sparse_attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, schedule:
     return O, LSE
 
 
-def select_blocks_r1(Q: torch.Tensor, K: torch.Tensor, topK: int, indices: torch.Tensor | None = None,
+def select_blocks_r4(Q: torch.Tensor, K: torch.Tensor, topK: int, indices: torch.Tensor | None = None,
                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """msa_select_blocks_r4: as select_blocks_r1 with four quarter-mean representatives."""
+    return select_blocks_r1(Q, K, topK, indices, workspace, stream, _entry="msa_select_blocks_r4")
+
+
+def select_blocks_r1(Q: torch.Tensor, K: torch.Tensor, topK: int, indices: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None, stream=None,
+                     _entry: str = "msa_select_blocks_r1") -> torch.Tensor:
     """msa_select_blocks_r1: int32 block lists [N, Hkv, topK] (device) for bf16 Q [N, Hq, 128]
     and K [Lkv, Hkv, 128]; the workspace is allocated here unless given."""
     N, Hq, _ = Q.shape
@@ -251,9 +260,9 @@ def select_blocks_r1(Q: torch.Tensor, K: torch.Tensor, topK: int, indices: torch
     ptr = workspace.data_ptr()
     aligned = (ptr + 255) // 256 * 256
     usable = max(0, workspace.numel() * workspace.element_size() - (aligned - ptr))
-    st = lib().msa_select_blocks_r1(_tensor(Q), _tensor(K), int(topK), indices.data_ptr(), aligned, usable,
-                                    _stream_ptr(stream))
-    _check(st, "msa_select_blocks_r1")
+    st = getattr(lib(), _entry)(_tensor(Q), _tensor(K), int(topK), indices.data_ptr(), aligned, usable,
+                                _stream_ptr(stream))
+    _check(st, _entry)
     return indices
 
 

@@ -336,8 +336,9 @@ size_t msa_select_workspace_bytes(int N, int Hq, int Hkv, int nblocks) {
   return msa::select_workspace_bytes(N, Hq, Hkv, nblocks);
 }
 
-msa_status_t msa_select_blocks_r1(msa_tensor_t Q, msa_tensor_t K, int topK, int32_t* indices, void* workspace,
-                                  size_t workspace_bytes, cudaStream_t stream) {
+namespace {
+msa_status_t select_blocks(int reps, msa_tensor_t Q, msa_tensor_t K, int topK, int32_t* indices, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
   if (!Q.ptr || !K.ptr || !indices || !workspace) return MSA_ERR_INVALID_ARG;
   if (!aligned16(Q.ptr) || !aligned16(K.ptr) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return MSA_ERR_INVALID_ARG;
@@ -351,7 +352,20 @@ msa_status_t msa_select_blocks_r1(msa_tensor_t Q, msa_tensor_t K, int topK, int3
             Hkv = static_cast<int>(K.h);
   if (Lkv / msa::kBlock > 40960) return MSA_ERR_UNSUPPORTED;
   if (workspace_bytes < msa::select_workspace_bytes(N, Hq, Hkv, Lkv / msa::kBlock)) return MSA_ERR_INVALID_ARG;
-  return from_cuda(msa::launch_select_r1(Q.ptr, K.ptr, N, Lkv, Hq, Hkv, topK, indices, workspace, stream));
+  return from_cuda(reps == 4 ? msa::launch_select_r4(Q.ptr, K.ptr, N, Lkv, Hq, Hkv, topK, indices, workspace, stream)
+                             : msa::launch_select_r1(Q.ptr, K.ptr, N, Lkv, Hq, Hkv, topK, indices, workspace, stream));
+}
+}  // namespace
+
+
+msa_status_t msa_select_blocks_r1(msa_tensor_t Q, msa_tensor_t K, int topK, int32_t* indices, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+  return select_blocks(1, Q, K, topK, indices, workspace, workspace_bytes, stream);
+}
+
+msa_status_t msa_select_blocks_r4(msa_tensor_t Q, msa_tensor_t K, int topK, int32_t* indices, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+  return select_blocks(4, Q, K, topK, indices, workspace, workspace_bytes, stream);
 }
 
 msa_status_t msa_sparse_attn_fwd_tiles(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, const int32_t* tile_lists,

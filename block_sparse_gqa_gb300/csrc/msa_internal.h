@@ -105,8 +105,10 @@ cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, 
 
 // select.cu: block selector R1
 size_t select_workspace_bytes(int N, int Hq, int Hkv, int nblocks);
-uint32_t select_smem_bytes(int nblocks);
+uint32_t select_smem_bytes(int nblocks, int reps);
 cudaError_t launch_select_r1(const void* Q, const void* K, int N, int Lkv, int Hq, int Hkv, int topK, int32_t* indices,
+                             void* workspace, cudaStream_t st);
+cudaError_t launch_select_r4(const void* Q, const void* K, int N, int Lkv, int Hq, int Hkv, int topK, int32_t* indices,
                              void* workspace, cudaStream_t st);
 
 // attn_tiles.cu: forward for lists shared by tiles of consecutive queries

@@ -19,6 +19,15 @@
 //                 columns) and their maximum; then topK rounds of a CTA-wide arg-max;
 //                 the list is written for every query of the tile.
 // All three read their inputs once: the selector is bound by HBM reads of Q and K.
+//
+// Block selector R4 (same chapter, "R4: Four Representatives"): the tile and the block
+// are each cut into four consecutive 32-token quarters, each summarised by its mean; the
+// block's score is the largest of the 16 quarter-pair dot products over the group's
+// heads.  A quarter of a short last tile that holds no query has no representative.
+//   pool_keys4    one CTA per (block, group): quarter x 4 row groups x 16 chunks  -> krep
+//   pool_queries4 one CTA per (tile, group): thread = (quarter, head, 8 columns)  -> qrep
+//   select4       as select, with the 64 query representatives in shared memory and
+//                 four key representatives per candidate block.
 #include <cuda_bf16.h>
 
 #include "msa_internal.h"
@@ -110,15 +119,49 @@ __device__ __forceinline__ bool better(float sa, int ba, float sb, int bb) {
   return sa > sb || (sa == sb && ba >= 0 && (bb < 0 || ba < bb));
 }
 
+// topK rounds of a CTA-wide arg-max over the scores sc[nblocks] (a chosen block is
+// struck out), then the list is written for every query of the tile.
+__device__ void topk_and_write(float* sc, int nblocks, int topK, int N, int Hkv, int g, int i0, int i1,
+                               int32_t* __restrict__ indices) {
+  __shared__ float red_s[kSelThreads / 32];
+  __shared__ int red_b[kSelThreads / 32];
+  __shared__ int list[64];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int k = 0; k < topK; ++k) {
+    float bs = -INFINITY;
+    int bb = -1;
+    for (int b = tid; b < nblocks; b += kSelThreads) {
+      const float s = sc[b];
+      if (s != -INFINITY && better(s, b, bs, bb)) { bs = s; bb = b; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+      const int ob = __shfl_xor_sync(0xffffffffu, bb, o);
+      if (ob >= 0 && better(os, ob, bs, bb)) { bs = os; bb = ob; }
+    }
+    if (lane == 0) { red_s[warp] = bs; red_b[warp] = bb; }
+    __syncthreads();
+    if (tid == 0) {
+      for (int w = 1; w < kSelThreads / 32; ++w)
+        if (red_b[w] >= 0 && better(red_s[w], red_b[w], bs, bb)) { bs = red_s[w]; bb = red_b[w]; }
+      list[k] = bb;
+      if (bb >= 0) sc[bb] = -INFINITY;
+    }
+    __syncthreads();
+  }
+  for (int e = tid; e < (i1 - i0) * topK; e += kSelThreads) {
+    const int i = i0 + e / topK, k = e % topK;
+    indices[(static_cast<int64_t>(i) * Hkv + g) * topK + k] = list[k];
+  }
+}
+
 __global__ void __launch_bounds__(kSelThreads) k_select(const float* __restrict__ qbar, const float* __restrict__ kbar,
                                                         int N, int Lkv, int Hq, int Hkv, int nblocks, int topK,
                                                         int32_t* __restrict__ indices) {
   extern __shared__ float sm[];
   float* qs = sm;                        // [16][128]
   float* sc = sm + kGroup * kHeadDim;    // [nblocks]
-  __shared__ float red_s[kSelThreads / 32];
-  __shared__ int red_b[kSelThreads / 32];
-  __shared__ int list[64];
   const int t = blockIdx.x, g = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i0 = t * kBlock, i1 = min(i0 + kBlock, N);
@@ -150,46 +193,108 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const float* __restrict_
     if (lane == 0) sc[b] = s;
   }
   __syncthreads();
-  // topK rounds of a CTA-wide arg-max; a chosen block is struck out
-  for (int k = 0; k < topK; ++k) {
-    float bs = -INFINITY;
-    int bb = -1;
-    for (int b = tid; b < nblocks; b += kSelThreads) {
-      const float s = sc[b];
-      if (s != -INFINITY && better(s, b, bs, bb)) { bs = s; bb = b; }
-    }
+  topk_and_write(sc, nblocks, topK, N, Hkv, g, i0, i1, indices);
+}
+
+
+// R4 key representatives: one CTA of 256 threads per (block, group); thread = (quarter
+// s = tid / 64, row group r = (tid / 16) % 4, 16-byte chunk c = tid % 16) sums keys
+// 32 s + r, 32 s + r + 4, ... of the block; the row groups are added in shared memory.
+__global__ void __launch_bounds__(256) k_pool_keys4(const __nv_bfloat16* __restrict__ K, int Hkv, int nblocks,
+                                                    float* __restrict__ krep) {
+  __shared__ float part[4][4][kHeadDim];
+  const int b = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, sq = tid >> 6, r = (tid >> 4) & 3, c = tid & 15;
+  const int64_t row = static_cast<int64_t>(Hkv) * kHeadDim / 8;  // uint4 per key
+  const uint4* src =
+      reinterpret_cast<const uint4*>(K + ((static_cast<int64_t>(b) * kBlock + 32 * sq) * Hkv + g) * kHeadDim) + c;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-      const int ob = __shfl_xor_sync(0xffffffffu, bb, o);
-      if (ob >= 0 && better(os, ob, bs, bb)) { bs = os; bb = ob; }
-    }
-    if (lane == 0) { red_s[warp] = bs; red_b[warp] = bb; }
-    __syncthreads();
-    if (tid == 0) {
-      for (int w = 1; w < kSelThreads / 32; ++w)
-        if (red_b[w] >= 0 && better(red_s[w], red_b[w], bs, bb)) { bs = red_s[w]; bb = red_b[w]; }
-      list[k] = bb;
-      if (bb >= 0) sc[bb] = -INFINITY;
-    }
-    __syncthreads();
-  }
-  for (int e = tid; e < (i1 - i0) * topK; e += kSelThreads) {
-    const int i = i0 + e / topK, k = e % topK;
-    indices[(static_cast<int64_t>(i) * Hkv + g) * topK + k] = list[k];
+  for (int j = r; j < 32; j += 4) add8(a, __ldg(src + j * row));
+#pragma unroll
+  for (int e = 0; e < 8; ++e) part[sq][r][c * 8 + e] = a[e];
+  __syncthreads();
+  for (int o = tid; o < 4 * kHeadDim; o += 256) {
+    const int q = o / kHeadDim, d = o % kHeadDim;
+    const float v = (part[q][0][d] + part[q][1][d]) + (part[q][2][d] + part[q][3][d]);
+    krep[((static_cast<int64_t>(g) * nblocks + b) * 4 + q) * kHeadDim + d] = v * (1.f / 32.f);
   }
 }
 
+// R4 query representatives: one CTA of 1024 threads per (tile, group); thread = (quarter
+// s = tid / 256, head h = (tid / 16) % 16, 8 columns c = tid % 16) sums the quarter's
+// queries (0 queries -> 0, never read).
+__global__ void __launch_bounds__(1024) k_pool_queries4(const __nv_bfloat16* __restrict__ Q, int N, int Hq,
+                                                        float* __restrict__ qrep) {
+  const int t = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, sq = tid >> 8, h = (tid >> 4) & 15, c = tid & 15;
+  const int a0 = t * kBlock + 32 * sq, a1 = min(a0 + 32, N);
+  const int64_t row = static_cast<int64_t>(Hq) * kHeadDim / 8;
+  const uint4* src = reinterpret_cast<const uint4*>(Q + (static_cast<int64_t>(a0) * Hq + g * kGroup + h) * kHeadDim) + c;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int i = 0; i < a1 - a0; ++i) add8(a, __ldg(src + i * row));
+  const float inv = a1 > a0 ? 1.f / static_cast<float>(a1 - a0) : 0.f;
+  float* dst = qrep + ((static_cast<int64_t>(t) * Hq + g * kGroup + h) * 4 + sq) * kHeadDim + c * 8;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) dst[e] = a[e] * inv;
+}
+
+__global__ void __launch_bounds__(kSelThreads) k_select4(const float* __restrict__ qrep, const float* __restrict__ krep,
+                                                         int N, int Lkv, int Hq, int Hkv, int nblocks, int topK,
+                                                         int32_t* __restrict__ indices) {
+  extern __shared__ float sm[];
+  float* qs = sm;                            // [16 heads][4 quarters][128]
+  float* sc = sm + kGroup * 4 * kHeadDim;    // [nblocks]
+  const int t = blockIdx.x, g = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i0 = t * kBlock, i1 = min(i0 + kBlock, N);
+  const int nq = (i1 - i0 + 31) / 32;  // quarters holding queries
+  const int lb_first = (Lkv - N + i0) / kBlock, lb_last = (Lkv - N + i1 - 1) / kBlock;
+
+  const float* qsrc = qrep + (static_cast<int64_t>(t) * Hq + g * kGroup) * 4 * kHeadDim;
+  for (int e = tid; e < kGroup * 4 * kHeadDim; e += kSelThreads) qs[e] = qsrc[e];
+  __syncthreads();
+  // scores: one warp per candidate block, lane = columns 4 lane .. 4 lane + 3
+  for (int b = warp; b < nblocks; b += kSelThreads / 32) {
+    float s;
+    if (b > lb_last) {
+      s = -INFINITY;
+    } else if (b >= lb_first) {
+      s = INFINITY;
+    } else {
+      float m = -INFINITY;
+      const float4* kb = reinterpret_cast<const float4*>(krep + (static_cast<int64_t>(g) * nblocks + b) * 4 * kHeadDim);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float4 k4 = kb[r * (kHeadDim / 4) + lane];
+        for (int q = 0; q < nq; ++q) {
+          float part[kGroup];
+#pragma unroll
+          for (int h = 0; h < kGroup; ++h) {
+            const float4 q4 = reinterpret_cast<const float4*>(qs + (h * 4 + q) * kHeadDim)[lane];
+            part[h] = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, q4.w * k4.w)));
+          }
+          m = fmaxf(m, warp_sum16(part, lane));  // dot product of head (lane >> 1)
+        }
+      }
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      s = m;
+    }
+    if (lane == 0) sc[b] = s;
+  }
+  __syncthreads();
+  topk_and_write(sc, nblocks, topK, N, Hkv, g, i0, i1, indices);
+}
 }  // namespace
 
+// Enough for either selector: R4 keeps four representatives per tile / block, R1 one.
 size_t select_workspace_bytes(int N, int Hq, int Hkv, int nblocks) {
   const size_t ntiles = (static_cast<size_t>(N) + kBlock - 1) / kBlock;
-  const size_t q = ntiles * Hq * kHeadDim * sizeof(float);
-  return ((q + 255) / 256) * 256 + static_cast<size_t>(Hkv) * nblocks * kHeadDim * sizeof(float);
+  const size_t q = ntiles * Hq * 4 * kHeadDim * sizeof(float);
+  return ((q + 255) / 256) * 256 + static_cast<size_t>(Hkv) * nblocks * 4 * kHeadDim * sizeof(float);
 }
 
-uint32_t select_smem_bytes(int nblocks) {
-  return static_cast<uint32_t>((kGroup * kHeadDim + nblocks) * sizeof(float));
+uint32_t select_smem_bytes(int nblocks, int reps) {
+  return static_cast<uint32_t>((kGroup * reps * kHeadDim + nblocks) * sizeof(float));
 }
 
 cudaError_t launch_select_r1(const void* Q, const void* K, int N, int Lkv, int Hq, int Hkv, int topK, int32_t* indices,
@@ -199,7 +304,7 @@ cudaError_t launch_select_r1(const void* Q, const void* K, int N, int Lkv, int H
   const size_t q = static_cast<size_t>(ntiles) * Hq * kHeadDim * sizeof(float);
   float* qbar = static_cast<float*>(workspace);
   float* kbar = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((q + 255) / 256) * 256);
-  const uint32_t smem = select_smem_bytes(nblocks);
+  const uint32_t smem = select_smem_bytes(nblocks, 1);
   static uint32_t smem_set = 0;
   if (smem > 48 * 1024 && smem > smem_set) {
     cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -209,6 +314,26 @@ cudaError_t launch_select_r1(const void* Q, const void* K, int N, int Lkv, int H
   k_pool_keys<<<dim3(nblocks, Hkv), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(K), Hkv, nblocks, kbar);
   k_pool_queries<<<dim3(ntiles, Hkv), 1024, 0, st>>>(static_cast<const __nv_bfloat16*>(Q), N, Hq, qbar);
   k_select<<<dim3(ntiles, Hkv), kSelThreads, smem, st>>>(qbar, kbar, N, Lkv, Hq, Hkv, nblocks, topK, indices);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select_r4(const void* Q, const void* K, int N, int Lkv, int Hq, int Hkv, int topK, int32_t* indices,
+                             void* workspace, cudaStream_t st) {
+  const int nblocks = Lkv / kBlock;
+  const int ntiles = (N + kBlock - 1) / kBlock;
+  const size_t q = static_cast<size_t>(ntiles) * Hq * 4 * kHeadDim * sizeof(float);
+  float* qrep = static_cast<float*>(workspace);
+  float* krep = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((q + 255) / 256) * 256);
+  const uint32_t smem = select_smem_bytes(nblocks, 4);
+  static uint32_t smem_set = 0;
+  if (smem > 48 * 1024 && smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_select4, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    smem_set = smem;
+  }
+  k_pool_keys4<<<dim3(nblocks, Hkv), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(K), Hkv, nblocks, krep);
+  k_pool_queries4<<<dim3(ntiles, Hkv), 1024, 0, st>>>(static_cast<const __nv_bfloat16*>(Q), N, Hq, qrep);
+  k_select4<<<dim3(ntiles, Hkv), kSelThreads, smem, st>>>(qrep, krep, N, Lkv, Hq, Hkv, nblocks, topK, indices);
   return cudaGetLastError();
 }
 

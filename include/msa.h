@@ -259,7 +259,7 @@ msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int N, int Hkv,
  * Q: bf16 [N, Hq, 128]; K: bf16 [Lkv, Hkv, 128], Lkv a multiple of 128, N <= Lkv
  * (queries are the last N positions); Hq = 16 * Hkv.  indices: device int32
  * [N, Hkv, topK], written completely.  workspace: device memory of at least
- * msa_select_workspace_bytes(N, Hq, Hkv, Lkv / 128) bytes, 256-byte aligned, owned by
+ * msa_select_workspace_bytes(N, Hq, Hkv, Lkv / 128) bytes (enough for R1 and R4), 256-byte aligned, owned by
  * the caller; its contents are scratch.  Arithmetic is fp32 (means, dot products).
  * Asynchronous on `stream`; nothing is allocated.
  *
@@ -270,6 +270,18 @@ msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int N, int Hkv,
  */
 size_t msa_select_workspace_bytes(int N, int Hq, int Hkv, int nblocks);
 msa_status_t msa_select_blocks_r1(msa_tensor_t Q, msa_tensor_t K, int topK, int32_t* indices, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * msa_select_blocks_r4 -- block selector R4 ("Sparse Attention" (dinara-dl), Chapter 4,
+ * "R4: Four Representatives").  As msa_select_blocks_r1, except that a 128-query tile and
+ * a 128-key block are each cut into four consecutive 32-token quarters summarised by
+ * their means, and a block's score is the largest of the 16 quarter-pair dot products
+ * over the group's query heads (a quarter of a short last tile that holds no query has no
+ * representative).  Same arguments, list order, forced own blocks, padding, workspace
+ * size (msa_select_workspace_bytes covers both selectors) and errors.
+ */
+msa_status_t msa_select_blocks_r4(msa_tensor_t Q, msa_tensor_t K, int topK, int32_t* indices, void* workspace,
                                   size_t workspace_bytes, cudaStream_t stream);
 
 /*
