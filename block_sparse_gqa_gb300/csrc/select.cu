@@ -24,10 +24,14 @@
 // are each cut into four consecutive 32-token quarters, each summarised by its mean; the
 // block's score is the largest of the 16 quarter-pair dot products over the group's
 // heads.  A quarter of a short last tile that holds no query has no representative.
-//   pool_keys4    one CTA per (block, group): quarter x 4 row groups x 16 chunks  -> krep
-//   pool_queries4 one CTA per (tile, group): thread = (quarter, head, 8 columns)  -> qrep
-//   select4       as select, with the 64 query representatives in shared memory and
-//                 four key representatives per candidate block.
+//   pool_keys4    one CTA per (block, group): quarter x 4 row groups x 16 chunks
+//                 -> krepT [group][128 columns][4 nblocks]
+//   pool_queries4 one CTA per (tile, group): thread = (quarter, head, 8 columns)
+//                 -> qrepT [tile][group][128 columns][64 = head x 4 + quarter]
+//   select4       the scores are a 64 x 4 nblocks x 128 product per (tile, group) with a
+//                 maximum over each block's 64 x 4 entries: chunks of 16 candidate blocks,
+//                 both operands transposed in shared memory, each thread accumulating 8
+//                 query x 2 key representatives with packed fp32 FMAs; then the R1 top-K.
 #include <cuda_bf16.h>
 
 #include "msa_internal.h"
@@ -214,9 +218,9 @@ __global__ void __launch_bounds__(256) k_pool_keys4(const __nv_bfloat16* __restr
   for (int e = 0; e < 8; ++e) part[sq][r][c * 8 + e] = a[e];
   __syncthreads();
   for (int o = tid; o < 4 * kHeadDim; o += 256) {
-    const int q = o / kHeadDim, d = o % kHeadDim;
+    const int q = o & 3, d = o >> 2;
     const float v = (part[q][0][d] + part[q][1][d]) + (part[q][2][d] + part[q][3][d]);
-    krep[((static_cast<int64_t>(g) * nblocks + b) * 4 + q) * kHeadDim + d] = v * (1.f / 32.f);
+    krep[(static_cast<int64_t>(g) * kHeadDim + d) * (4 * static_cast<int64_t>(nblocks)) + 4 * b + q] = v * (1.f / 32.f);
   }
 }
 
@@ -232,58 +236,95 @@ __global__ void __launch_bounds__(1024) k_pool_queries4(const __nv_bfloat16* __r
   float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int i = 0; i < a1 - a0; ++i) add8(a, __ldg(src + i * row));
   const float inv = a1 > a0 ? 1.f / static_cast<float>(a1 - a0) : 0.f;
-  float* dst = qrep + ((static_cast<int64_t>(t) * Hq + g * kGroup + h) * 4 + sq) * kHeadDim + c * 8;
+  const int Hkv = Hq / kGroup;
+  float* dst = qrep + ((static_cast<int64_t>(t) * Hkv + g) * kHeadDim + c * 8) * 64 + h * 4 + sq;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) dst[e] = a[e] * inv;
+  for (int e = 0; e < 8; ++e) dst[e * 64] = a[e] * inv;
 }
 
+// (x0, x1) * (s, s) + (c0, c1) on a pair of floats held as one 64-bit register
+__device__ __forceinline__ uint64_t ffma2s(float s, uint64_t x, uint64_t c) {
+  uint64_t ss, d;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(s));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(ss), "l"(c));
+  return d;
+}
+
+// qrepT [tile][group][128][64], krepT [group][128][4 nblocks]; one CTA per (tile, group).
+// Thread (warp w, lane l) of a chunk of 16 candidate blocks (64 key representatives)
+// accumulates query representatives 8 w .. 8 w + 7 against key representatives 2 l, 2 l + 1.
 __global__ void __launch_bounds__(kSelThreads) k_select4(const float* __restrict__ qrep, const float* __restrict__ krep,
                                                          int N, int Lkv, int Hq, int Hkv, int nblocks, int topK,
                                                          int32_t* __restrict__ indices) {
   extern __shared__ float sm[];
-  float* qs = sm;                            // [16 heads][4 quarters][128]
-  float* sc = sm + kGroup * 4 * kHeadDim;    // [nblocks]
+  float* qs = sm;                       // [128][64]
+  float* ks = sm + kHeadDim * 64;       // [128][64]
+  float* red = ks + kHeadDim * 64;      // [8 warps][64]
+  float* sc = red + 8 * 64;             // [nblocks]
   const int t = blockIdx.x, g = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i0 = t * kBlock, i1 = min(i0 + kBlock, N);
   const int nq = (i1 - i0 + 31) / 32;  // quarters holding queries
   const int lb_first = (Lkv - N + i0) / kBlock, lb_last = (Lkv - N + i1 - 1) / kBlock;
+  const int64_t kcols = 4 * static_cast<int64_t>(nblocks);
 
-  const float* qsrc = qrep + (static_cast<int64_t>(t) * Hq + g * kGroup) * 4 * kHeadDim;
-  for (int e = tid; e < kGroup * 4 * kHeadDim; e += kSelThreads) qs[e] = qsrc[e];
-  __syncthreads();
-  // scores: one warp per candidate block, lane = columns 4 lane .. 4 lane + 3
-  for (int b = warp; b < nblocks; b += kSelThreads / 32) {
-    float s;
-    if (b > lb_last) {
-      s = -INFINITY;
-    } else if (b >= lb_first) {
-      s = INFINITY;
-    } else {
-      float m = -INFINITY;
-      const float4* kb = reinterpret_cast<const float4*>(krep + (static_cast<int64_t>(g) * nblocks + b) * 4 * kHeadDim);
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float4 k4 = kb[r * (kHeadDim / 4) + lane];
-        for (int q = 0; q < nq; ++q) {
-          float part[kGroup];
-#pragma unroll
-          for (int h = 0; h < kGroup; ++h) {
-            const float4 q4 = reinterpret_cast<const float4*>(qs + (h * 4 + q) * kHeadDim)[lane];
-            part[h] = fmaf(q4.x, k4.x, fmaf(q4.y, k4.y, fmaf(q4.z, k4.z, q4.w * k4.w)));
-          }
-          m = fmaxf(m, warp_sum16(part, lane));  // dot product of head (lane >> 1)
-        }
-      }
-#pragma unroll
-      for (int o = 2; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      s = m;
+  const float4* qsrc = reinterpret_cast<const float4*>(qrep + (static_cast<int64_t>(t) * Hkv + g) * kHeadDim * 64);
+  for (int e = tid; e < kHeadDim * 16; e += kSelThreads) reinterpret_cast<float4*>(qs)[e] = qsrc[e];
+  // candidates scored: blocks before the tile's first own block
+  for (int b0 = 0; b0 < lb_first; b0 += 16) {
+    __syncthreads();  // the previous chunk's key representatives have been read
+    const float* kc = krep + static_cast<int64_t>(g) * kHeadDim * kcols + 4 * b0;
+    for (int e = tid; e < kHeadDim * 16; e += kSelThreads) {
+      const int d = e >> 4, c4 = (e & 15) * 4;  // 4 representatives (one block) per float4
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (b0 + (c4 >> 2) < nblocks) v = *reinterpret_cast<const float4*>(kc + d * kcols + c4);
+      reinterpret_cast<float4*>(ks + d * 64)[e & 15] = v;
     }
-    if (lane == 0) sc[b] = s;
+    __syncthreads();
+    uint64_t acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0;
+#pragma unroll 4
+    for (int d = 0; d < kHeadDim; ++d) {
+      const float4 qa = reinterpret_cast<const float4*>(qs + d * 64 + 8 * warp)[0];
+      const float4 qb = reinterpret_cast<const float4*>(qs + d * 64 + 8 * warp)[1];
+      const uint64_t k2 = reinterpret_cast<const uint64_t*>(ks + d * 64)[lane];
+      acc[0] = ffma2s(qa.x, k2, acc[0]);
+      acc[1] = ffma2s(qa.y, k2, acc[1]);
+      acc[2] = ffma2s(qa.z, k2, acc[2]);
+      acc[3] = ffma2s(qa.w, k2, acc[3]);
+      acc[4] = ffma2s(qb.x, k2, acc[4]);
+      acc[5] = ffma2s(qb.y, k2, acc[5]);
+      acc[6] = ffma2s(qb.z, k2, acc[6]);
+      acc[7] = ffma2s(qb.w, k2, acc[7]);
+    }
+    // maximum over this warp's query representatives (quarter = index % 4 must hold queries)
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (((8 * warp + i) & 3) >= nq) continue;
+      float x0, x1;
+      asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(acc[i]));
+      m0 = fmaxf(m0, x0);
+      m1 = fmaxf(m1, x1);
+    }
+    red[warp * 64 + 2 * lane] = m0;
+    red[warp * 64 + 2 * lane + 1] = m1;
+    __syncthreads();
+    if (tid < 16 && b0 + tid < lb_first) {
+      float m = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 8; ++w)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) m = fmaxf(m, red[w * 64 + 4 * tid + r]);
+      sc[b0 + tid] = m;
+    }
   }
+  for (int b = lb_first + tid; b < nblocks; b += kSelThreads) sc[b] = b > lb_last ? -INFINITY : INFINITY;
   __syncthreads();
   topk_and_write(sc, nblocks, topK, N, Hkv, g, i0, i1, indices);
 }
+
 }  // namespace
 
 // Enough for either selector: R4 keeps four representatives per tile / block, R1 one.
@@ -294,7 +335,8 @@ size_t select_workspace_bytes(int N, int Hq, int Hkv, int nblocks) {
 }
 
 uint32_t select_smem_bytes(int nblocks, int reps) {
-  return static_cast<uint32_t>((kGroup * reps * kHeadDim + nblocks) * sizeof(float));
+  if (reps == 4) return static_cast<uint32_t>((2 * kHeadDim * 64 + 8 * 64 + nblocks) * sizeof(float));
+  return static_cast<uint32_t>((kGroup * kHeadDim + nblocks) * sizeof(float));
 }
 
 cudaError_t launch_select_r1(const void* Q, const void* K, int N, int Lkv, int Hq, int Hkv, int topK, int32_t* indices,
