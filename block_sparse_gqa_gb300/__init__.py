@@ -40,7 +40,8 @@ class Tensor(ctypes.Structure):
 class FwdOpts(ctypes.Structure):
     _fields_ = [("stream", ctypes.c_void_p), ("path", ctypes.c_int), ("q_descale", ctypes.c_float),
                 ("k_descale", ctypes.c_float), ("v_descale", ctypes.c_float),
-                ("stage_events", ctypes.c_void_p * 3), ("num_ctas", ctypes.c_int), ("partials_fp32", ctypes.c_int)]
+                ("stage_events", ctypes.c_void_p * 3), ("num_ctas", ctypes.c_int), ("partials_fp32", ctypes.c_int),
+                ("debug_flags", ctypes.c_int)]
 
 
 class ScheduleInfo(ctypes.Structure):
@@ -214,7 +215,7 @@ def sparse_attn_bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.
 def sparse_attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, schedule: Schedule, scale: float | None = None,
                     O: torch.Tensor | None = None, LSE: torch.Tensor | None = None, path: str = "auto",
                     descales=(1.0, 1.0, 1.0), stage_events=None, num_ctas: int = 0, partials_fp32: bool = False,
-                    stream=None):
+                    debug_flags: int = 0, stream=None):
     """msa_sparse_attn_fwd; returns (O bf16 [N,Hq,D], LSE fp32 [N,Hq])."""
     N, Hq, D = Q.shape
     if scale is None:
@@ -230,6 +231,7 @@ def sparse_attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, schedule:
     opts.q_descale, opts.k_descale, opts.v_descale = (float(x) for x in descales)
     opts.num_ctas = int(num_ctas)
     opts.partials_fp32 = 1 if partials_fp32 else 0
+    opts.debug_flags = int(debug_flags)
     if stage_events is not None:
         for k, ev in enumerate(stage_events[:3]):
             opts.stage_events[k] = ev

@@ -125,6 +125,7 @@ struct KvParams {
   int N, Lkv, nblocks;
   float sl2;  // scale * log2(e) (* q descale * k descale for E4M3)
   int force_path;
+  int debug_flags;  // bit 0: the scheduler publishes no work (every other role's bounded wait expires)
 };
 
 __device__ __forceinline__ void flag_timeout(SchedHeader* hdr) { atomicOr(&hdr->status, kStatusTimeout); }
@@ -300,7 +301,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
 
   if (warp < 4) {
     regs_dec<kRegCtl>();
-    if (warp == 0) {
+    if (warp == 0 && (p.debug_flags & 1) == 0) {
       // ---------------------------------------------------------- producer (whole warp)
       int* counter = &p.hdr->pad[0];
       const int T = p.hdr->ntiles;
@@ -778,6 +779,7 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   p.nblocks = s->nblocks;
   p.sl2 = a.scale * a.qk_descale * 1.4426950408889634f;
   p.force_path = a.force_path;
+  p.debug_flags = a.debug_flags;
   static bool attr_set[4] = {false, false, false, false};
   const int inst = (fp8 ? 1 : 0) | (a.f32p ? 2 : 0);
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, KvParams);

@@ -227,7 +227,8 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
   const int Hq = static_cast<int>(Q.h);
   cudaError_t e;
   if (opts->stage_events[0] && (e = cudaEventRecord(opts->stage_events[0], stream))) return from_cuda(e);
-  msa::KvOuterArgs a{s, Q.ptr, K.ptr, V.ptr, Hq, s->nblocks * msa::kBlock, scale, force, ctas, fp8, qk_descale, f32p};
+  msa::KvOuterArgs a{s, Q.ptr, K.ptr, V.ptr, Hq, s->nblocks * msa::kBlock, scale, force, ctas, fp8, qk_descale, f32p,
+                     opts->debug_flags};
   if ((e = msa::launch_kv_outer(a, stream))) return from_cuda(e);
   if (opts->stage_events[1] && (e = cudaEventRecord(opts->stage_events[1], stream))) return from_cuda(e);
   if ((e = msa::launch_combine(s, Hq, O, LSE, v_descale, force, f32p, stream))) return from_cuda(e);

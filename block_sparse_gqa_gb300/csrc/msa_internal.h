@@ -92,6 +92,7 @@ struct KvOuterArgs {
   bool fp8;          // E4M3 inputs
   float qk_descale;  // q descale * k descale (1 for bf16)
   bool f32p;         // fp32 partial outputs
+  int debug_flags;   // msa_fwd_opts_t.debug_flags
 };
 cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st);
 

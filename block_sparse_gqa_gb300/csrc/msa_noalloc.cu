@@ -122,7 +122,7 @@ extern "C" msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int 
   cudaError_t e;
   if ((e = msa::enqueue_schedule(&s, indices, stream))) return msa::status_from_cuda(e);
   if (opts->stage_events[0] && (e = cudaEventRecord(opts->stage_events[0], stream))) return msa::status_from_cuda(e);
-  msa::KvOuterArgs a{&s, Q.ptr, K.ptr, V.ptr, Hq, nblocks * msa::kBlock, scale, force, ctas, false, 1.f, false};
+  msa::KvOuterArgs a{&s, Q.ptr, K.ptr, V.ptr, Hq, nblocks * msa::kBlock, scale, force, ctas, false, 1.f, false, 0};
   if ((e = msa::launch_kv_outer(a, stream))) return msa::status_from_cuda(e);
   if (opts->stage_events[1] && (e = cudaEventRecord(opts->stage_events[1], stream))) return msa::status_from_cuda(e);
   if ((e = msa::launch_combine(&s, Hq, O, LSE, 1.f, force, false, stream))) return msa::status_from_cuda(e);
