@@ -23,7 +23,8 @@
 //                tile info and query ids ahead of time and publishes each tile in a
 //                shared-memory ring for the other roles (it only waits for ring slots)
 //   warp 2       K/V loader: on a row change loads K_b into the next of two K
-//                buffers and V_b into the V buffer (TMA); a ring slot is reused only
+//                buffers and V_b into the V buffer (TMA; E4M3: into the next of two V
+//                buffers, widened to f16 by the whole warp); a ring slot is reused only
 //                after both this warp and the output warps have released it
 //   warp 1       TMEM allocation (512 columns: S[0], S[1], O[0], O[1]) and issue of
 //                S[s] = Q K^T (tcgen05, smem x smem) for tile t into stage s = t % 2
@@ -88,8 +89,11 @@ struct Lay {
   static constexpr uint32_t kOffQ = 0;                       // + kInTile * stage
   static constexpr uint32_t kOffK0 = kQStages * kInTile;
   static constexpr uint32_t kOffK1 = kOffK0 + kInTile;
-  static constexpr uint32_t kOffV = kOffK1 + kInTile;         // 16-bit V (bf16, or f16 from E4M3)
-  static constexpr uint32_t kOffVst = kOffV + kTileBytes;     // E4M3 V as loaded (fp8 only)
+  // 16-bit V (bf16, or f16 widened from E4M3): one buffer for bf16 (shared memory is full),
+  // two for E4M3 so that the next row's V is widened while this row's P V runs
+  static constexpr int kVBuf = kFp8 ? 2 : 1;
+  static constexpr uint32_t kOffV = kOffK1 + kInTile;
+  static constexpr uint32_t kOffVst = kOffV + kVBuf * kTileBytes;  // E4M3 V as loaded (fp8 only)
   static constexpr uint32_t kOffSt = kOffVst + (kFp8 ? 16384 : 0);  // output staging
   static constexpr uint32_t kOffCtl = kOffSt + kTileBytes;
   static constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + alignment slack
@@ -98,9 +102,9 @@ static_assert(Lay<false>::kSmemBytes <= 232448 && Lay<true>::kSmemBytes <= 23244
 
 // barrier slots (8 bytes each) at the start of the control area
 enum {
-  B_QFULL0 = 0, B_KFULL0 = 3, B_KFREE0 = 5, B_VFULL = 7, B_VFREE = 8, B_VSTAGE = 9,
-  B_SFULL0 = 10, B_PFULL0 = 12, B_PVDONE0 = 14, B_OFREE0 = 16, B_TFULL0 = 18, B_TEMPTY0 = 18 + kRing,
-  B_COUNT = 18 + 2 * kRing
+  B_QFULL0 = 0, B_KFULL0 = 3, B_KFREE0 = 5, B_VFULL0 = 7, B_VFREE0 = 9, B_VSTAGE = 11,
+  B_SFULL0 = 12, B_PFULL0 = 14, B_PVDONE0 = 16, B_OFREE0 = 18, B_TFULL0 = 20, B_TEMPTY0 = 20 + kRing,
+  B_COUNT = 20 + 2 * kRing
 };
 constexpr uint32_t kOffTmemSlot = 8 * B_COUNT;  // 4 bytes
 constexpr uint32_t kOffRing = 512;              // kRing entries of 64 bytes
@@ -273,8 +277,10 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
 
   if (tid == 0) {
     for (int s = 0; s < kQStages; ++s) mbar_init(bar(B_QFULL0 + s), 128);  // one cp.async arrive per gather thread
-    mbar_init(bar(B_VFULL), 1);
-    mbar_init(bar(B_VFREE), 1);
+    for (int v = 0; v < 2; ++v) {
+      mbar_init(bar(B_VFULL0 + v), 1);
+      mbar_init(bar(B_VFREE0 + v), 1);
+    }
     mbar_init(bar(B_VSTAGE), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_KFULL0 + s), 1);
@@ -458,6 +464,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
         if (!ok || count == 0) break;
         if (!(flags & 1)) continue;
         const int g = row / p.nblocks, b = row - g * p.nblocks, kb = nk & 1;
+        const int vb = nk % L::kVBuf, vuse = nk / L::kVBuf;  // V buffer of this row, its use count
         if (lane == 0) {
           // K: two buffers, buffer kb was last read by the row before the previous one
           const uint32_t dk = sb + (kb ? L::kOffK1 : L::kOffK0);
@@ -471,8 +478,8 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
               mbar_expect_tx(bar(B_VSTAGE), 16384);
               tma_load_3d(sb + L::kOffVst, &tmV, 0, g, b * kBlock, bar(B_VSTAGE), pol_kv);
             }
-            // V: one buffer, freed after the previous row's last P V
-            ok = mbar_wait(bar(B_VFREE), (nk & 1) ^ 1);
+            // V buffer vb: free once the last P V of the row that used it before is done
+            ok = mbar_wait(bar(B_VFREE0 + vb), (vuse & 1) ^ 1);
             if constexpr (kFp8) {
               const bool staged = mbar_wait(bar(B_VSTAGE), nk & 1);  // also on failure: no copy left in flight
               ok = ok && staged;
@@ -480,9 +487,9 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           }
           if (ok) {
             if constexpr (!kFp8) {
-              mbar_expect_tx(bar(B_VFULL), kTileBytes);
-              tma_load_3d(sb + L::kOffV, &tmV, 0, g, b * kBlock, bar(B_VFULL), pol_kv);
-              tma_load_3d(sb + L::kOffV + 16384, &tmV, 64, g, b * kBlock, bar(B_VFULL), pol_kv);
+              mbar_expect_tx(bar(B_VFULL0), kTileBytes);
+              tma_load_3d(sb + L::kOffV, &tmV, 0, g, b * kBlock, bar(B_VFULL0), pol_kv);
+              tma_load_3d(sb + L::kOffV + 16384, &tmV, 64, g, b * kBlock, bar(B_VFULL0), pol_kv);
             }
           }
         }
@@ -502,13 +509,13 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
               asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * q + 1]) : "h"(static_cast<uint16_t>(w[q] >> 16)));
             }
             const int half = c >> 2, ch = (2 * c) & 7;  // D 16c.. lies in half c/4, 16-byte chunks 2c%8, +1
-            uint8_t* dst = smem + L::kOffV + half * 16384 + k * 128;
+            uint8_t* dst = smem + L::kOffV + vb * kTileBytes + half * 16384 + k * 128;
             *reinterpret_cast<uint4*>(dst + ((ch ^ (k & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
             *reinterpret_cast<uint4*>(dst + (((ch + 1) ^ (k & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
           }
           fence_proxy_async_smem();  // read next by the tensor cores
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_VFULL));
+          if (lane == 0) mbar_arrive(bar(B_VFULL0 + vb));
         }
         ++nk;
       }
@@ -527,15 +534,15 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           if (count == 0) break;
           const int s = u & 1;
           if (flags & 1) {
-            // a new row: the V buffer is free once the P V MMAs issued so far are done
-            if (++vseg > 0) mma_commit(bar(B_VFREE));
-            if (!(ok = mbar_wait(bar(B_VFULL), vseg & 1))) break;
+            // a new row: the previous row's V buffer is free once the P V MMAs issued so far are done
+            if (++vseg > 0) mma_commit(bar(B_VFREE0 + (vseg - 1) % L::kVBuf));
+            if (!(ok = mbar_wait(bar(B_VFULL0 + vseg % L::kVBuf), (vseg / L::kVBuf) & 1))) break;
           }
           if (!(ok = mbar_wait(bar(B_PFULL0 + s), (u >> 1) & 1))) break;
           // O[s] is reused: the output warps must have read O of tile u-2
           if (u >= 2 && !(ok = mbar_wait(bar(B_OFREE0 + s), ((u - 2) >> 1) & 1))) break;
           tc_fence_after();
-          const uint32_t va = sb + L::kOffV;
+          const uint32_t va = sb + L::kOffV + (vseg % L::kVBuf) * kTileBytes;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             mma_f16_ts(tmem + 256 + s * 128, tmem + s * 128 + k * 8, smem_desc(va + k * 2048, 16384, 1024, 2),
