@@ -150,3 +150,23 @@ def test_bwd_rejects_unsupported():
         msa.sparse_attn_bwd(Q, K[:384].contiguous(), V[:384].contiguous(), O, dO, LSE, s)
     assert e.value.status == 1
     s.close()
+
+
+def test_bwd_long_sampled():
+    """The long workload (N = 32768 at the tail of Lkv = 131072, lists shared by runs of 64
+    queries, Zipf-weighted picks) at full size: dQ of sampled queries, dK and dV of the two
+    last blocks of groups 0 and 3 (the own blocks of the last queries, masked)."""
+    wl = workloads.make_workload("long")
+    cfg = wl.cfg
+    rng = np.random.default_rng(43)
+    dO = bf16(rng, (cfg.N, cfg.Hq, cfg.D))
+    dQ, dK, dV = run_gpu(wl.Q, wl.K, wl.V, dO, wl.indices.numpy(), cfg.nblocks, cfg.scale)
+    qids = workloads.sample_queries(cfg, 32)
+    nb = cfg.nblocks
+    rows = np.array([0 * nb + nb - 1, 0 * nb + nb - 2, 3 * nb + nb - 1], np.int32)
+    Qb, Kb, Vb = wl.np_inputs()
+    rQ, rK, rV, _ = oracle.attn_bwd(Qb, Kb, Vb, bits(dO), wl.indices.numpy(), Lkv=cfg.Lkv, scale=cfg.scale,
+                                    qids=qids, rows=rows)
+    gK = np.stack([dK[(r % nb) * 128:(r % nb + 1) * 128, r // nb] for r in rows])
+    gV = np.stack([dV[(r % nb) * 128:(r % nb + 1) * 128, r // nb] for r in rows])
+    print("rel-L2 dQ dK dV", check((dQ[qids], gK, gV), (rQ, rK, rV)))
