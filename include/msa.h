@@ -83,8 +83,9 @@ typedef struct {
    * 16x (bf16) or 32x (fp32) the final bf16 output).  fp32 doubles the partial bytes and
    * keeps the per-block P V sums unrounded until the combine. */
   int partials_fp32;
-  /* Test use only; 0 in normal calls.  Bit 0: the KV-outer kernel's scheduler warp
-   * publishes no work, so every other role's bounded wait (2 s) expires: the call then
+  /* Test use only; 0 in normal calls.  Bit 0 (bf16 inputs, bf16 partials, KV-outer
+   * path): a separate build of the KV-outer kernel whose scheduler warp publishes no
+   * work runs instead, so every other role's bounded wait (2 s) expires: the call then
    * leaves O undefined, sets the schedule's timeout bit (msa_schedule_query returns
    * MSA_ERR_TIMEOUT until the schedule is rebuilt) and the device stays usable.  It
    * exercises the timeout path without faulting anything. */
