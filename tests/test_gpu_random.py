@@ -1,0 +1,76 @@
+"""Randomised parity sweep: many small seeded shapes through every forward path and the
+backward, against the fp64 oracle.
+
+Each case draws N (1 .. 600, ragged), Lkv (a multiple of 128 with N <= Lkv), Hkv (1 .. 4),
+topK (1 .. 20), lists with pads, duplicates, future blocks and invalid-free ids, and a
+scale of either sign; the forward runs with AUTO, KV-outer forced and Q-outer forced (the
+three must agree with the oracle), and the backward runs over the same schedule.  Queries
+sit at the tail of the keys and the own block is always in the list.
+
+Tolerance: relative L2 <= 1e-2 over O and |dLSE| <= 1e-3 as everywhere; element-wise
+|dO| <= 2e-2 + 8e-3 |O| instead of a flat 2e-2, because short lists (topK = 1: only the
+causal part of the own block) give outputs as large as the V values themselves, where a
+bf16 output alone rounds by up to 1.6e-2 (|O| in [4, 8)) before the bf16 P and partial
+roundings; 8e-3 is about two bf16 roundings.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.util import BF16_MAX_ABS, BF16_REL_L2, BWD_REL_L2, LSE_MAX_ABS, compare_outputs, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    N = int(rng.integers(1, 601))
+    nb = int(rng.integers(max(1, -(-N // 128)), 24))
+    Lkv = 128 * nb
+    Hkv = int(rng.integers(1, 5))
+    topK = int(rng.integers(1, 21))
+    scale = float(rng.choice([1.0, -1.0]) * rng.uniform(0.02, 0.3))
+    mk = lambda shape: torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(torch.bfloat16)
+    Q, K, V, dO = mk((N, 16 * Hkv, 128)), mk((Lkv, Hkv, 128)), mk((Lkv, Hkv, 128)), mk((N, 16 * Hkv, 128))
+    idx = rng.integers(-1, nb, size=(N, Hkv, topK)).astype(np.int32)  # pads and future blocks
+    idx[:, :, 0] = ((Lkv - N + np.arange(N)) // 128)[:, None]
+    if topK > 2:
+        dup = rng.random((N, Hkv)) < 0.3
+        idx[:, :, 2] = np.where(dup, idx[:, :, 1], idx[:, :, 2])
+    return Q, K, V, dO, idx, Lkv, scale
+
+
+def bits(t):
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_case(seed):
+    import block_sparse_gqa_gb300 as msa
+    Q, K, V, dO, idx, Lkv, scale = case(seed)
+    dev = torch.device("cuda")
+    Qd, Kd, Vd, dOd = (t.to(dev) for t in (Q, K, V, dO))
+    s = msa.build_schedule(torch.from_numpy(idx).to(dev), Lkv // 128)
+    Or, Lr, _ = oracle.attn_fwd(bits(Q), bits(K), bits(V), idx, Lkv=Lkv, scale=scale)
+    outs = {}
+    for path in ("auto", "kv_outer", "q_outer"):
+        O, LSE = msa.sparse_attn_fwd(Qd, Kd, Vd, s, scale=scale, path=path)
+        torch.cuda.synchronize()
+        outs[path] = (O, LSE)
+        Og = O.float().cpu().numpy()
+        rel, mabs, lerr = compare_outputs(Og, LSE.cpu().numpy(), Or, Lr)
+        excess = float((np.abs(Og - Or) - (BF16_MAX_ABS + 8e-3 * np.abs(Or))).max())
+        assert rel <= BF16_REL_L2 and excess <= 0 and lerr <= LSE_MAX_ABS, (path, rel, mabs, excess, lerr)
+    O, LSE = outs["kv_outer"]
+    dQ, dK, dV = msa.sparse_attn_bwd(Qd, Kd, Vd, O, dOd, LSE, s, scale=scale)
+    torch.cuda.synchronize()
+    assert s.query()["status"] == 0
+    s.close()
+    rQ, rK, rV, _ = oracle.attn_bwd(bits(Q), bits(K), bits(V), bits(dO), idx, Lkv=Lkv, scale=scale)
+    for got, ref in ((dQ, rQ), (dK, rK), (dV, rV)):
+        g = got.float().cpu().numpy()
+        if np.abs(ref).max() == 0:
+            assert np.all(g == 0)
+        else:
+            assert rel_l2(g, ref) <= BWD_REL_L2
