@@ -19,8 +19,11 @@
 // One CTA of 256 threads per (i, g) unit at a time: thread (h, c) owns head h and
 // output columns [8c, 8c + 8); a warp reads 512 contiguous bytes of each partial.  The
 // statistics and partial loads of 8 slots are issued together once the combine map is
-// known; 64 registers per thread keep 4 CTAs (32 warps) resident per SM so that enough
-// loads are in flight to cover HBM latency.
+// known; the first 8 map entries of a CTA's next unit are loaded while it merges the
+// current one, so a unit of up to 8 slots costs one round trip.  Partials and statistics
+// are read once: streaming loads (evict-first).  64 registers per thread keep 4 CTAs (32
+// warps) resident per SM so that enough loads are in flight to cover HBM latency; the
+// grid is 32 CTAs per SM (8 waves), which shortens the tail of the last wave.
 #include <cuda_bf16.h>
 
 #include "msa_internal.h"
@@ -73,25 +76,39 @@ combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ parti
   if (path != kPathKvOuter) return;
   const int h = threadIdx.x >> 4, c = threadIdx.x & 15;
   const int64_t units = static_cast<int64_t>(N) * Hkv;
+  int pre[kKChunk];  // the first map entries of this CTA's next unit
+  {
+    const int64_t u0 = blockIdx.x;
+#pragma unroll
+    for (int k = 0; k < kKChunk; ++k) pre[k] = (u0 < units && k < topK) ? __ldg(cmap + u0 * topK + k) : -1;
+  }
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const int32_t* cm = cmap + u * topK;
+    int first[kKChunk];
+#pragma unroll
+    for (int k = 0; k < kKChunk; ++k) first[k] = pre[k];
+    {
+      const int64_t un = u + gridDim.x;
+#pragma unroll
+      for (int k = 0; k < kKChunk; ++k) pre[k] = (un < units && k < topK) ? __ldg(cmap + un * topK + k) : -1;
+    }
     float M = -INFINITY, L = 0.f;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int k0 = 0; k0 < topK; k0 += kKChunk) {
       int pos[kKChunk];
 #pragma unroll
-      for (int k = 0; k < kKChunk; ++k) pos[k] = (k0 + k < topK) ? __ldg(cm + k0 + k) : -1;
+      for (int k = 0; k < kKChunk; ++k) pos[k] = k0 == 0 ? first[k] : (k0 + k < topK) ? __ldg(cm + k0 + k) : -1;
       float2 st[kKChunk];
       Part8<kF32> v[kKChunk];
 #pragma unroll
       for (int k = 0; k < kKChunk; ++k) {
         const int64_t r = static_cast<int64_t>(pos[k]) * kGroup + h;
-        st[k] = pos[k] >= 0 ? __ldg(pstat + r) : make_float2(-INFINITY, 0.f);
+        st[k] = pos[k] >= 0 ? __ldcs(pstat + r) : make_float2(-INFINITY, 0.f);
         if constexpr (kF32) {
-          v[k].a = pos[k] >= 0 ? __ldg(partial + r * 32 + 2 * c) : make_uint4(0, 0, 0, 0);
-          v[k].b = pos[k] >= 0 ? __ldg(partial + r * 32 + 2 * c + 1) : make_uint4(0, 0, 0, 0);
+          v[k].a = pos[k] >= 0 ? __ldcs(partial + r * 32 + 2 * c) : make_uint4(0, 0, 0, 0);
+          v[k].b = pos[k] >= 0 ? __ldcs(partial + r * 32 + 2 * c + 1) : make_uint4(0, 0, 0, 0);
         } else {
-          v[k].a = pos[k] >= 0 ? __ldg(partial + r * 16 + c) : make_uint4(0, 0, 0, 0);
+          v[k].a = pos[k] >= 0 ? __ldcs(partial + r * 16 + c) : make_uint4(0, 0, 0, 0);
         }
       }
       float Mc = M;
@@ -138,7 +155,7 @@ cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, f
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t units = static_cast<int64_t>(s->N) * s->Hkv;
-  int64_t grid = sms * 16;
+  int64_t grid = sms * 32;
   if (grid > units) grid = units;
   if (f32p)
     combine_kernel<true><<<static_cast<int>(grid), kThreads, 0, st>>>(
