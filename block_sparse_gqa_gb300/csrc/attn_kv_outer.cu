@@ -815,7 +815,11 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   // the chunk counter this launch claims its work from starts at zero
   cudaError_t e = cudaMemsetAsync(&s->d.hdr->pad[0], 0, sizeof(int32_t), st);
   if (e != cudaSuccess) return e;
-  kern<<<a.num_ctas, kThreads, smem, st>>>(tmK, tmV, tmP128, tmP16, p);
+  // no more CTAs than work-list chunks can exist (decode sizes: a few; also makes the
+  // launch cheap where the device picks the Q-outer path and this kernel exits at once)
+  const int64_t max_chunks = (s->cap_tiles + kChunkTiles - 1) / kChunkTiles;
+  const int grid = max_chunks < a.num_ctas ? static_cast<int>(max_chunks) : a.num_ctas;
+  kern<<<grid, kThreads, smem, st>>>(tmK, tmV, tmP128, tmP16, p);
   return cudaGetLastError();
 }
 

@@ -27,6 +27,14 @@
 //                memory), P^T (bf16) into shared memory in the MMA's B layout, and the
 //                running output o[h] (its column d) rescaled by 2^(m_old - m_new)
 // The causal limit only matters in the query's own block (keys > pos(i) get p = 0).
+//
+// Few units (decode-size N): each unit's list is split into S contiguous chunks of its
+// valid blocks, and a work item is (unit, chunk), so that up to S times more SMs work.
+// An item ends with its unnormalised output o (fp32 [16 heads][128]) and (m, l) per
+// head in a workspace; the warpgroup that finishes a unit's last item (a counter per
+// unit, incremented after a GPU-scope fence) merges the S partials in chunk order:
+// O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, LSE = ln 2 (M + log2 of the
+// denominator).  The merge order is fixed, so results do not depend on timing.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -62,7 +70,17 @@ struct QoParams {
   int N, Lkv, Hq, Hkv, topK, nblocks;
   float sl2;  // scale * log2(e)
   int force_path;
+  int splits;       // chunks per unit (1: no splitting)
+  float* qs_o;      // [items][16][128] partial outputs (splits > 1)
+  float2* qs_ml;    // [items][16] (m, l)
+  int32_t* qs_cnt;  // [units] finished chunks, zero at launch
 };
+
+// Chunk sp of the unit's nb valid blocks (list order): [lo, hi)
+__device__ __forceinline__ void chunk_range(int nb, int sp, int S, int& lo, int& hi) {
+  lo = nb * sp / S;
+  hi = nb * (sp + 1) / S;
+}
 
 __device__ __forceinline__ void flag_timeout(SchedHeader* hdr) { atomicOr(&hdr->status, kStatusTimeout); }
 
@@ -131,6 +149,9 @@ __device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
   return op(d, __shfl_xor_sync(0xffffffffu, d, 1));
 }
 
+// kSplit: the instance for split units (p.splits > 1); the other one is the plain
+// per-unit kernel (p.splits is 1 there and never read)
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const QoParams p) {
@@ -149,6 +170,8 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t units = static_cast<int64_t>(p.N) * p.Hkv;
+  const int S = kSplit ? p.splits : 1;
+  const int64_t nitems = units * S;
 
   if (tid == 0) {
     for (int s = 0; s < kSlots; ++s) {
@@ -180,10 +203,13 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const uint64_t pol = policy_evict_normal();
     bool ok = true;
     int item = 0, nu = 0;
-    for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    for (int64_t x = blockIdx.x; x < nitems && ok; x += gridDim.x) {
+      const int64_t u = kSplit ? x / S : x;
       UnitIds mine;
       const int nb = unit_blocks(p, u, lane, mine);
-      if (nb == 0) continue;
+      int k_lo = 0, k_hi = nb;
+      if constexpr (kSplit) chunk_range(nb, static_cast<int>(x % S), S, k_lo, k_hi);
+      if (k_hi == k_lo) continue;
       const int i = static_cast<int>(u / p.Hkv), g = static_cast<int>(u % p.Hkv);
       const int qb = nu & 1;
       if (lane == 0) {
@@ -197,7 +223,7 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      for (int k = 0; k < nb && ok; ++k, ++item) {
+      for (int k = k_lo; k < k_hi && ok; ++k, ++item) {
         const int b = block_at(mine, k);
         if (lane == 0) {
           // one box per tensor: the whole 128 x 128 block, both halves of each 256-byte row
@@ -242,14 +268,17 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       mma_commit(bar(B_EMPTY0 + vs));
       return true;
     };
-    for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    for (int64_t x = blockIdx.x; x < nitems && ok; x += gridDim.x) {
+      const int64_t u = kSplit ? x / S : x;
       UnitIds mine;
       const int nb = unit_blocks(p, u, lane, mine);
-      if (nb == 0) continue;
+      int k_lo = 0, k_hi = nb;
+      if constexpr (kSplit) chunk_range(nb, static_cast<int>(x % S), S, k_lo, k_hi);
+      if (k_hi == k_lo) continue;
       const int qb = nu & 1;
       if (lane == 0) {
         ok = mbar_wait(bar(B_QFULL0 + qb), (nu >> 1) & 1);
-        for (int k = 0; k < nb && ok; ++k, ++item) {
+        for (int k = k_lo; k < k_hi && ok; ++k, ++item) {
           const int kn = 2 * item, ks = kn % kSlots, s = item & 1;
           if (!(ok = mbar_wait(bar(B_FULL0 + ks), (kn / kSlots) & 1))) break;
           // S[s] is reused: the softmax warps must have read S of item - 2
@@ -262,7 +291,7 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                        smem_desc(qa + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024, 2), idesc_s, kk > 0);
           mma_commit(bar(B_SFULL0 + s));
           mma_commit(bar(B_EMPTY0 + ks));
-          if (k == nb - 1) mma_commit(bar(B_QEMPTY0 + qb));
+          if (k == k_hi - 1) mma_commit(bar(B_QEMPTY0 + qb));
           if (pending >= 0 && !(ok = issue_pv(pending))) break;
           pending = item;
         }
@@ -281,18 +310,91 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const float kLn2 = 0.6931471805599453f;
     bool ok = true;
     int item = 0;
-    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + kOffCtl + 192);
+    float* mscr = reinterpret_cast<float*>(smem + kOffP);  // merge scratch (P is free then)
+    // split item x of unit u done: store its partial; the last of the unit's chunks merges
+    auto finish_split = [&](int64_t x, int64_t u, __nv_bfloat16* Orow, float* lse_out, const float (&m)[kGroup],
+                            const float (&l)[kGroup], const float (&o)[kGroup]) {
+      float* po = p.qs_o + x * (kGroup * kHeadDim);
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) po[h * kHeadDim + key] = o[h];
+      if (key < kGroup) {
+        float mk = m[0], lk = l[0];
+#pragma unroll
+        for (int h = 1; h < kGroup; ++h)
+          if (key == h) { mk = m[h]; lk = l[h]; }
+        p.qs_ml[x * kGroup + key] = make_float2(mk, lk);
+      }
+      // every thread's stores come before the counting thread's fence (grid-barrier pattern)
+      named_bar_sync(bar_id, 128);
+      if (tid == 64) {
+        __threadfence();
+        *last_flag = atomicAdd(p.qs_cnt + u, 1) == S - 1;
+      }
+      named_bar_sync(bar_id, 128);
+      if (!*last_flag) return;
+      __threadfence();
+      const int64_t x0 = u * S;
+      // (m, l) of every (chunk, head) -> weights 2^(m - M) per chunk and the denominator
+      float* mm = mscr;            // [chunk][head]
+      float* ll = mscr + 128;      // [chunk][head]
+      float* ww = mscr + 256;      // [chunk][head]
+      float* LL = mscr + 384;      // [head]
+      float* MM = mscr + 400;      // [head]
+      if (key < S * kGroup) {
+        const float2 v = __ldcg(p.qs_ml + x0 * kGroup + key);
+        mm[key] = v.x;
+        ll[key] = v.y;
+      }
+      named_bar_sync(bar_id, 128);
+      if (key < kGroup) {
+        float M = -INFINITY;
+        for (int sp = 0; sp < S; ++sp) M = fmaxf(M, mm[sp * kGroup + key]);
+        float L = 0.f;
+        for (int sp = 0; sp < S; ++sp) {
+          const float mv = mm[sp * kGroup + key];
+          const float w = mv == -INFINITY ? 0.f : ex2(mv - M);
+          ww[sp * kGroup + key] = w;
+          L = fmaf(w, ll[sp * kGroup + key], L);
+        }
+        LL[key] = L;
+        MM[key] = M;
+      }
+      named_bar_sync(bar_id, 128);
+      const float* po0 = p.qs_o + x0 * (kGroup * kHeadDim) + key;
+#pragma unroll
+      for (int h0 = 0; h0 < kGroup; h0 += 4) {
+        float v[4][kQSplitMax];
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+#pragma unroll
+          for (int sp = 0; sp < kQSplitMax; ++sp)
+            v[hh][sp] = sp < S ? __ldcg(po0 + (static_cast<int64_t>(sp) * kGroup + h0 + hh) * kHeadDim) : 0.f;
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+          const int h = h0 + hh;
+          float acc = 0.f;
+#pragma unroll
+          for (int sp = 0; sp < kQSplitMax; ++sp)
+            if (sp < S) acc = fmaf(ww[sp * kGroup + h], v[hh][sp], acc);
+          const float L = LL[h];
+          Orow[h * kHeadDim + key] = __float2bfloat16(L > 0.f ? acc / L : 0.f);
+        }
+      }
+      if (lse_out && key < kGroup) {
+        const float L = LL[key];
+        lse_out[key] = L > 0.f ? (MM[key] + lg2(L)) * kLn2 : -INFINITY;
+      }
+    };
+    for (int64_t x = blockIdx.x; x < nitems; x += gridDim.x) {
+      const int64_t u = kSplit ? x / S : x;
       UnitIds mine;
       const int nb = unit_blocks(p, u, lane, mine);
+      int k_lo = 0, k_hi = nb;
+      if constexpr (kSplit) chunk_range(nb, static_cast<int>(x % S), S, k_lo, k_hi);
       const int i = static_cast<int>(u / p.Hkv), g = static_cast<int>(u % p.Hkv);
       __nv_bfloat16* Orow = p.O + (static_cast<int64_t>(i) * p.Hq + g * kGroup) * kHeadDim;
-      if (nb == 0) {
-#pragma unroll
-        for (int h = 0; h < kGroup; ++h) Orow[h * kHeadDim + key] = __float2bfloat16(0.f);
-        if (p.LSE && key < kGroup) p.LSE[static_cast<int64_t>(i) * p.Hq + g * kGroup + key] = -INFINITY;
-        continue;
-      }
-      const int pos = p.Lkv - p.N + i;
+      float* lse_out = p.LSE ? p.LSE + static_cast<int64_t>(i) * p.Hq + g * kGroup : nullptr;
       float m[kGroup], l[kGroup], o[kGroup], aprev[kGroup];
 #pragma unroll
       for (int h = 0; h < kGroup; ++h) {
@@ -301,7 +403,19 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         o[h] = 0.f;
         aprev[h] = 0.f;
       }
-      for (int k = 0; k < nb; ++k, ++item) {
+      if (k_hi == k_lo) {
+        if constexpr (kSplit) {
+          finish_split(x, u, Orow, lse_out, m, l, o);
+          named_bar_sync(bar_id, 128);  // the merge scratch and the flag are read before reuse
+        } else {
+#pragma unroll
+          for (int h = 0; h < kGroup; ++h) Orow[h * kHeadDim + key] = __float2bfloat16(0.f);
+          if (lse_out && key < kGroup) lse_out[key] = -INFINITY;
+        }
+        continue;
+      }
+      const int pos = p.Lkv - p.N + i;
+      for (int k = k_lo; k < k_hi; ++k, ++item) {
         const int b = block_at(mine, k);
         const int s = item & 1;
         ok = mbar_wait(bar(B_SFULL0 + s), (item >> 1) & 1);
@@ -336,7 +450,7 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         if (!(lane & 1)) rs[(lane >> 1) * 4 + q4] = sm;
         // the previous block's P V: accumulate it (relative to the previous maximum), then
         // the P buffer is free for this block
-        if (k > 0) {
+        if (k > k_lo) {
           ok = mbar_wait(bar(B_PVDONE), (item - 1) & 1);
           if (!named_bar_and(bar_id, 128, ok)) { ok = false; break; }
           tc_fence_after();
@@ -379,18 +493,22 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       tmem_ld_wait();
       tc_fence_before();
 #pragma unroll
-      for (int h = 0; h < kGroup; ++h) {
-        o[h] = fmaf(o[h], aprev[h], __uint_as_float(ov[h]));
-        Orow[h * kHeadDim + key] = __float2bfloat16(o[h] / l[h]);
-      }
-      if (p.LSE && key < kGroup) {
-        float mk = m[0], lk = l[0];
+      for (int h = 0; h < kGroup; ++h) o[h] = fmaf(o[h], aprev[h], __uint_as_float(ov[h]));
+      if constexpr (kSplit) {
+        finish_split(x, u, Orow, lse_out, m, l, o);
+      } else {
 #pragma unroll
-        for (int h = 1; h < kGroup; ++h)
-          if (key == h) { mk = m[h]; lk = l[h]; }
-        p.LSE[static_cast<int64_t>(i) * p.Hq + g * kGroup + key] = (mk + lg2(lk)) * kLn2;
+        for (int h = 0; h < kGroup; ++h) Orow[h * kHeadDim + key] = __float2bfloat16(o[h] / l[h]);
+        if (lse_out && key < kGroup) {
+          float mk = m[0], lk = l[0];
+#pragma unroll
+          for (int h = 1; h < kGroup; ++h)
+            if (key == h) { mk = m[h]; lk = l[h]; }
+          lse_out[key] = (mk + lg2(lk)) * kLn2;
+        }
       }
-      // all 128 threads are past this unit's reads of `red` before the next unit writes it
+      // all 128 threads are past this item's reads of `red` (and of the merge scratch and
+      // flag) before the next item writes them
       named_bar_sync(bar_id, 128);
     }
     if (!ok && tid == 64) flag_timeout(p.hdr_w);
@@ -434,7 +552,9 @@ cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, 
   }
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(q_outer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(q_outer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(q_outer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -453,9 +573,31 @@ cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, 
   p.sl2 = scale * 1.4426950408889634f;
   p.force_path = force_path;
   const int64_t units = static_cast<int64_t>(s->N) * s->Hkv;
+  // split the units' lists while the units fill at most a quarter of the SMs: the
+  // merge and the counter reset cost a few microseconds, which 2 or 3 chunks per unit do
+  // not win back (measured: N = 16, 64 units, 2 chunks was slower than 1)
+  int splits = 1;
+  if (s->qs_items > 0 && units * kQSplitMin <= sms) {
+    splits = static_cast<int>(sms / units);
+    if (splits > kQSplitMax) splits = kQSplitMax;
+    if (splits > s->topK) splits = s->topK;
+    if (static_cast<int64_t>(splits) * units > s->qs_items) splits = static_cast<int>(s->qs_items / units);
+    if (splits < kQSplitMin) splits = 1;
+  }
+  p.splits = splits;
+  p.qs_o = s->d.qs_o;
+  p.qs_ml = s->d.qs_ml;
+  p.qs_cnt = s->d.qs_cnt;
+  if (splits > 1) {
+    cudaError_t e = cudaMemsetAsync(s->d.qs_cnt, 0, static_cast<size_t>(units) * sizeof(int32_t), st);
+    if (e != cudaSuccess) return e;
+  }
   int64_t grid = sms;
-  if (grid > units) grid = units;
-  q_outer_kernel<<<static_cast<int>(grid), kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, p);
+  if (grid > units * splits) grid = units * splits;
+  if (splits > 1)
+    q_outer_kernel<true><<<static_cast<int>(grid), kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, p);
+  else
+    q_outer_kernel<false><<<static_cast<int>(grid), kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }
 

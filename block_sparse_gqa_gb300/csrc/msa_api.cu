@@ -111,6 +111,9 @@ void carve_schedule(msa_schedule* s, char* base) {
   d.window_tiles = c.take<int32_t>(static_cast<size_t>(s->nW) + 1);
   d.segoff = c.take<int32_t>(static_cast<size_t>(s->nseg) + 1);
   d.seg_sums = c.take<int32_t>(static_cast<size_t>(s->nseg_blocks) + 1);
+  d.qs_o = c.take<float>(static_cast<size_t>(s->qs_items) * kGroup * kHeadDim);
+  d.qs_ml = c.take<float2>(static_cast<size_t>(s->qs_items) * kGroup);
+  d.qs_cnt = c.take<int32_t>(s->qs_items > 0 ? static_cast<size_t>(s->N) * s->Hkv : 0);
   d.hdr = c.take<msa::SchedHeader>(1);
   s->dev_bytes = c.off;
 }
@@ -129,6 +132,8 @@ void schedule_dims(msa_schedule* s, int N, int Hkv, int topK, int nblocks) {
   s->nseg_blocks = (s->nseg + kSegScanBlock - 1) / kSegScanBlock;
   const int64_t nonempty = s->nseg < s->cap_entries ? s->nseg : s->cap_entries;
   s->cap_tiles = s->cap_entries / kTileQ + nonempty + 1;
+  const int64_t units = static_cast<int64_t>(N) * Hkv;
+  s->qs_items = units <= kQSplitMaxUnits ? static_cast<int>(units * kQSplitMax) : 0;
 }
 
 msa_status_t status_from_cuda(cudaError_t e) { return from_cuda(e); }

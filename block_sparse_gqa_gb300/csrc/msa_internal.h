@@ -15,6 +15,12 @@ constexpr int kTileQ = 8;        // queries per tile: 8 queries x 16 heads = 128
 constexpr int kChunk = 32;       // queries per bitmask word of the schedule
 constexpr int kWindow = 256;     // queries per work-list window (multiple of kChunk)
 
+// Q-outer split units: at most this many splits per unit, and only while the units
+// number at most kQSplitMaxUnits (more units fill the GPU without splitting)
+constexpr int kQSplitMax = 8;
+constexpr int kQSplitMin = 4;
+constexpr int kQSplitMaxUnits = 64;
+
 constexpr int kPathKvOuter = 1;
 constexpr int kPathQOuter = 2;
 
@@ -45,6 +51,11 @@ struct SchedDev {
   int32_t* window_tiles; // [nW + 1]
   int32_t* segoff;       // [nW * R + 1] tiles per (window, row) segment, then their exclusive prefix
   int32_t* seg_sums;     // [nseg_blocks + 1] scan scratch: per-block sums of segment tile counts
+  // Q-outer split units (few units): per work item the fp32 partial output [16][128] and
+  // (m, l) per head; per unit the count of finished splits
+  float* qs_o;           // [qs_items * 16 * 128]
+  float2* qs_ml;         // [qs_items * 16]
+  int32_t* qs_cnt;       // [N * Hkv] when qs_items > 0
   SchedHeader* hdr;
 };
 
@@ -53,6 +64,7 @@ struct SchedDev {
 struct msa_schedule {
   int N, Hkv, topK, nblocks;
   int R, C, nW;
+  int qs_items;  // capacity of the Q-outer split workspace in work items (0: no splitting)
   int64_t cap_entries, cap_tiles, nseg, nseg_blocks;
   void* dev_base;
   size_t dev_bytes;

@@ -23,6 +23,9 @@
 //                     more segments: scan_rows + seg_reduce / seg_top / seg_down
 //   entries<scatter>  qlist, slot, cmap, blist
 //   tiles             the work list, window-major, 8-entry tiles
+// Tiny inputs (decode sizes) take one CTA instead: schedule_one runs the same phases
+// with CTA barriers in between and writes the same arrays, in one launch instead of two
+// memsets and five kernels.
 #include "msa_internal.h"
 #include "ptx.cuh"
 
@@ -187,11 +190,9 @@ __global__ void __launch_bounds__(NT) k_scan_rows(const int32_t* __restrict__ co
 constexpr int kSmallSegPer = 32;
 
 template <int NT>
-__global__ void __launch_bounds__(NT) k_scan_small(const int32_t* __restrict__ counts, int R, int N,
-                                                   int32_t* __restrict__ offsets, int32_t* __restrict__ seg,
-                                                   int nseg, int32_t* __restrict__ window_tiles, int nW,
-                                                   SchedHeader* hdr) {
-  __shared__ int warp_buf[32];
+__device__ void scan_small_body(const int32_t* __restrict__ counts, int R, int N, int32_t* __restrict__ offsets,
+                                int32_t* __restrict__ seg, int nseg, int32_t* __restrict__ window_tiles, int nW,
+                                SchedHeader* hdr, int* warp_buf) {
   {
     const int per = (R + NT - 1) / NT;
     const int r0 = min(static_cast<int>(threadIdx.x) * per, R), r1 = min(r0 + per, R);
@@ -231,6 +232,15 @@ __global__ void __launch_bounds__(NT) k_scan_small(const int32_t* __restrict__ c
     window_tiles[nW] = total;
     hdr->ntiles = total;
   }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) k_scan_small(const int32_t* __restrict__ counts, int R, int N,
+                                                   int32_t* __restrict__ offsets, int32_t* __restrict__ seg,
+                                                   int nseg, int32_t* __restrict__ window_tiles, int nW,
+                                                   SchedHeader* hdr) {
+  __shared__ int warp_buf[32];
+  scan_small_body<NT>(counts, R, N, offsets, seg, nseg, window_tiles, nW, hdr, warp_buf);
 }
 
 template <int NT>
@@ -316,6 +326,109 @@ __global__ void k_tiles(const int32_t* __restrict__ segoff, int64_t nseg, int R,
   }
 }
 
+// The whole schedule in one CTA (small inputs).  Phases, separated by CTA barriers:
+// zero the bitmask and the header; mark (entries<mark>); per row the popcount prefix,
+// the count and the segment tile counts (rowscan); the scans (scan_small); scatter
+// (entries<scatter>); tiles.  An entry is what entries<> calls one (valid id, not in
+// the future, first occurrence in its list), so every array equals the multi-kernel
+// schedule's.  The bitmask, built with atomics, is read back through L2.
+constexpr int kOneThreads = 1024;
+
+__device__ __forceinline__ bool slot_entry(const int32_t* __restrict__ lst, int k, int b, int lb, int nblocks,
+                                           bool& bad) {
+  if (b < -1 || b >= nblocks) {
+    bad = true;
+    return false;
+  }
+  if (b < 0 || b > lb) return false;
+  for (int k2 = 0; k2 < k; ++k2)
+    if (lst[k2] == b) return false;
+  return true;
+}
+
+__global__ void __launch_bounds__(kOneThreads, 1)
+k_schedule_one(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int R, int C, int nW,
+               SchedDev d) {
+  __shared__ int warp_buf[32];
+  __shared__ int s_bad;
+  constexpr int kCpw = kWindow / kChunk;
+  const int t = threadIdx.x;
+  const int64_t nmask = static_cast<int64_t>(R) * C;
+  for (int64_t q = t; q < nmask; q += kOneThreads) d.mask[q] = 0u;
+  if (t < static_cast<int>(sizeof(SchedHeader) / sizeof(int32_t))) reinterpret_cast<int32_t*>(d.hdr)[t] = 0;
+  if (t == 0) s_bad = 0;
+  __syncthreads();
+  const int64_t nslot = static_cast<int64_t>(N) * Hkv * topK;
+  bool bad = false;
+  for (int64_t e = t; e < nslot; e += kOneThreads) {
+    const int64_t L = e / topK;
+    const int k = static_cast<int>(e - L * topK);
+    const int i = static_cast<int>(L / Hkv), g = static_cast<int>(L % Hkv);
+    const int b = idx[e];
+    const int lb = (Lkv - N + i) / kBlock;
+    if (slot_entry(idx + L * topK, k, b, lb, nblocks, bad))
+      atomicOr(&d.mask[(static_cast<size_t>(g) * nblocks + b) * C + (i >> 5)], 1u << (i & 31));
+  }
+  if (bad) s_bad = 1;
+  __syncthreads();
+  for (int r = t; r < R; r += kOneThreads) {
+    const uint32_t* m = d.mask + static_cast<size_t>(r) * C;
+    int32_t* rb = d.rowbase + static_cast<size_t>(r) * (C + 1);
+    int run = 0;
+    for (int c = 0; c < C; ++c) {
+      rb[c] = run;
+      run += __popc(__ldcg(m + c));
+    }
+    rb[C] = run;
+    d.counts[r] = run;
+    for (int w = 0; w < nW; ++w) {
+      const int cw0 = w * kCpw, cw1 = min(cw0 + kCpw, C);
+      const int cnt = rb[cw1] - rb[cw0];
+      d.segoff[static_cast<size_t>(w) * R + r] = (cnt + kTileQ - 1) / kTileQ;
+    }
+  }
+  __syncthreads();
+  const int nseg = nW * R;
+  scan_small_body<kOneThreads>(d.counts, R, N, d.offsets, d.segoff, nseg, d.window_tiles, nW, d.hdr, warp_buf);
+  __syncthreads();
+  for (int64_t e = t; e < nslot; e += kOneThreads) {
+    const int64_t L = e / topK;
+    const int k = static_cast<int>(e - L * topK);
+    const int i = static_cast<int>(L / Hkv), g = static_cast<int>(L % Hkv);
+    const int b = idx[e];
+    const int lb = (Lkv - N + i) / kBlock;
+    bool unused = false;
+    int p = -1;
+    const bool entry = slot_entry(idx + L * topK, k, b, lb, nblocks, unused);
+    if (entry) {
+      const size_t r = static_cast<size_t>(g) * nblocks + b;
+      const uint32_t word = __ldcg(d.mask + r * C + (i >> 5));
+      p = d.offsets[r] + d.rowbase[r * (C + 1) + (i >> 5)] + __popc(word & ((1u << (i & 31)) - 1u));
+      d.qlist[p] = i;
+      d.slot[p] = k;
+    }
+    d.cmap[e] = p;
+    d.blist[e] = entry ? b : -1;
+  }
+  for (int q = t; q < nseg; q += kOneThreads) {
+    const int t0 = d.segoff[q], n = d.segoff[q + 1] - t0;
+    if (n == 0) continue;
+    const int w = q / R, r = q % R;
+    const int cw0 = w * kCpw, cw1 = min(cw0 + kCpw, C);
+    const int32_t* rb = d.rowbase + static_cast<size_t>(r) * (C + 1);
+    const int first = d.offsets[r] + rb[cw0];
+    const int cnt = rb[cw1] - rb[cw0];
+    for (int j = 0; j < n; ++j) d.tiles[t0 + j] = make_int4(r, first + kTileQ * j, min(kTileQ, cnt - kTileQ * j), w);
+  }
+  if (t == 0 && s_bad) atomicOr(&d.hdr->status, kStatusBadIndex);
+}
+
+// One CTA is latency-bound (its loops run serially per thread): it wins only while the
+// lists and the rows are few.  Measured on GB300, graph-replayed decode steps: N = 1 and
+// 16 (64 and 1024 slots, 4096 rows) 49.6 -> 43.0 and 56 -> 52 us; at 4096 slots it was
+// 21 us slower than the multi-kernel path, at 16384 slots 130 us slower.
+constexpr int64_t kOneMaxSlots = 1024, kOneMaxMaskWords = 8192, kOneMaxSegments = 8192;
+
 int grid_for(int64_t n, int threads, int cap) {
   int64_t g = (n + threads - 1) / threads;
   if (g < 1) g = 1;
@@ -332,6 +445,12 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
   const int lists_per_cta = kEntThreads / s->topK;  // topK <= 64
   const int ent_grid = grid_for(nl, lists_per_cta, 1 << 20);
   cudaError_t e;
+  // tiny inputs: one CTA (limits keep its serial per-thread loops short)
+  if (nl * s->topK <= kOneMaxSlots && static_cast<int64_t>(s->R) * s->C <= kOneMaxMaskWords && s->C <= 64 &&
+      s->nseg <= kOneMaxSegments) {
+    k_schedule_one<<<1, kOneThreads, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->R, s->C, s->nW, d);
+    return cudaGetLastError();
+  }
   if ((e = cudaMemsetAsync(d.mask, 0, sizeof(uint32_t) * static_cast<size_t>(s->R) * s->C, st))) return e;
   if ((e = cudaMemsetAsync(d.hdr, 0, sizeof(SchedHeader), st))) return e;
   k_entries<false><<<ent_grid, kEntThreads, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C,

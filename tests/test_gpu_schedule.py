@@ -90,3 +90,23 @@ def test_schedule_deterministic_and_reusable():
     _, c = gpu_schedule(idx2, cfg.nblocks, schedule=s)
     assert_same(c, oracle.schedule(idx2, Lkv=cfg.Lkv), cfg.N, cfg.Lkv)
     s.close()
+
+
+@pytest.mark.parametrize("N,Lkv,Hkv,topK", [(1, 131072, 4, 16), (5, 2048, 1, 3), (31, 65536, 4, 8), (33, 8192, 2, 15),
+                                            (64, 4096, 1, 16), (64, 4096, 4, 4), (65, 4096, 4, 4), (16, 65536, 4, 17)])
+def test_schedule_small_inputs_match_oracle(N, Lkv, Hkv, topK):
+    """Tiny inputs (at most 1024 list slots and 8192 bitmask words) are scheduled by one
+    CTA; the shapes here sit on both sides of that limit, with pads, duplicates, future
+    blocks and one invalid id."""
+    rng = np.random.default_rng(N * 100 + topK)
+    nb = Lkv // 128
+    idx = rng.integers(-1, nb, size=(N, Hkv, topK)).astype(np.int32)
+    idx[:, :, 0] = ((Lkv - N + np.arange(N)) // 128)[:, None]
+    if topK > 2:
+        idx[::2, :, 2] = idx[::2, :, 1]
+    idx[0, 0, -1] = nb + 3  # invalid: ignored and flagged
+    ref = oracle.schedule(idx, Lkv=Lkv)
+    s, exp = gpu_schedule(idx, nb)
+    assert exp["status"] & 1 and ref["status"] == 1
+    assert_same(exp, ref, N, Lkv)
+    s.close()
