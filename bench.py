@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="m3", choices=["tiny", "m3", "long", "lowreuse", "fp8"])
+    ap.add_argument("--workload", default="m3", choices=["tiny", "m3", "long", "lowreuse", "fp8", "decode"])
     ap.add_argument("--lists", default="workload", choices=["workload", "r1", "r4"],
                     help="block lists: the workload's own, or chosen by the R1 / R4 selector (once, before timing)")
     ap.add_argument("--mode", default="general", choices=["general", "tiles", "bwd"],

@@ -312,6 +312,7 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     int item = 0;
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + kOffCtl + 192);
     float* mscr = reinterpret_cast<float*>(smem + kOffP);  // merge scratch (P is free then)
+    static_assert((3 * kQSplitMax + 2) * kGroup * 4 <= 4096, "merge scratch");
     // split item x of unit u done: store its partial; the last of the unit's chunks merges
     auto finish_split = [&](int64_t x, int64_t u, __nv_bfloat16* Orow, float* lse_out, const float (&m)[kGroup],
                             const float (&l)[kGroup], const float (&o)[kGroup]) {
@@ -336,15 +337,16 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       __threadfence();
       const int64_t x0 = u * S;
       // (m, l) of every (chunk, head) -> weights 2^(m - M) per chunk and the denominator
-      float* mm = mscr;            // [chunk][head]
-      float* ll = mscr + 128;      // [chunk][head]
-      float* ww = mscr + 256;      // [chunk][head]
-      float* LL = mscr + 384;      // [head]
-      float* MM = mscr + 400;      // [head]
-      if (key < S * kGroup) {
-        const float2 v = __ldcg(p.qs_ml + x0 * kGroup + key);
-        mm[key] = v.x;
-        ll[key] = v.y;
+      constexpr int kPairs = kQSplitMax * kGroup;
+      float* mm = mscr;                // [chunk][head]
+      float* ll = mscr + kPairs;       // [chunk][head]
+      float* ww = mscr + 2 * kPairs;   // [chunk][head]
+      float* LL = mscr + 3 * kPairs;   // [head]
+      float* MM = LL + kGroup;         // [head]
+      for (int q = key; q < S * kGroup; q += 128) {
+        const float2 v = __ldcg(p.qs_ml + x0 * kGroup + q);
+        mm[q] = v.x;
+        ll[q] = v.y;
       }
       named_bar_sync(bar_id, 128);
       if (key < kGroup) {

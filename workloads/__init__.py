@@ -78,6 +78,9 @@ CONFIGS = {
     "lowreuse": Config("lowreuse", 256, 524288, 64, 4, 128, 16, "uniform", 1003),
     "fp8": Config("fp8", 65536, 65536, 64, 4, 128, 16, "gauss", 1004, dtype="e4m3",
                   extra={"sigma": 32.0}),
+    # not one of the five configured workloads: one decode step (a single query at the tail
+    # of a 128K-token context) for the decode-size study
+    "decode": Config("decode", 1, 131072, 64, 4, 128, 16, "uniform", 1005),
 }
 
 
