@@ -23,7 +23,8 @@
 // current one, so a unit of up to 8 slots costs one round trip.  Partials and statistics
 // are read once: streaming loads (evict-first).  64 registers per thread keep 4 CTAs (32
 // warps) resident per SM so that enough loads are in flight to cover HBM latency; the
-// grid is 32 CTAs per SM (8 waves), which shortens the tail of the last wave.
+// grid is 64 CTAs per SM (16 waves), which shortens the tail of the last wave (16, 32,
+// 64, 128 per SM measured: 0.335, 0.332, 0.331, 0.333 ms at M3).
 #include <cuda_bf16.h>
 
 #include "msa_internal.h"
@@ -155,7 +156,7 @@ cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, f
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t units = static_cast<int64_t>(s->N) * s->Hkv;
-  int64_t grid = sms * 32;
+  int64_t grid = sms * 64;
   if (grid > units) grid = units;
   if (f32p)
     combine_kernel<true><<<static_cast<int>(grid), kThreads, 0, st>>>(
