@@ -39,13 +39,13 @@ def kernels_per_step(cfg):
     """Launches of libmsa kernels in one step: schedule (one kernel for tiny inputs: at
     most 1024 list slots, 8192 bitmask words and 8192 segments; else mark, rowscan, one
     fused scan or four scan kernels when there are more than 32768 (window, row)
-    segments, scatter, tiles) + kv_outer + combine + q_outer (the two attention kernels
-    not chosen exit at once)."""
+    segments, scatter + tiles in one launch) + kv_outer + combine + q_outer (the two
+    attention kernels not chosen exit at once)."""
     rows, words = cfg.Hkv * cfg.nblocks, -(-cfg.N // 32)
     nseg = -(-cfg.N // 256) * rows
     if cfg.N * cfg.Hkv * cfg.topK <= 1024 and rows * words <= 8192 and words <= 64 and nseg <= 8192:
         return 1 + 3
-    return (5 if nseg <= 32768 else 8) + 3
+    return (4 if nseg <= 32768 else 7) + 3
 
 
 def parse_args():

@@ -21,8 +21,8 @@
 //   scan_small        one CTA: offsets, E, nsb, the Q-outer / KV-outer decision and the
 //                     exclusive scan of the segment tile counts (at most 32768 segments);
 //                     more segments: scan_rows + seg_reduce / seg_top / seg_down
-//   entries<scatter>  qlist, slot, cmap, blist
-//   tiles             the work list, window-major, 8-entry tiles
+//   entries<scatter>  qlist, slot, cmap, blist  } one launch (scatter_tiles): the two only
+//   tiles             the work list, window-major, 8-entry tiles  } read what the scans wrote
 // Tiny inputs (decode sizes) take one CTA instead: schedule_one runs the same phases
 // with CTA barriers in between and writes the same arrays, in one launch instead of two
 // memsets and five kernels.
@@ -70,18 +70,20 @@ __device__ int block_exclusive_scan(int v, int* total, int* warp_buf) {
 //   and blist (b or -1).
 constexpr int kEntThreads = 256;
 
+// Body of entries<>: CTA bid of nbid (the scatter shares its launch with the tiles).
 template <bool kScatter>
-__global__ void __launch_bounds__(kEntThreads)
-k_entries(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int C, int lists_per_cta,
-          uint32_t* __restrict__ mask, const int32_t* __restrict__ rowbase, const int32_t* __restrict__ offsets,
-          int32_t* __restrict__ qlist, int32_t* __restrict__ slot, int32_t* __restrict__ cmap,
-          int32_t* __restrict__ blist, SchedHeader* hdr) {
+__device__ __forceinline__ void entries_body(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks,
+                                             int Lkv, int C, int lists_per_cta, uint32_t* __restrict__ mask,
+                                             const int32_t* __restrict__ rowbase, const int32_t* __restrict__ offsets,
+                                             int32_t* __restrict__ qlist, int32_t* __restrict__ slot,
+                                             int32_t* __restrict__ cmap, int32_t* __restrict__ blist, SchedHeader* hdr,
+                                             int bid, int nbid) {
   __shared__ int32_t s_idx[kEntThreads];
   const int64_t nl = static_cast<int64_t>(N) * Hkv;
   const int t = threadIdx.x;
   bool bad = false;
-  for (int64_t L0 = static_cast<int64_t>(blockIdx.x) * lists_per_cta; L0 < nl;
-       L0 += static_cast<int64_t>(gridDim.x) * lists_per_cta) {
+  for (int64_t L0 = static_cast<int64_t>(bid) * lists_per_cta; L0 < nl;
+       L0 += static_cast<int64_t>(nbid) * lists_per_cta) {
     const int64_t e0 = L0 * topK;
     const int nle = static_cast<int>(min(static_cast<int64_t>(lists_per_cta), nl - L0)) * topK;
     const int b = t < nle ? idx[e0 + t] : -1;
@@ -123,6 +125,13 @@ k_entries(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks
     __syncthreads();
   }
   if (!kScatter && bad) atomicOr(&hdr->status, kStatusBadIndex);
+}
+
+__global__ void __launch_bounds__(kEntThreads)
+k_mark(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int C, int lists_per_cta,
+       uint32_t* __restrict__ mask, SchedHeader* hdr) {
+  entries_body<false>(idx, N, Hkv, topK, nblocks, Lkv, C, lists_per_cta, mask, nullptr, nullptr, nullptr, nullptr,
+                      nullptr, nullptr, hdr, blockIdx.x, gridDim.x);
 }
 
 template <int NT>
@@ -308,12 +317,13 @@ __global__ void __launch_bounds__(NT) k_seg_down(int32_t* __restrict__ seg, int6
   }
 }
 
-__global__ void k_tiles(const int32_t* __restrict__ segoff, int64_t nseg, int R, int C,
-                        const int32_t* __restrict__ rowbase, const int32_t* __restrict__ offsets,
-                        int4* __restrict__ tiles) {
+// Work-list tiles of the segments, CTA bid of nbid (256 threads).
+__device__ __forceinline__ void tiles_body(const int32_t* __restrict__ segoff, int64_t nseg, int R, int C,
+                                           const int32_t* __restrict__ rowbase, const int32_t* __restrict__ offsets,
+                                           int4* __restrict__ tiles, int bid, int nbid) {
   constexpr int kCpw = kWindow / kChunk;
-  for (int64_t s = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; s < nseg;
-       s += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+  for (int64_t s = bid * static_cast<int64_t>(kEntThreads) + threadIdx.x; s < nseg;
+       s += static_cast<int64_t>(nbid) * kEntThreads) {
     const int t0 = segoff[s], n = segoff[s + 1] - t0;
     if (n == 0) continue;
     const int w = static_cast<int>(s / R), r = static_cast<int>(s % R);
@@ -324,6 +334,23 @@ __global__ void k_tiles(const int32_t* __restrict__ segoff, int64_t nseg, int R,
     for (int j = 0; j < n; ++j)
       tiles[t0 + j] = make_int4(r, first + kTileQ * j, min(kTileQ, cnt - kTileQ * j), w);
   }
+}
+
+// scatter (entries<true>) on CTAs [0, ent_grid), the work-list tiles on the rest: both
+// only read what the scans wrote, so one launch serves both
+__global__ void __launch_bounds__(kEntThreads)
+k_scatter_tiles(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int C,
+                int lists_per_cta, int ent_grid, const uint32_t* __restrict__ mask,
+                const int32_t* __restrict__ rowbase, const int32_t* __restrict__ offsets,
+                int32_t* __restrict__ qlist, int32_t* __restrict__ slot, int32_t* __restrict__ cmap,
+                int32_t* __restrict__ blist, const int32_t* __restrict__ segoff, int64_t nseg, int R,
+                int4* __restrict__ tiles, SchedHeader* hdr) {
+  const int b = blockIdx.x;
+  if (b < ent_grid)
+    entries_body<true>(idx, N, Hkv, topK, nblocks, Lkv, C, lists_per_cta, const_cast<uint32_t*>(mask), rowbase,
+                       offsets, qlist, slot, cmap, blist, hdr, b, ent_grid);
+  else
+    tiles_body(segoff, nseg, R, C, rowbase, offsets, tiles, b - ent_grid, static_cast<int>(gridDim.x) - ent_grid);
 }
 
 // The whole schedule in one CTA (small inputs).  Phases, separated by CTA barriers:
@@ -453,9 +480,8 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
   }
   if ((e = cudaMemsetAsync(d.mask, 0, sizeof(uint32_t) * static_cast<size_t>(s->R) * s->C, st))) return e;
   if ((e = cudaMemsetAsync(d.hdr, 0, sizeof(SchedHeader), st))) return e;
-  k_entries<false><<<ent_grid, kEntThreads, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C,
-                                                      lists_per_cta, d.mask, nullptr, nullptr, nullptr, nullptr,
-                                                      nullptr, nullptr, d.hdr);
+  k_mark<<<ent_grid, kEntThreads, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C, lists_per_cta,
+                                            d.mask, d.hdr);
   k_rowscan<256><<<grid_for(s->R, 1, 1 << 20), 256, 0, st>>>(d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
                                                              d.segoff);
   if (s->nseg <= 1024 * kSmallSegPer) {
@@ -468,11 +494,10 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
     k_seg_top<1024><<<1, 1024, 0, st>>>(d.seg_sums, nb, d.segoff, s->nseg, d.window_tiles, s->nW, d.hdr);
     k_seg_down<256><<<nb, 256, 0, st>>>(d.segoff, s->nseg, d.seg_sums, s->R, d.window_tiles);
   }
-  k_entries<true><<<ent_grid, kEntThreads, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C,
-                                                     lists_per_cta, d.mask, d.rowbase, d.offsets, d.qlist, d.slot,
-                                                     d.cmap, d.blist, d.hdr);
-  k_tiles<<<grid_for(s->nseg, 256, 1 << 16), 256, 0, st>>>(d.segoff, s->nseg, s->R, s->C, d.rowbase, d.offsets,
-                                                            d.tiles);
+  const int tiles_grid = grid_for(s->nseg, kEntThreads, 1 << 16);
+  k_scatter_tiles<<<ent_grid + tiles_grid, kEntThreads, 0, st>>>(
+      indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C, lists_per_cta, ent_grid, d.mask, d.rowbase, d.offsets,
+      d.qlist, d.slot, d.cmap, d.blist, d.segoff, s->nseg, s->R, d.tiles, d.hdr);
   return cudaGetLastError();
 }
 
