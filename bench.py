@@ -487,7 +487,9 @@ def run_ours(args, world, rank, local, pg):
     nominal = cfg.nominal_flops() * (2.5 if bwd else 1.0)  # the backward runs 5 products to the forward's 2
     value = world * nominal / (ms_per_step * 1e-3) / 1e12
 
-    # algorithmic bytes ("Roofline"): attention kernel and whole step
+    # algorithmic bytes: the KV-outer kernel reads Q once, each selected K/V block once, the
+    # lists and tiles, and writes every partial row and its (m, l) once; the whole step adds
+    # the combine (partials read, O and LSE written) and the schedule's list reads
     E, nsb, T = info["entries"], info["nsb"], info["ntiles"]
     G, D = cfg.G, cfg.D
     es = 1 if cfg.dtype == "e4m3" else 2  # bytes per input element
