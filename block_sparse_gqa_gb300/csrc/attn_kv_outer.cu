@@ -23,9 +23,9 @@
 //                tile info and query ids ahead of time and publishes each tile in a
 //                shared-memory ring for the other roles (it only waits for ring slots)
 //   warp 2       K/V loader: on a row change loads K_b into the next of two K
-//                buffers and V_b into the V buffer (TMA; E4M3: into the next of two V
-//                buffers, widened to f16 by the whole warp); a ring slot is reused only
-//                after both this warp and the output warps have released it
+//                buffers and V_b into the V buffer (TMA; E4M3: V as f16, into the next of
+//                two V buffers); a ring slot is reused only after both this warp and
+//                the output warps have released it
 //   warp 1       TMEM allocation (512 columns: S[0], S[1], O[0], O[1]) and issue of
 //                S[s] = Q K^T (tcgen05, smem x smem) for tile t into stage s = t % 2
 //   warp 3       issue of O[s] = P V with P read from TMEM (it overwrites S[s] in
@@ -54,10 +54,13 @@
 //
 // fp8 E4M3 inputs (per-tensor descales): S = Q K^T runs on kind::f8f6f4 (K-major, one
 // 128-byte swizzle span per row, 32 elements per MMA); q and k descales are folded
-// into the softmax scale.  P V runs in f16: the loader converts each V block from
-// E4M3 to f16 once (exact) into the layout the bf16 path loads by TMA, and P is
-// packed as f16 (more mantissa than bf16 for values in [0, 1]).  The v descale is
-// applied by the combine.
+// into the softmax scale.  P V runs in f16: the forward widens the whole E4M3 V tensor
+// to f16 once per call (exact, widen_e4m3_kernel below), the loader loads its blocks by
+// TMA as the bf16 path loads V, and P is packed as f16 (more mantissa than bf16 for
+// values in [0, 1]).  The v descale is applied by the combine.  (Widening each selected
+// block in shared memory with the loader warp instead cost 45% more kernel time on the
+// 65536-query E4M3 workload: one warp's conversion, once per row change, was on the
+// critical path.)
 #include <cfloat>
 
 #include <cuda_bf16.h>
@@ -90,11 +93,10 @@ struct Lay {
   static constexpr uint32_t kOffK0 = kQStages * kInTile;
   static constexpr uint32_t kOffK1 = kOffK0 + kInTile;
   // 16-bit V (bf16, or f16 widened from E4M3): one buffer for bf16 (shared memory is full),
-  // two for E4M3 so that the next row's V is widened while this row's P V runs
+  // two for E4M3 so that the next row's V loads while this row's P V runs
   static constexpr int kVBuf = kFp8 ? 2 : 1;
   static constexpr uint32_t kOffV = kOffK1 + kInTile;
-  static constexpr uint32_t kOffVst = kOffV + kVBuf * kTileBytes;  // E4M3 V as loaded (fp8 only)
-  static constexpr uint32_t kOffSt = kOffVst + (kFp8 ? 16384 : 0);  // output staging
+  static constexpr uint32_t kOffSt = kOffV + kVBuf * kTileBytes;  // output staging
   static constexpr uint32_t kOffCtl = kOffSt + kTileBytes;
   static constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + alignment slack
 };
@@ -102,7 +104,7 @@ static_assert(Lay<false>::kSmemBytes <= 232448 && Lay<true>::kSmemBytes <= 23244
 
 // barrier slots (8 bytes each) at the start of the control area
 enum {
-  B_QFULL0 = 0, B_KFULL0 = 3, B_KFREE0 = 5, B_VFULL0 = 7, B_VFREE0 = 9, B_VSTAGE = 11,
+  B_QFULL0 = 0, B_KFULL0 = 3, B_KFREE0 = 5, B_VFULL0 = 7, B_VFREE0 = 9,  // slot 11 unused
   B_SFULL0 = 12, B_PFULL0 = 14, B_PVDONE0 = 16, B_OFREE0 = 18, B_TFULL0 = 20, B_TEMPTY0 = 20 + kRing,
   B_COUNT = 20 + 2 * kRing
 };
@@ -282,7 +284,6 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       mbar_init(bar(B_VFULL0 + v), 1);
       mbar_init(bar(B_VFREE0 + v), 1);
     }
-    mbar_init(bar(B_VSTAGE), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_KFULL0 + s), 1);
       mbar_init(bar(B_KFREE0 + s), 1);
@@ -478,50 +479,19 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
             mbar_expect_tx(bar(B_KFULL0 + kb), L::kInTile);
             tma_load_3d(dk, &tmK, 0, g, b * kBlock, bar(B_KFULL0 + kb), pol_kv);
             if constexpr (!kFp8) tma_load_3d(dk + 16384, &tmK, 64, g, b * kBlock, bar(B_KFULL0 + kb), pol_kv);
-            if constexpr (kFp8) {
-              // E4M3 V lands in its own staging area at once; the V buffer is filled later
-              mbar_expect_tx(bar(B_VSTAGE), 16384);
-              tma_load_3d(sb + L::kOffVst, &tmV, 0, g, b * kBlock, bar(B_VSTAGE), pol_kv);
-            }
             // V buffer vb: free once the last P V of the row that used it before is done
             ok = mbar_wait(bar(B_VFREE0 + vb), (vuse & 1) ^ 1);
-            if constexpr (kFp8) {
-              const bool staged = mbar_wait(bar(B_VSTAGE), nk & 1);  // also on failure: no copy left in flight
-              ok = ok && staged;
-            }
           }
           if (ok) {
-            if constexpr (!kFp8) {
-              mbar_expect_tx(bar(B_VFULL0), kTileBytes);
-              tma_load_3d(sb + L::kOffV, &tmV, 0, g, b * kBlock, bar(B_VFULL0), pol_kv);
-              tma_load_3d(sb + L::kOffV + 16384, &tmV, 64, g, b * kBlock, bar(B_VFULL0), pol_kv);
-            }
+            // V (bf16, or the f16 copy of E4M3 V): two 64-column boxes of 128-byte rows
+            const uint32_t dv = sb + L::kOffV + vb * kTileBytes;
+            mbar_expect_tx(bar(B_VFULL0 + vb), kTileBytes);
+            tma_load_3d(dv, &tmV, 0, g, b * kBlock, bar(B_VFULL0 + vb), pol_kv);
+            tma_load_3d(dv + 16384, &tmV, 64, g, b * kBlock, bar(B_VFULL0 + vb), pol_kv);
           }
         }
         ok = __shfl_sync(full, ok, 0);
         if (!ok) break;
-        if constexpr (kFp8) {
-          // E4M3 [128 keys][128 B, swizzled] -> f16 [2 halves][128 keys][128 B, swizzled]:
-          // unit (key k, 16-byte source chunk c) = D columns 16c .. 16c + 15
-          for (int u = lane; u < 128 * 8; u += 32) {
-            const int k = u >> 3, c = u & 7;
-            const uint4 src = *reinterpret_cast<const uint4*>(smem + L::kOffVst + k * 128 + ((c ^ (k & 7)) << 4));
-            const uint32_t w[4] = {src.x, src.y, src.z, src.w};
-            uint32_t h[8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * q]) : "h"(static_cast<uint16_t>(w[q] & 0xFFFFu)));
-              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * q + 1]) : "h"(static_cast<uint16_t>(w[q] >> 16)));
-            }
-            const int half = c >> 2, ch = (2 * c) & 7;  // D 16c.. lies in half c/4, 16-byte chunks 2c%8, +1
-            uint8_t* dst = smem + L::kOffV + vb * kTileBytes + half * 16384 + k * 128;
-            *reinterpret_cast<uint4*>(dst + ((ch ^ (k & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(dst + (((ch + 1) ^ (k & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-          }
-          fence_proxy_async_smem();  // read next by the tensor cores
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_VFULL0 + vb));
-        }
         ++nk;
       }
       if (!ok && lane == 0) flag_timeout(p.hdr);
@@ -746,7 +716,38 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// E4M3 -> f16, elementwise and exact (every E4M3 value is an f16 value): 16 source bytes
+// per thread and step, read once (streaming), written as two 16-byte f16 chunks in order.
+__global__ void __launch_bounds__(256) widen_e4m3_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                         int64_t n16) {
+  for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n16; i += static_cast<int64_t>(gridDim.x) * 256) {
+    const uint4 v = __ldcs(src + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * q]) : "h"(static_cast<uint16_t>(w[q] & 0xFFFFu)));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * q + 1]) : "h"(static_cast<uint16_t>(w[q] >> 16)));
+    }
+    dst[2 * i] = make_uint4(h[0], h[1], h[2], h[3]);
+    dst[2 * i + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_widen_e4m3(const void* src, void* dst, int64_t n, cudaStream_t st) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t n16 = n / 16;
+  int64_t grid = (n16 + 255) / 256;
+  if (grid > sms * 8) grid = sms * 8;
+  if (grid < 1) grid = 1;
+  widen_e4m3_kernel<<<static_cast<int>(grid), 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                                            n16);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   const msa_schedule* s = a.s;
@@ -762,7 +763,11 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
     const uint32_t box[3] = {fp8 ? 128u : 64u, 1, kBlock};
     if (!encode_tmap(&tmK, dt, 3, a.K, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-    if (!encode_tmap(&tmV, dt, 3, a.V, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    // V: bf16, or (E4M3 inputs) the f16 copy made by launch_widen_e4m3, 64 elements per box row
+    const uint64_t vstrides[2] = {kHeadDim * 2, static_cast<uint64_t>(s->Hkv) * kHeadDim * 2};
+    const uint32_t vbox[3] = {64u, 1, kBlock};
+    if (!encode_tmap(&tmV, fp8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                     fp8 ? a.Vf16 : a.V, dims, vstrides, vbox, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   {

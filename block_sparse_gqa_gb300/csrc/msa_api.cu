@@ -230,10 +230,19 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
   int ctas = opts->num_ctas > 0 ? opts->num_ctas : device_sms();
   if (ctas < 1) return MSA_ERR_CUDA;
   const int Hq = static_cast<int>(Q.h);
+  const int64_t v_elems = static_cast<int64_t>(K.n) * K.h * K.d;
+  if (fp8 && !s->vf16) {
+    // the f16 copy of E4M3 V (first E4M3 call of this schedule; later calls allocate nothing)
+    void* p = nullptr;
+    cudaError_t ea = cudaMalloc(&p, static_cast<size_t>(v_elems) * 2);
+    if (ea != cudaSuccess) return from_cuda(ea);
+    s->vf16 = p;
+  }
   cudaError_t e;
   if (opts->stage_events[0] && (e = cudaEventRecord(opts->stage_events[0], stream))) return from_cuda(e);
+  if (fp8 && (e = msa::launch_widen_e4m3(V.ptr, s->vf16, v_elems, stream))) return from_cuda(e);
   msa::KvOuterArgs a{s, Q.ptr, K.ptr, V.ptr, Hq, s->nblocks * msa::kBlock, scale, force, ctas, fp8, qk_descale, f32p,
-                     opts->debug_flags};
+                     opts->debug_flags, s->vf16};
   if ((e = msa::launch_kv_outer(a, stream))) return from_cuda(e);
   if (opts->stage_events[1] && (e = cudaEventRecord(opts->stage_events[1], stream))) return from_cuda(e);
   if ((e = msa::launch_combine(s, Hq, O, LSE, v_descale, force, f32p, stream))) return from_cuda(e);
@@ -286,6 +295,7 @@ msa_status_t msa_schedule_destroy(msa_schedule_t s) {
   cudaError_t e = cudaStreamSynchronize(s->last_stream);
   if (s->partial) cudaFree(s->partial);
   if (s->bwd_ws) cudaFree(s->bwd_ws);
+  if (s->vf16) cudaFree(s->vf16);
   if (s->dev_base) cudaFree(s->dev_base);
   delete s;
   return from_cuda(e);

@@ -75,6 +75,7 @@ struct msa_schedule {
   int partial_G;
   int partial_elem;    // bytes per element the partial buffer was sized for (2 or 4)
   void* bwd_ws;  // backward workspace (first backward call)
+  void* vf16;    // E4M3 forwards: V widened to f16 [Lkv][Hkv][128] (first E4M3 call)
   cudaStream_t last_stream;
 };
 
@@ -105,8 +106,11 @@ struct KvOuterArgs {
   float qk_descale;  // q descale * k descale (1 for bf16)
   bool f32p;         // fp32 partial outputs
   int debug_flags;   // msa_fwd_opts_t.debug_flags
+  const void* Vf16;  // E4M3 inputs: V widened to f16 (launch_widen_e4m3)
 };
 cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st);
+// E4M3 [n] -> f16 [n], exact; n a multiple of 16
+cudaError_t launch_widen_e4m3(const void* src, void* dst, int64_t n, cudaStream_t st);
 
 // combine.cu
 cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, float v_descale, int force_path,
