@@ -93,11 +93,12 @@ def test_schedule_deterministic_and_reusable():
 
 
 @pytest.mark.parametrize("N,Lkv,Hkv,topK", [(1, 131072, 4, 16), (5, 2048, 1, 3), (31, 65536, 4, 8), (33, 8192, 2, 15),
-                                            (64, 4096, 1, 16), (64, 4096, 4, 4), (65, 4096, 4, 4), (16, 65536, 4, 17)])
+                                            (64, 4096, 1, 16), (64, 4096, 4, 4), (65, 4096, 4, 4), (16, 65536, 4, 17),
+                                            (300, 2048, 1, 3), (1024, 1024, 1, 1)])
 def test_schedule_small_inputs_match_oracle(N, Lkv, Hkv, topK):
     """Tiny inputs (at most 1024 list slots and 8192 bitmask words) are scheduled by one
-    CTA; the shapes here sit on both sides of that limit, with pads, duplicates, future
-    blocks and one invalid id."""
+    CTA; the shapes here sit on both sides of that limit (the last two: one CTA with 2
+    and 4 query windows), with pads, duplicates, future blocks and one invalid id."""
     rng = np.random.default_rng(N * 100 + topK)
     nb = Lkv // 128
     idx = rng.integers(-1, nb, size=(N, Hkv, topK)).astype(np.int32)
