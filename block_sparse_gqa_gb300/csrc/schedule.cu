@@ -14,8 +14,8 @@
 // that follows is a pure function of the input and rows come out sorted by query.
 //
 // Kernels, in stream order:
-//   entries<mark>     one thread per list slot: bits for every valid entry; bad ids ->
-//                     sticky status bit
+//   mark              (entries<mark>) one thread per list slot: bits for every valid
+//                     entry; bad ids -> sticky status bit
 //   rowscan           per row: exclusive popcount prefix over words, row count, tiles
 //                     per (window, row) segment
 //   scan_small        one CTA: offsets, E, nsb, the Q-outer / KV-outer decision and the
@@ -25,7 +25,7 @@
 //   tiles             the work list, window-major, 8-entry tiles  } read what the scans wrote
 // Tiny inputs (decode sizes) take one CTA instead: schedule_one runs the same phases
 // with CTA barriers in between and writes the same arrays, in one launch instead of two
-// memsets and five kernels.
+// memsets and four kernels.
 #include "msa_internal.h"
 #include "ptx.cuh"
 
