@@ -49,7 +49,7 @@ def _load():
         lib.oracle_schedule.restype = i32
         lib.oracle_schedule.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
         lib.oracle_worklist.restype = ctypes.c_long
-        lib.oracle_worklist.argtypes = [P, P, i32, i32, P, ctypes.c_long]
+        lib.oracle_worklist.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.c_long]
         lib.oracle_lse_merge.restype = None
         lib.oracle_lse_merge.argtypes = [i32, i32, P, P, P, P]
         lib.oracle_bf16_decode.restype = f64
@@ -182,17 +182,22 @@ def schedule(indices, *, Lkv, block=128):
                 cmap=cmap, E=E, nsb=int(nsb.value), status=int(st))
 
 
-def worklist(counts, offsets, tile_rows=8):
-    """Tiles (row, first, count) of at most tile_rows entries, in row order."""
+def worklist(offsets, qlist, N, window=256, tile_rows=8):
+    """Window-ordered tiles of a schedule's CSR: (tiles [T, 4] as (row, first, count,
+    window), window_tiles [nW + 1])."""
     lib = _load()
-    counts = np.ascontiguousarray(counts, dtype=np.int32)
     offsets = np.ascontiguousarray(offsets, dtype=np.int32)
-    R = len(counts)
-    cap = int(sum((int(c) + tile_rows - 1) // tile_rows for c in counts)) + 1
-    tiles = np.zeros((cap, 3), np.int32)
-    T = lib.oracle_worklist(_ptr(counts), _ptr(offsets), R, tile_rows, _ptr(tiles), cap)
+    qlist = np.ascontiguousarray(qlist, dtype=np.int32)
+    R = len(offsets) - 1
+    nW = (N + window - 1) // window
+    E = int(offsets[-1])
+    cap = E + R * nW + 1
+    tiles = np.zeros((cap, 4), np.int32)
+    wt = np.zeros(nW + 1, np.int32)
+    T = lib.oracle_worklist(_ptr(offsets), _ptr(qlist if len(qlist) else np.zeros(1, np.int32)), R, N, window,
+                            tile_rows, _ptr(tiles), _ptr(wt), cap)
     assert T >= 0
-    return tiles[:T].copy()
+    return tiles[:T].copy(), wt
 
 
 def lse_merge(O_parts, lse_parts):

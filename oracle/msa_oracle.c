@@ -23,7 +23,7 @@
  *  - "Sparse Attention", Chapter 5, "Partial outputs and Combine": partials are merged
  *    with weights computed from their log-sum-exp values.
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent, taken as the plainest the rest supports:
  *  - queries occupy the last N positions of the KV sequence: pos(i) = Lkv - N + i;
  *  - key j is visible to query i iff j <= pos(i) (diagonal included);
  *  - block ids per list: -1 is padding; a repeated id counts once (union); an id
@@ -33,13 +33,18 @@
  *  - LSE is the natural log of sum_j exp(s_j); an empty key set gives O = 0 and
  *    LSE = -inf;
  *  - schedule rows are r = g * nblocks + b; each row lists its queries ascending,
- *    with the slot (list position) of the first occurrence of b in the query's list.
+ *    with the slot (list position) of the first occurrence of b in the query's list;
+ *  - the work list cuts each row's entries per window of 256 query ids into tiles of
+ *    at most 8 entries, listed window by window (the page's split rule is garbled;
+ *    see oracle_worklist);
+ *  - the dispatch threshold is stated at oracle_dispatch.
  *
  * Pins: every function here is checked by the CPU test suite against results fixed
  * independently of this file (dense causal attention, explicit single-block softmax,
  * closed forms, brute-force masks, invariances, the worked example of the reverse
- * index).  The work-list split rule and the dispatch threshold constant are
- * builder-defined; their restatement here is parity unpinned.
+ * index, a hand-derived work list).  The work-list split rule and the dispatch
+ * threshold are readings rather than statements of the pages: the tests pin this
+ * file's restatement of them, not the pages' intent.
  */
 #include <math.h>
 #include <pthread.h>
@@ -265,21 +270,44 @@ int oracle_schedule(const int32_t* indices, int N, int Lkv, int Hkv, int topK, i
   return bad;
 }
 
-/* Work list: each row's entries cut, in order, into tiles of at most tile_rows
- * entries; tiles listed in row order.  tiles[3*t] = row, [3*t+1] = first CSR
- * position, [3*t+2] = count.  Returns the number of tiles (or -1 if cap is too
- * small).  Builder-defined split rule: parity unpinned by the pages. */
-long oracle_worklist(const int32_t* counts, const int32_t* offsets, int R, int tile_rows,
-                     int32_t* tiles, long cap) {
+/* Work list ("Kernel optimization for MiniMax M3", load-balancing section: heavy
+ * blocks are split into pieces spread over the CTAs; the page's own split rule is
+ * lost in extraction).  Reading used by this project: the queries are cut into
+ * windows of `window` consecutive query ids (the last one may be shorter); inside a
+ * window every row r = g * nblocks + b, in increasing r, contributes the run of its
+ * CSR entries whose query lies in the window (a contiguous run, since each row lists
+ * its queries ascending), cut in order into tiles of at most tile_rows entries.  Tiles
+ * are listed window by window, then row by row, then by first entry.
+ *
+ * tiles[4*t .. 4*t+3] = (row, first CSR position, count, window);
+ * window_tiles[w] = index of the first tile of window w, window_tiles[nW] = total,
+ * nW = ceil(N / window).  Returns the number of tiles, or -1 if cap is too small.
+ * The split rule is a reading, not fixed by the pages. */
+long oracle_worklist(const int32_t* offsets, const int32_t* qlist, int R, int N, int window, int tile_rows,
+                     int32_t* tiles, int32_t* window_tiles, long cap) {
+  const int nW = (N + window - 1) / window;
   long T = 0;
-  for (int r = 0; r < R; ++r)
-    for (int f = 0; f < counts[r]; f += tile_rows) {
-      if (T >= cap) return -1;
-      tiles[3 * T] = r;
-      tiles[3 * T + 1] = offsets[r] + f;
-      tiles[3 * T + 2] = counts[r] - f < tile_rows ? counts[r] - f : tile_rows;
-      ++T;
+  for (int w = 0; w < nW; ++w) {
+    window_tiles[w] = (int32_t)T;
+    for (int r = 0; r < R; ++r) {
+      /* the entries of row r whose query is in window w */
+      int first = -1, count = 0;
+      for (int p = offsets[r]; p < offsets[r + 1]; ++p) {
+        if (qlist[p] / window != w) continue;
+        if (first < 0) first = p;
+        ++count;
+      }
+      for (int f = 0; f < count; f += tile_rows) {
+        if (T >= cap) return -1;
+        tiles[4 * T] = r;
+        tiles[4 * T + 1] = first + f;
+        tiles[4 * T + 2] = count - f < tile_rows ? count - f : tile_rows;
+        tiles[4 * T + 3] = w;
+        ++T;
+      }
     }
+  }
+  window_tiles[nW] = (int32_t)T;
   return T;
 }
 
@@ -316,7 +344,7 @@ int oracle_dispatch(int32_t nsb, int N) {
  * and every KV block of the group by the mean of its 128 key vectors; the block's
  * score is the largest, over the group's heads, of the dot product of the two means;
  * the tile keeps the topK best blocks ("TopK16" in the chapter).
- * Readings where the chapter is silent (also in the design notes):
+ * Readings where the chapter is silent:
  *  - a tile is queries [128 t, min(128 t + 128, N)); its mean is over the queries it
  *    holds;
  *  - candidates are the blocks b <= lb(last query of the tile) (causal for at least one

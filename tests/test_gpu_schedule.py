@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads
-from tests.util import check_worklist
+from tests.util import TILE, WINDOW, check_worklist
 
 pytestmark = pytest.mark.gpu
 
@@ -32,6 +32,9 @@ def assert_same(exp, ref, N, Lkv):
     assert exp["E"] == ref["E"] and exp["nsb"] == ref["nsb"]
     assert exp["path"] == oracle.dispatch(ref["nsb"], N)
     check_worklist(exp, ref, N)
+    tiles, wt = oracle.worklist(ref["offsets"], ref["qlist"], N, window=WINDOW, tile_rows=TILE)
+    np.testing.assert_array_equal(np.asarray(exp["window_tiles"]), wt, err_msg="window_tiles")
+    np.testing.assert_array_equal(np.asarray(exp["tiles"]).reshape(-1, 4), tiles, err_msg="tiles")
 
 
 @pytest.mark.parametrize("name", ["tiny", "m3", "long", "lowreuse", "fp8"])
@@ -74,7 +77,11 @@ def test_schedule_bad_index_flagged_and_ignored():
     for k in ("counts", "offsets", "qlist", "slot", "cmap"):
         np.testing.assert_array_equal(exp[k], ref[k])
     assert s.query()["status_code"] == 5  # MSA_ERR_BAD_INDEX
+    assert msa.lib().msa_schedule_status(s.handle) == 5  # the same sticky bit through msa_schedule_status
     s.close()
+    clean, _ = gpu_schedule(np.array([[[0, -1]], [[1, 0]]], np.int32), 2)
+    assert msa.lib().msa_schedule_status(clean.handle) == 0
+    clean.close()
     with pytest.raises(msa.MsaError):
         msa.build_schedule(torch.zeros((4, 1, 2), dtype=torch.int32, device="cuda"), 0)
 

@@ -278,11 +278,52 @@ def test_schedule_invalid_ids_flagged():
     assert s["status"] == 1 and s["E"] == 1
 
 
-def test_worklist_covers_rows():
-    counts = np.array([0, 3, 17, 8, 1], np.int32)
-    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
-    t = oracle.worklist(counts, offsets, 8)
-    assert t.tolist() == [[1, 0, 3], [2, 3, 8], [2, 11, 8], [2, 19, 1], [3, 20, 8], [4, 28, 1]]
+def test_worklist_golden_windows():
+    """The window-ordered work list against a hand-derived example: a short last
+    window, a row whose entries span both windows, an empty segment and segments cut
+    into tiles of 8 with a ragged last tile (tests/golden/worklist_windows.json)."""
+    with open(os.path.join(GOLDEN, "worklist_windows.json")) as f:
+        ex = json.load(f)
+    N, Lkv, block = ex["N"], ex["Lkv"], ex["block"]
+    lb = (Lkv - N + np.arange(N)) // block
+    idx = np.full((N, ex["Hkv"], ex["topK"]), -1, np.int32)
+    idx[:, 0, 0] = lb
+    idx[ex["second_block_zero_queries"], 0, 1] = 0
+    s = oracle.schedule(idx, Lkv=Lkv, block=block)
+    assert s["E"] == ex["expected_E"] and s["offsets"].tolist() == ex["expected_offsets"]
+    tiles, wt = oracle.worklist(s["offsets"], s["qlist"], N, window=ex["window"], tile_rows=ex["tile"])
+    assert wt.tolist() == ex["expected_window_tiles"]
+    assert tiles.tolist() == ex["expected_tiles"]
+
+
+@pytest.mark.parametrize("seed,N,Lkv,Hkv,window", [(0, 700, 1024, 2, 256), (1, 256, 512, 1, 256), (2, 97, 2048, 3, 32),
+                                                   (3, 1, 128, 1, 256)])
+def test_worklist_invariants(seed, N, Lkv, Hkv, window):
+    """Every CSR entry in exactly one tile; a tile holds 1..8 consecutive entries of one
+    row whose queries all lie in its window; only a segment's last tile is short; tiles
+    ordered by (window, row, first); window_tiles brackets each window's tiles."""
+    rng = np.random.default_rng(40 + seed)
+    nb, topK = Lkv // 128, 5
+    idx = rng.integers(-1, nb, size=(N, Hkv, topK)).astype(np.int32)
+    s = oracle.schedule(idx, Lkv=Lkv)
+    tiles, wt = oracle.worklist(s["offsets"], s["qlist"], N, window=window)
+    E, R, nW = s["E"], len(s["counts"]), (N + window - 1) // window
+    assert len(wt) == nW + 1 and wt[0] == 0 and wt[-1] == len(tiles)
+    seen = np.zeros(E, np.int64)
+    row_of = np.repeat(np.arange(R), s["counts"])
+    seg_len = {}
+    for t, (r, first, cnt, w) in enumerate(tiles.tolist()):
+        assert wt[w] <= t < wt[w + 1] and 1 <= cnt <= 8
+        assert s["offsets"][r] <= first and first + cnt <= s["offsets"][r + 1]
+        for p in range(first, first + cnt):
+            seen[p] += 1
+            assert row_of[p] == r and s["qlist"][p] // window == w
+        seg_len.setdefault((w, r), []).append(cnt)
+    assert np.all(seen == 1)
+    for lens in seg_len.values():
+        assert all(c == 8 for c in lens[:-1])
+    keys = [(w, r, f) for r, f, _, w in tiles.tolist()]
+    assert keys == sorted(keys) and len(set(keys)) == len(keys)
 
 
 def test_dispatch_threshold():
@@ -302,10 +343,14 @@ def test_e4m3_decoder_matches_library_cast():
 
 
 def test_bf16_decoder_matches_library_cast():
-    rng = np.random.default_rng(7)
-    x = torch.from_numpy(rng.standard_normal(1000).astype(np.float32)).to(torch.bfloat16)
-    bits = x.view(torch.int16).numpy().view(np.uint16)
-    assert all(oracle.bf16_decode(int(u)) == float(v) for u, v in zip(bits, x.to(torch.float64)))
+    """The bf16 decoder agrees with torch's bfloat16 -> float64 cast on all 65,536 codes."""
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    lib = torch.from_numpy(codes.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    ours = np.array([oracle.bf16_decode(int(u)) for u in codes])
+    nan = np.isnan(lib)
+    assert np.array_equal(nan, np.isnan(ours)) and nan.sum() == 2 * 127
+    assert np.array_equal(lib[~nan], ours[~nan])
+    assert np.array_equal(np.signbit(lib[~nan]), np.signbit(ours[~nan]))
 
 
 def test_fp8_path_equals_decoded_f64():
