@@ -7,11 +7,16 @@ scale of either sign; the forward runs with AUTO, KV-outer forced and Q-outer fo
 three must agree with the oracle), and the backward runs over the same schedule.  Queries
 sit at the tail of the keys and the own block is always in the list.
 
-Tolerance: relative L2 <= 1e-2 over O and |dLSE| <= 1e-3 as everywhere; element-wise
-|dO| <= 2e-2 + 8e-3 |O| instead of a flat 2e-2, because short lists (topK = 1: only the
-causal part of the own block) give outputs as large as the V values themselves, where a
-bf16 output alone rounds by up to 1.6e-2 (|O| in [4, 8)) before the bf16 P and partial
-roundings; 8e-3 is about two bf16 roundings.
+Tolerance: relative L2 <= 1e-2 over O and |dLSE| <= 1e-3 as everywhere, and the flat
+element-wise |dO| <= 2e-2 wherever the oracle's |O| <= 2.  There bf16 rounding stays well
+inside the flat bound: a number below 2 has a bf16 spacing of at most 2^-7, so the three
+roundings on the way to O (the bf16 P weights, the bf16 partial, the bf16 output) add up
+to at most about 1.2e-2.  In [2, 4) the spacing is 2^-6 and the same three roundings reach
+2.3e-2, in [4, 8) twice that; so only elements with |O| > 2 get 2e-2 + 8e-3 |O| (8e-3 |O|
+is about two bf16 roundings of O itself).  Such outputs come from queries that see only a
+few keys (short lists, e.g. topK = 1: the causal part of the own block), where O is
+nearly a single V row; the configured workloads have |O| < 1 everywhere.  The count of
+elements over the flat 2e-2 is printed for every path.
 """
 import numpy as np
 import pytest
@@ -60,7 +65,12 @@ def test_random_case(seed):
         outs[path] = (O, LSE)
         Og = O.float().cpu().numpy()
         rel, mabs, lerr = compare_outputs(Og, LSE.cpu().numpy(), Or, Lr)
-        excess = float((np.abs(Og - Or) - (BF16_MAX_ABS + 8e-3 * np.abs(Or))).max())
+        err, mag = np.abs(Og - Or), np.abs(Or)
+        bound = np.where(mag > 2.0, BF16_MAX_ABS + 8e-3 * mag, BF16_MAX_ABS)
+        excess = float((err - bound).max())
+        over_flat = int((err > BF16_MAX_ABS).sum())
+        print(f"seed {seed} {path}: rel-L2 {rel:.2e}, max|dO| {mabs:.2e}, elements over 2e-2: {over_flat} "
+              f"(|O| > 2: {int((mag > 2.0).sum())})")
         assert rel <= BF16_REL_L2 and excess <= 0 and lerr <= LSE_MAX_ABS, (path, rel, mabs, excess, lerr)
     O, LSE = outs["kv_outer"]
     dQ, dK, dV = msa.sparse_attn_bwd(Qd, Kd, Vd, O, dOd, LSE, s, scale=scale)
