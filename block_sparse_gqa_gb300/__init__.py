@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
         L.msa_schedule_destroy.argtypes = [P]
         L.msa_schedule_query.restype = I
         L.msa_schedule_query.argtypes = [P, ctypes.POINTER(ScheduleInfo)]
+        L.msa_schedule_status.restype = I
+        L.msa_schedule_status.argtypes = [P]
         L.msa_schedule_export.restype = I
         L.msa_schedule_export.argtypes = [P] + [P] * 7
         L.msa_status_string.restype = ctypes.c_char_p
@@ -134,6 +136,10 @@ class Schedule:
         d = {k: getattr(info, k) for k, _ in ScheduleInfo._fields_}
         d["status_code"] = st
         return d
+
+    def status(self) -> int:
+        """msa_schedule_status: the sticky device status as an msa_status_t code (synchronises)."""
+        return lib().msa_schedule_status(self.handle)
 
     def export(self) -> dict:
         """Host copies of the schedule arrays (synchronises)."""

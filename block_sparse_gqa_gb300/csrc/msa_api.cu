@@ -301,6 +301,12 @@ msa_status_t msa_schedule_destroy(msa_schedule_t s) {
   return from_cuda(e);
 }
 
+msa_status_t msa_schedule_status(msa_schedule_t s) {
+  if (!s) return MSA_ERR_INVALID_ARG;
+  msa_schedule_info_t info;
+  return msa_schedule_query(s, &info);
+}
+
 msa_status_t msa_schedule_query(msa_schedule_t s, msa_schedule_info_t* info) {
   if (!s || !info) return MSA_ERR_INVALID_ARG;
   cudaError_t e = cudaStreamSynchronize(s->last_stream);

@@ -213,6 +213,17 @@ typedef struct {
  * filled).  Test and debug use. */
 msa_status_t msa_schedule_query(msa_schedule_t s, msa_schedule_info_t* info);
 
+/* msa_schedule_status -- the schedule's sticky device status (test and debug use).
+ * Synchronises the schedule's last stream, then returns MSA_ERR_TIMEOUT if a bounded
+ * device wait of a call on this schedule expired, else MSA_ERR_BAD_INDEX if the
+ * schedule build saw a block id >= nblocks or < -1 (ignored as padding), else MSA_OK.
+ * MSA_ERR_INVALID_ARG for a NULL schedule; MSA_ERR_CUDA if the synchronisation or the
+ * read fails.  The same bits as msa_schedule_query's info->status; they stay set until
+ * the schedule is rebuilt.  Device-detected errors never abort or trap ("Kernel
+ * optimization for MiniMax M3": shapes fixed per request, no device-to-host sync on the
+ * hot path, so this check is kept off the hot path). */
+msa_status_t msa_schedule_status(msa_schedule_t s);
+
 /* Synchronises and copies the schedule to host arrays (any may be NULL):
  * counts[rows], offsets[rows+1], qlist[E], slot[E], cmap[N*Hkv*topK],
  * tiles[4*ntiles] as (row, first, count, window), window_tiles[windows+1].
@@ -235,13 +246,23 @@ msa_status_t msa_schedule_export(msa_schedule_t s, int32_t* counts, int32_t* off
  * the device-wide synchronisation of cudaMalloc / cudaFree.
  *
  * Arguments are those of msa_build_schedule followed by those of
- * msa_sparse_attn_fwd (without a schedule handle); results are the same as that
- * pair's.  The schedule and the partial outputs live in one fixed device array of
- * MSA_NOALLOC_SCRATCH_BYTES inside libmsa, which every GPU that loads the library
- * holds until the process exits.  Limits: the workspace for N * Hkv * topK list
- * slots (about 4.2 KB per slot for the partial outputs, plus the schedule) must fit
- * in that array, else MSA_ERR_CAPACITY is returned before anything is enqueued (the
- * 1024-query, 1 KV head, topK 4 shape fits; the M3 shape does not).
+ * msa_sparse_attn_fwd (without a schedule handle), then `status`; results are the
+ * same as that pair's.  The schedule and the partial outputs live in one fixed device
+ * array of MSA_NOALLOC_SCRATCH_BYTES inside libmsa, which every GPU that loads the
+ * library holds until the process exits.  Limits: the workspace for N * Hkv * topK
+ * list slots (about 4.2 KB per slot for the partial outputs, plus the schedule) must
+ * fit in that array, else MSA_ERR_CAPACITY is returned before anything is enqueued (the
+ * 1024-query, 1 KV head, topK 4 shape fits; the M3 shape does not).  Inputs must be
+ * bf16; opts->partials_fp32 and opts->debug_flags must be 0 (MSA_ERR_UNSUPPORTED
+ * otherwise).
+ *
+ * status: optional (NULL = not wanted) int32 in caller memory that the device can
+ * write (device memory, or pinned / managed host memory).  After the forward, on the
+ * same stream, the call copies the schedule's sticky bits into it: bit 0 = a block id
+ * >= nblocks or < -1 was seen (and ignored), bit 1 = a bounded device wait expired
+ * (outputs undefined).  These are the bits msa_schedule_query reports for the
+ * allocating pair; here the schedule lives in the shared array, and the next call
+ * clears them, so this copy is the only way to see them.
  *
  * The first call on a device looks up the array's device address with that device
  * current; make that first call before any stream capture.  Every call reuses the
@@ -251,7 +272,7 @@ msa_status_t msa_schedule_export(msa_schedule_t s, int32_t* counts, int32_t* off
  */
 msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int N, int Hkv, int topK, int nblocks,
                                          msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, void* O, float* LSE,
-                                         float scale, const msa_fwd_opts_t* opts);
+                                         float scale, int32_t* status, const msa_fwd_opts_t* opts);
 
 /*
  * Block selector R1 ("Sparse Attention" (dinara-dl), Chapter 4, "R1: One

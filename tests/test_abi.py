@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for required in ("msa_build_schedule", "msa_sparse_attn_fwd", "msa_schedule_destroy",
-                     "msa_schedule_query", "msa_schedule_export", "msa_status_string"):
+                     "msa_schedule_status", "msa_schedule_query", "msa_schedule_export", "msa_status_string"):
         assert required in names
 
 
@@ -51,6 +51,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.msa_sparse_attn_fwd(t, t, t, None, None, None, 1.0, None) == 1
     assert lib.msa_schedule_destroy(None) == 1
     assert lib.msa_schedule_query(None, None) == 1
+    assert lib.msa_schedule_status(None) == 1
     assert lib.msa_status_string(6) == b"bounded device wait expired"
     assert lib.msa_version() >= 100
     opts = msa.FwdOpts()

@@ -32,11 +32,12 @@ def test_kv_outer_wait_expires_and_device_recovers():
     torch.cuda.synchronize()
     info = s.query()
     assert info["status"] & 2 and info["status_code"] == 6  # MSA_ERR_TIMEOUT
+    assert s.status() == 6  # msa_schedule_status reports the same sticky bit
     # the same schedule rebuilt (clears the sticky bits), a normal forward, parity
     msa.build_schedule(idx_d, Lkv // 128, schedule=s)
     O, LSE = msa.sparse_attn_fwd(Qd, Kd, Vd, s, path="kv_outer")
     torch.cuda.synchronize()
-    assert s.query()["status"] == 0
+    assert s.query()["status"] == 0 and s.status() == 0
     s.close()
     bits = [t.view(torch.int16).numpy().view(np.uint16) for t in (Q, K, V)]
     Or, Lr, _ = oracle.attn_fwd(*bits, idx, Lkv=Lkv, scale=128 ** -0.5)
