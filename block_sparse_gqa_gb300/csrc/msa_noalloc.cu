@@ -69,7 +69,8 @@ int device_sms() {
 
 extern "C" msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int N, int Hkv, int topK, int nblocks,
                                                     msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, void* O,
-                                                    float* LSE, float scale, const msa_fwd_opts_t* opts) {
+                                                    float* LSE, float scale, int32_t* status,
+                                                    const msa_fwd_opts_t* opts) {
   msa_fwd_opts_t def;
   if (!opts) {
     msa_fwd_opts_init(&def);
@@ -79,6 +80,7 @@ extern "C" msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int 
   if (!indices || !Q.ptr || !K.ptr || !V.ptr || !O) return MSA_ERR_INVALID_ARG;
   if (N < 1 || Hkv < 1 || topK < 1 || nblocks < 1) return MSA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(nblocks) * msa::kBlock > INT32_MAX) return MSA_ERR_CAPACITY;
+  if (static_cast<int64_t>(Hkv) * nblocks > INT32_MAX) return MSA_ERR_CAPACITY;
   if (static_cast<int64_t>(N) > static_cast<int64_t>(nblocks) * msa::kBlock) return MSA_ERR_INVALID_ARG;
   if (topK > 64) return MSA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(N) * Hkv * topK * msa::kGroup > INT32_MAX) return MSA_ERR_CAPACITY;
@@ -91,6 +93,9 @@ extern "C" msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int 
   if (!std::isfinite(scale)) return MSA_ERR_INVALID_ARG;
   if (opts->path != MSA_PATH_AUTO && opts->path != MSA_PATH_KV_OUTER && opts->path != MSA_PATH_Q_OUTER)
     return MSA_ERR_INVALID_ARG;
+  // the scratch holds bf16 partials only, and the test-only kernel instances stay with
+  // the allocating entry points
+  if (opts->partials_fp32 != 0 || opts->debug_flags != 0) return MSA_ERR_UNSUPPORTED;
 
   // layout inside the scratch array: schedule arrays, then partial outputs and their (m, l)
   msa_schedule s;
@@ -129,5 +134,7 @@ extern "C" msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int 
   if ((e = msa::launch_q_outer(&s, Q.ptr, K.ptr, V.ptr, Hq, scale, O, LSE, force, stream)))
     return msa::status_from_cuda(e);
   if (opts->stage_events[2] && (e = cudaEventRecord(opts->stage_events[2], stream))) return msa::status_from_cuda(e);
+  if (status && (e = cudaMemcpyAsync(status, &s.d.hdr->status, sizeof(int32_t), cudaMemcpyDefault, stream)))
+    return msa::status_from_cuda(e);
   return MSA_OK;
 }
