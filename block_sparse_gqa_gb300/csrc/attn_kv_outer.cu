@@ -20,8 +20,11 @@
 // Warp roles (512 threads = 4 warpgroups, one CTA per SM; a warp reaches TMEM
 // lanes 32 * (warp % 4) .. + 31, so a warpgroup covers all 128 rows):
 //   warp 0       scheduler, all 32 lanes: claims chunks, reads the next chunk's
-//                tile info and query ids ahead of time and publishes each tile in a
-//                shared-memory ring for the other roles (it only waits for ring slots)
+//                tile info and query ids ahead of time, gathers each tile's Q into Q
+//                stage t % 3 (three stages) once S(t - 3) has read it -- one TMA box per
+//                query, the 16 heads of its group (4 KB bf16, 2 KB E4M3), landing in the
+//                128-byte-swizzled MMA layout through a 5-D (bf16) or 3-D (E4M3) view of
+//                Q -- and publishes each tile in a shared-memory ring for the other roles
 //   warp 2       K/V loader: on a row change loads K_b into the next of two K
 //                buffers and V_b into the V buffer (TMA; E4M3: V as f16, into the next of
 //                two V buffers); a ring slot is reused only after both this warp and
@@ -32,14 +35,20 @@
 //                place).  Two issuing threads: S of tile t + 1 never waits behind
 //                the P V of tile t (its softmax, or an E4M3 V block being widened)
 //   warps 4-7    softmax of even tiles (TMEM stage 0)
-//   warps 8-11   softmax of odd tiles  (TMEM stage 1); after tile it, a softmax
-//                warpgroup gathers Q of tile it + 3 into Q stage it % 3 (three
-//                stages): 16-byte cp.async copies of the 8 query boxes (contiguous
-//                4 KB of G x D each) straight into the 128-byte-swizzled MMA layout,
-//                completion signalled by cp.async.mbarrier.arrive.noinc.  Small
-//                boxes are slow through the TMA unit, which keeps the large K/V
-//                loads and the output stores.
-//   warps 12-15  output: O[s] -> bf16 -> swizzled staging -> TMA store
+//   warps 8-11   softmax of odd tiles  (TMEM stage 1)
+//                (The Q gather used to be 16-byte cp.async copies issued by the softmax
+//                warpgroups after each softmax: the load/store unit throttled their
+//                issue to ~1.3 us per 32 KB tile, half of a warpgroup's time, while the
+//                partial stores went through the TMA unit.  The roles are now swapped:
+//                TMA carries the gather, the load/store unit the partial stores,
+//                0.554 -> 0.498 ms at M3.)
+//   warps 12-15  output: O[s] -> registers -> bf16 -> 16-byte global stores, no staging:
+//                the partial workspace is chunk-major inside each aligned group of 8
+//                CSR positions (part_index), so the 32 rows a warp holds after one
+//                TMEM load (32 consecutive columns each) are stored as 512 contiguous
+//                bytes per 16-byte column chunk.  No shared memory or CTA barrier is
+//                spent on the partials (a staged TMA store moved 64 KB of shared memory
+//                per tile, a third of the kernel's shared-memory traffic)
 // Registers are rebalanced per warpgroup with setmaxnreg: 72 for the control
 // warpgroup (at 64 its scheduler / MMA code spills, which costs 6% of kernel time),
 // 176 for the softmax warpgroups (a row's 128 scores stay in registers), 88 for the
@@ -49,8 +58,10 @@
 // scale folded in), P = 2^(s*scale*log2e - m) written back over S as bf16 pairs,
 // row sum l; (m, l) go to global as one float2 per row.
 //
-// Partial layout: raw bf16 [E*16, 128] (row = 16*CSR position + head-in-group;
-// O_k = sum_j P_j V_j, not yet divided by l) and float2 (m, l) [E*16].
+// Partial layout: raw bf16 (O_k = sum_j P_j V_j, not yet divided by l) of (CSR position
+// p, head h) in the chunk-major groups of part_index, and float2 (m, l) at [16 p + h].
+// A tile's entries are consecutive CSR positions, so its partials fill one aligned
+// group of 8 positions (32 KB, contiguous) or parts of two.
 //
 // fp8 E4M3 inputs (per-tensor descales): S = Q K^T runs on kind::f8f6f4 (K-major, one
 // 128-byte swizzle span per row, 32 elements per MMA); q and k descales are folded
@@ -96,8 +107,7 @@ struct Lay {
   // two for E4M3 so that the next row's V loads while this row's P V runs
   static constexpr int kVBuf = kFp8 ? 2 : 1;
   static constexpr uint32_t kOffV = kOffK1 + kInTile;
-  static constexpr uint32_t kOffSt = kOffV + kVBuf * kTileBytes;  // output staging
-  static constexpr uint32_t kOffCtl = kOffSt + kTileBytes;
+  static constexpr uint32_t kOffCtl = kOffV + kVBuf * kTileBytes;
   static constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + alignment slack
 };
 static_assert(Lay<false>::kSmemBytes <= 232448 && Lay<true>::kSmemBytes <= 232448, "shared memory");
@@ -106,7 +116,7 @@ static_assert(Lay<false>::kSmemBytes <= 232448 && Lay<true>::kSmemBytes <= 23244
 enum {
   B_QFULL0 = 0, B_KFULL0 = 3, B_KFREE0 = 5, B_VFULL0 = 7, B_VFREE0 = 9,  // slot 11 unused
   B_SFULL0 = 12, B_PFULL0 = 14, B_PVDONE0 = 16, B_OFREE0 = 18, B_TFULL0 = 20, B_TEMPTY0 = 20 + kRing,
-  B_COUNT = 20 + 2 * kRing
+  B_QFREE0 = 20 + 2 * kRing, B_COUNT = 20 + 2 * kRing + kQStages
 };
 constexpr uint32_t kOffTmemSlot = 8 * B_COUNT;  // 4 bytes
 constexpr uint32_t kOffRing = 512;              // kRing entries of 64 bytes
@@ -123,6 +133,7 @@ static_assert(sizeof(TileInfo) == 64, "ring entry");
 
 struct KvParams {
   const uint8_t* Q;  // bf16 or E4M3 elements
+  uint4* partial;
   int Hq;
   const int4* tiles;
   const int32_t* qlist;
@@ -158,14 +169,6 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
 }
 __device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-// the barrier receives one arrive when all of this thread's earlier cp.async copies have landed
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -255,8 +258,7 @@ __device__ __forceinline__ float2 softmax_row_any_scale(uint32_t (&v)[128], int 
 template <bool kFp8, bool kF32P, bool kWithhold = false>
 __global__ void __launch_bounds__(kThreads, 1)
 kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                const __grid_constant__ CUtensorMap tmP128, const __grid_constant__ CUtensorMap tmP16,
-                const KvParams p) {
+                const __grid_constant__ CUtensorMap tmQ, const KvParams p) {
   using L = Lay<kFp8>;
   const int path = p.force_path ? p.force_path : p.hdr->path;
   if (path != kPathKvOuter) return;
@@ -273,13 +275,17 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // zero the Q stages once so rows of a partly filled tile never hold NaN patterns
+  // zero the Q stages once so rows of a partly filled tile (no TMA box for its missing
+  // queries: they keep an earlier tile's finite values) never hold NaN patterns
   for (uint32_t o = tid * 16; o < kQStages * L::kInTile; o += kThreads * 16)
     *reinterpret_cast<uint4*>(smem + L::kOffQ + o) = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
 
   if (tid == 0) {
-    for (int s = 0; s < kQStages; ++s) mbar_init(bar(B_QFULL0 + s), 128);  // one cp.async arrive per gather thread
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(bar(B_QFULL0 + s), 1);
+      mbar_init(bar(B_QFREE0 + s), 1);
+    }
     for (int v = 0; v < 2; ++v) {
       mbar_init(bar(B_VFULL0 + v), 1);
       mbar_init(bar(B_VFREE0 + v), 1);
@@ -316,6 +322,8 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
         // ---------------------------------------------------------- producer (whole warp)
         int* counter = &p.hdr->pad[0];
         const int T = p.hdr->ntiles;
+        if (lane == 0) tma_prefetch_desc(&tmQ);
+        const uint64_t pol_q = policy_evict_normal();
         const unsigned full = 0xffffffffu;
         // Metadata of a chunk, spread over the warp: lane k < 8 holds tile k's
         // (row, first, count, -) in `tile`; lane j holds the id of query (j % 8) of
@@ -369,9 +377,8 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
         bool ok = true;
         while (ok) {
           if (cur.n == 0) {
-            // three end markers: the softmax warpgroups read alternate entries and
-            // gather Q up to three entries ahead of the tile they finished last
-            for (int e = 0; e < 3 && ok; ++e) ok = publish(it + e, 0, 0, 0, 0, 0);
+            // two end markers: the softmax warpgroups read alternate entries
+            for (int e = 0; e < 2 && ok; ++e) ok = publish(it + e, 0, 0, 0, 0, 0);
             break;
           }
           bool ids_next = false;
@@ -383,6 +390,24 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
             const int qv = __shfl_sync(full, t < 4 ? cur.qa : cur.qb, ((t & 3) << 3) | (lane & 7));
             const bool new_row = row != prev_row;
             const int kb = new_row ? (nk & 1) : ((nk - 1) & 1);
+            {
+              // Q of this tile into stage it % 3 once S(it - 3) has read that stage: one TMA
+              // box per query (its 16 heads, 4 KB bf16 / 2 KB E4M3), issued by lane j for
+              // query j after lane 0 has armed the stage's barrier with the byte count
+              const int qs = it % kQStages;
+              bool w = true;
+              if (lane == 0) {
+                if (it >= kQStages) w = mbar_wait(bar(B_QFREE0 + qs), ((it / kQStages) - 1) & 1);
+                if (w) mbar_expect_tx(bar(B_QFULL0 + qs), static_cast<uint32_t>(count) * (L::kInTile / kTileQ));
+              }
+              if (!__shfl_sync(full, w, 0)) { ok = false; break; }
+              if (lane < count) {
+                const uint32_t dq = sb + L::kOffQ + qs * L::kInTile + lane * (L::kInTile / kTileQ);
+                const int g = row / p.nblocks;
+                if constexpr (kFp8) tma_load_3d(dq, &tmQ, 0, g * kGroup, qv, bar(B_QFULL0 + qs), pol_q);
+                else tma_load_5d(dq, &tmQ, 0, 0, 0, 2 * g, qv, bar(B_QFULL0 + qs), pol_q);
+              }
+            }
             if (!publish(it, row, first, count, (new_row ? 1 : 0) | (kb << 8), qv)) { ok = false; break; }
             if (new_row) {
               ++nk;
@@ -421,8 +446,6 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           if ((flags & 1) && !(ok = mbar_wait(bar(B_KFULL0 + (seg & 1)), (seg >> 1) & 1))) break;
           const int qs = it % kQStages;
           if (!(ok = mbar_wait(bar(B_QFULL0 + qs), (it / kQStages) & 1))) break;
-          // Q was written by cp.async (generic proxy); the MMA reads it through the async proxy
-          fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t qa = sb + L::kOffQ + qs * L::kInTile, ka = sb + ((seg & 1) ? L::kOffK1 : L::kOffK0);
           if constexpr (kFp8) {
@@ -434,12 +457,14 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           } else {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-              mma_f16_ss(tmem + s * 128, smem_desc(qa + off, 16, 1024, 2), smem_desc(ka + off, 16, 1024, 2),
-                         idesc_qk, k > 0);
+              // Q: [query][8-head group][D half][8 rows][128 B] (8-row groups 2048 B apart,
+              // D halves 1024 B apart); K: [D half][128 rows][128 B]
+              mma_f16_ss(tmem + s * 128, smem_desc(qa + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048, 2),
+                         smem_desc(ka + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, 2), idesc_qk, k > 0);
             }
           }
           mma_commit(bar(B_SFULL0 + s));
+          mma_commit(bar(B_QFREE0 + qs));  // the scheduler may load tile it + 3's Q into this stage
         }
         if (!ok) flag_timeout(p.hdr);
       }
@@ -531,48 +556,16 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
     regs_inc<kRegSoftmax>();
     // ------------------------------------------------------------ softmax
     const int wg = (warp - 4) >> 2;  // 0 or 1: the stage (tile parity) handled
-    const uint32_t bar_id = 1 + wg;
     const int row = 32 * (warp & 3) + lane;
     const uint32_t tS = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + wg * 128;
     const bool neg = p.sl2 < 0.f;  // a negative scale turns the row maximum into a minimum
-    // Q of tile t >= 0 is gathered by warpgroup (t + 1) % 2: tiles 0, 1, 2 here, tile
-    // it + 3 right after the softmax of tile it.  Returns false on a timed-out wait.
-    const int gtid = tid - 128 - 128 * wg;  // 0..127 within the warpgroup
-    auto gather = [&](int t) -> bool {
-      const int slot = t % kRing;
-      const bool ok = mbar_wait(bar(B_TFULL0 + slot), (t / kRing) & 1);
-      if (!named_bar_and(bar_id, 128, ok)) return false;
-      const int count = ring[slot].count;
-      if (count == 0) return true;
-      const int g = ring[slot].row / p.nblocks;
-      const uint32_t dq = sb + L::kOffQ + (t % kQStages) * L::kInTile;
-      if constexpr (kFp8) {
-        // chunk c (16 B = 16 elements) of query j, head h: idx = j * 128 + h * 8 + c
-        for (int idx = gtid; idx < count * 128; idx += 128) {
-          const int j = idx >> 7, h = (idx >> 3) & 15, c = idx & 7;
-          const int r = j * 16 + h;  // MMA row
-          const uint8_t* src = p.Q + (static_cast<size_t>(ring[slot].q[j]) * p.Hq + g * kGroup + h) * kHeadDim + c * 16;
-          cp_async16(dq + r * 128 + ((c ^ (r & 7)) << 4), src);
-        }
-      } else {
-        // chunk c (16 B = 8 elements) of query j, head h: idx = j * 256 + h * 16 + c
-        for (int idx = gtid; idx < count * 256; idx += 128) {
-          const int j = idx >> 8, h = (idx >> 4) & 15, c = idx & 15;
-          const int r = j * 16 + h;  // MMA row
-          const uint8_t* src =
-              p.Q + ((static_cast<size_t>(ring[slot].q[j]) * p.Hq + g * kGroup + h) * kHeadDim + c * 8) * 2;
-          cp_async16(dq + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4), src);
-        }
-      }
-      cp_async_arrive_noinc(bar(B_QFULL0 + t % kQStages));
-      return true;
-    };
-    bool gok = wg == 0 ? gather(1) : (gather(0) && gather(2));
-    if (!gok) flag_timeout(p.hdr);
-    for (int it = wg; gok; it += 2) {
+    // Each warp decides for itself (tcgen05.ld / st are warp-collective, not warpgroup-
+    // collective): a bounded wait that expires in one warp ends that warp's loop, and the
+    // others' waits then expire too, since the arrivals they wait for never come.
+    for (int it = wg;; it += 2) {
       const int slot = it % kRing;
       bool ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1);
-      if (!named_bar_and(bar_id, 128, ok)) { flag_timeout(p.hdr); break; }
+      if (!__all_sync(0xffffffffu, ok)) { flag_timeout(p.hdr); break; }
       const int count = ring[slot].count;
       if (count == 0) break;
       const int j = row >> 4;
@@ -587,7 +580,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       const bool masked = __any_sync(0xffffffffu, lim < kBlock - 1);
 
       ok = mbar_wait(bar(B_SFULL0 + wg), (it >> 1) & 1);
-      if (!named_bar_and(bar_id, 128, ok)) { flag_timeout(p.hdr); break; }
+      if (!__all_sync(0xffffffffu, ok)) { flag_timeout(p.hdr); break; }
       tc_fence_after();
       uint32_t v[128];
 #pragma unroll
@@ -601,19 +594,17 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       tc_fence_before();
       mbar_arrive(bar(B_PFULL0 + wg));
       if (valid) p.pstat[static_cast<size_t>(first) * kGroup + row] = ml;
-      if (!gather(it + 3)) { flag_timeout(p.hdr); break; }
     }
   } else {
     regs_dec<kRegOut>();
-    // ------------------------------------------------------------ output (raw O -> bf16 -> TMA store)
+    // ------------------------------------------------------------ output (raw O -> global)
     const uint32_t bar_id = 3;
     const int row = 32 * (warp & 3) + lane;
+    const int jr = row >> 4, h = row & 15;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const bool elected = (tid == 384);
-    uint8_t* stage = smem + L::kOffSt;
     const uint64_t pol_st = policy_evict_first();
-    if (elected) { tma_prefetch_desc(&tmP128); tma_prefetch_desc(&tmP16); }
-    bool stored_before = false;
+    constexpr int kChunks = kF32P ? 32 : 16;
     for (int it = 0;; ++it) {
       const int slot = it % kRing;
       bool ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1);
@@ -622,92 +613,39 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       if (count == 0) break;
       const int s = it & 1;
       ok = mbar_wait(bar(B_PVDONE0 + s), (it >> 1) & 1);
-      if (elected && stored_before) bulk_wait_read0();  // staging free again
       if (!named_bar_and(bar_id, 128, ok)) { flag_timeout(p.hdr); break; }
-      // every thread has read the ring entry before the barrier above: release the slot
       if (elected) mbar_arrive(bar(B_TEMPTY0 + slot));
       tc_fence_after();
       const uint32_t tO = tmem + lane_base + 256 + s * 128;
-      if constexpr (kF32P) {
-        // fp32 partials: one D half (64 columns, 32 KB for 128 rows) at a time through the
-        // staging tile, as two 32-column boxes of 128-byte rows
+      const bool store = jr < count;
+      uint4* dst = p.partial + part_index(static_cast<int64_t>(first) + jr, h, 0, kChunks);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          if (hh == 1) {
-            // the first half's stores must have read the staging tile
-            if (elected) bulk_wait_read0();
-            named_bar_sync(bar_id, 128);
-          }
-#pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            uint32_t v[32];
-            tmem_ld32(tO + 64 * hh + 32 * c2, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint32_t off = c2 * 16384 + row * 128 + ((q ^ (row & 7)) << 4);
-              *reinterpret_cast<uint4*>(stage + off) = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
-          }
-          if (hh == 1) {
-            tc_fence_before();
-            mbar_arrive(bar(B_OFREE0 + s));
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(bar_id, 128);
-          if (elected) {
-            const uint32_t src = sb + L::kOffSt;
-            if (count == kTileQ) {
-              tma_store_2d(&tmP128, 64 * hh, first * kGroup, src, pol_st);
-              tma_store_2d(&tmP128, 64 * hh + 32, first * kGroup, src + 16384, pol_st);
-            } else {
-              for (int q = 0; q < count; ++q) {
-                tma_store_2d(&tmP16, 64 * hh, (first + q) * kGroup, src + q * 2048, pol_st);
-                tma_store_2d(&tmP16, 64 * hh + 32, (first + q) * kGroup, src + 16384 + q * 2048, pol_st);
-              }
-            }
-            bulk_commit();
-          }
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + c * 32, v);
+        tmem_ld_wait();
+        if (c == 3) {
+          tc_fence_before();
+          mbar_arrive(bar(B_OFREE0 + s));
         }
-      } else {
+        if (store) {
+          if constexpr (kF32P) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tO + c * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int ch = c * 4 + q;
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]), __uint_as_float(v[q * 8 + 1]));
-            w.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]), __uint_as_float(v[q * 8 + 3]));
-            w.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]), __uint_as_float(v[q * 8 + 5]));
-            w.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]), __uint_as_float(v[q * 8 + 7]));
-            const uint32_t off = (ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
-            *reinterpret_cast<uint4*>(stage + off) = w;
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(bar(B_OFREE0 + s));
-        fence_proxy_async_smem();
-        named_bar_sync(bar_id, 128);
-        if (elected) {
-          const uint32_t src = sb + L::kOffSt;
-          if (count == kTileQ) {
-            tma_store_2d(&tmP128, 0, first * kGroup, src, pol_st);
-            tma_store_2d(&tmP128, 64, first * kGroup, src + 16384, pol_st);
+            for (int q = 0; q < 8; ++q)
+              st_global_v4_hint(dst + (c * 8 + q) * (kPartGroup * kGroup), v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                                v[4 * q + 3], pol_st);
           } else {
-            for (int q = 0; q < count; ++q) {
-              tma_store_2d(&tmP16, 0, (first + q) * kGroup, src + q * 2048, pol_st);
-              tma_store_2d(&tmP16, 64, (first + q) * kGroup, src + 16384 + q * 2048, pol_st);
-            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_global_v4_hint(dst + (c * 4 + q) * (kPartGroup * kGroup),
+                                pack_bf16x2(__uint_as_float(v[q * 8 + 0]), __uint_as_float(v[q * 8 + 1])),
+                                pack_bf16x2(__uint_as_float(v[q * 8 + 2]), __uint_as_float(v[q * 8 + 3])),
+                                pack_bf16x2(__uint_as_float(v[q * 8 + 4]), __uint_as_float(v[q * 8 + 5])),
+                                pack_bf16x2(__uint_as_float(v[q * 8 + 6]), __uint_as_float(v[q * 8 + 7])), pol_st);
           }
-          bulk_commit();
         }
       }
-      stored_before = true;
     }
-    if (elected) bulk_wait_all0();
   }
 
   tc_fence_before();
@@ -753,7 +691,28 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   const msa_schedule* s = a.s;
   const bool fp8 = a.fp8;
   const uint64_t es = fp8 ? 1 : 2;  // bytes per input element
-  CUtensorMap tmK, tmV, tmP128, tmP16;
+  CUtensorMap tmK, tmV, tmQ;
+  {
+    // Q [N][Hq][128]: bf16 as a 5-D view (64 elements of a D half, head within 8, D half,
+    // group of 8 heads, query): one box = one query's 16 heads, 4 KB, landing as
+    // [8-head group][D half][8 rows][128 B]; E4M3 as (128 elements, head, query), one box
+    // = 16 rows of 128 B
+    const uint64_t es = a.fp8 ? 1 : 2;
+    const uint64_t row = kHeadDim * es;
+    if (a.fp8) {
+      const uint64_t dims[3] = {kHeadDim, static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(s->N)};
+      const uint64_t strides[2] = {row, static_cast<uint64_t>(a.Hq) * row};
+      const uint32_t box[3] = {128, 16, 1};
+      if (!encode_tmap(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.Q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    } else {
+      const uint64_t dims[5] = {64, 8, 2, static_cast<uint64_t>(a.Hq) / 8, static_cast<uint64_t>(s->N)};
+      const uint64_t strides[4] = {row, 128, 8 * row, static_cast<uint64_t>(a.Hq) * row};
+      const uint32_t box[5] = {64, 8, 2, 2, 1};
+      if (!encode_tmap(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, a.Q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    }
+  }
   {
     // K / V [Lkv][Hkv][128]: one block of one group per load, 64 elements (bf16) or
     // 128 elements (E4M3) = 128 bytes per box row
@@ -770,22 +729,9 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
                      fp8 ? a.Vf16 : a.V, dims, vstrides, vbox, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  {
-    // partial rows [E * 16][128], bf16 or fp32; boxes of 128-byte rows (64 bf16 or 32 fp32
-    // columns) for a full tile's 128 rows or one entry's 16 rows
-    const uint64_t pes = a.f32p ? 4 : 2;
-    const uint64_t dims[2] = {kHeadDim, static_cast<uint64_t>(s->cap_entries) * kGroup};
-    const uint64_t strides[1] = {kHeadDim * pes};
-    const uint32_t bw = static_cast<uint32_t>(128 / pes);
-    const uint32_t box128[2] = {bw, 128}, box16[2] = {bw, 16};
-    const CUtensorMapDataType pdt = a.f32p ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (!encode_tmap(&tmP128, pdt, 2, s->partial, dims, strides, box128, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-    if (!encode_tmap(&tmP16, pdt, 2, s->partial, dims, strides, box16, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
   KvParams p;
   p.Q = static_cast<const uint8_t*>(a.Q);
+  p.partial = static_cast<uint4*>(s->partial);
   p.Hq = a.Hq;
   p.tiles = s->d.tiles;
   p.qlist = s->d.qlist;
@@ -798,7 +744,7 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   p.force_path = a.force_path;
   static bool attr_set[4] = {false, false, false, false};
   const int inst = (fp8 ? 1 : 0) | (a.f32p ? 2 : 0);
-  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, KvParams);
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, KvParams);
   switch (inst) {
     case 0: kern = kv_outer_kernel<false, false>; break;
     case 1: kern = kv_outer_kernel<true, false>; break;
@@ -824,7 +770,7 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   // launch cheap where the device picks the Q-outer path and this kernel exits at once)
   const int64_t max_chunks = (s->cap_tiles + kChunkTiles - 1) / kChunkTiles;
   const int grid = max_chunks < a.num_ctas ? static_cast<int>(max_chunks) : a.num_ctas;
-  kern<<<grid, kThreads, smem, st>>>(tmK, tmV, tmP128, tmP16, p);
+  kern<<<grid, kThreads, smem, st>>>(tmK, tmV, tmQ, p);
   return cudaGetLastError();
 }
 

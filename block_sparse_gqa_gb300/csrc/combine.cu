@@ -8,16 +8,19 @@
 // combine); combine gathers them through the map (query, kv_head, top-i) ->
 // partial row.  It is bandwidth-bound and tolerant of gather latency.
 //
-// Partial k of (query i, group g, head h) is row 16 * cmap[i, g, k] + h of the
-// bf16 (or, on request, fp32) [E*16, 128] slab: O_k = sum_j 2^(x_j - m_k) V_j over the block's visible keys
+// Partial k of (query i, group g, head h) belongs to CSR position p = cmap[i, g, k] of
+// the bf16 (or, on request, fp32) partial workspace, in the chunk-major layout of
+// part_index (aligned groups of 8 positions, 16-byte column chunks outermost), with its
+// statistics at pstat[16 p + h]: O_k = sum_j 2^(x_j - m_k) V_j over the block's visible keys
 // (x = score * scale * log2 e), with statistics (m_k, l_k = sum_j 2^(x_j - m_k)).
 // For E4M3 inputs the V descale multiplies the merged output (the partials hold P V
 // of the stored E4M3 values).
 // With M = max_k m_k and w_k = 2^(m_k - M):
 //   O = sum_k w_k O_k / sum_k w_k l_k,   LSE = ln 2 * (M + log2 sum_k w_k l_k).
 //
-// One CTA of 256 threads per (i, g) unit at a time: thread (h, c) owns head h and
-// output columns [8c, 8c + 8); a warp reads 512 contiguous bytes of each partial.  The
+// One CTA of 256 threads per (i, g) unit at a time: thread (h, c) = (tid % 16, tid / 16)
+// owns head h and output columns [8c, 8c + 8); a warp reads two 256-byte runs of each
+// partial (column chunks c, c + 1 of the 16 heads).  The
 // statistics and partial loads of 8 slots are issued together once the combine map is
 // known; the first 8 map entries of a CTA's next unit are loaded while it merges the
 // current one, so a unit of up to 8 slots costs one round trip.  Partials and statistics
@@ -75,7 +78,7 @@ combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ parti
   constexpr int kKChunk = kF32 ? 4 : 8;  // partial loads in flight per thread
   const int path = force_path ? force_path : hdr->path;
   if (path != kPathKvOuter) return;
-  const int h = threadIdx.x >> 4, c = threadIdx.x & 15;
+  const int h = threadIdx.x & 15, c = threadIdx.x >> 4;
   const int64_t units = static_cast<int64_t>(N) * Hkv;
   int pre[kKChunk];  // the first map entries of this CTA's next unit
   {
@@ -106,10 +109,11 @@ combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ parti
         const int64_t r = static_cast<int64_t>(pos[k]) * kGroup + h;
         st[k] = pos[k] >= 0 ? __ldcs(pstat + r) : make_float2(-INFINITY, 0.f);
         if constexpr (kF32) {
-          v[k].a = pos[k] >= 0 ? __ldcs(partial + r * 32 + 2 * c) : make_uint4(0, 0, 0, 0);
-          v[k].b = pos[k] >= 0 ? __ldcs(partial + r * 32 + 2 * c + 1) : make_uint4(0, 0, 0, 0);
+          const int64_t x = part_index(pos[k], h, 2 * c, 32);
+          v[k].a = pos[k] >= 0 ? __ldcs(partial + x) : make_uint4(0, 0, 0, 0);
+          v[k].b = pos[k] >= 0 ? __ldcs(partial + x + kPartGroup * kGroup) : make_uint4(0, 0, 0, 0);
         } else {
-          v[k].a = pos[k] >= 0 ? __ldcs(partial + r * 16 + c) : make_uint4(0, 0, 0, 0);
+          v[k].a = pos[k] >= 0 ? __ldcs(partial + part_index(pos[k], h, c, 16)) : make_uint4(0, 0, 0, 0);
         }
       }
       float Mc = M;

@@ -68,7 +68,7 @@ msa_status_t ensure_partials(msa_schedule* s, int G, int elem = 2) {
     s->partial = nullptr;
     s->pstat = nullptr;
   }
-  const size_t rows = static_cast<size_t>(s->cap_entries) * G;
+  const size_t rows = static_cast<size_t>(msa::part_rows(s->cap_entries)) * G / msa::kGroup;
   const size_t obytes = align_up(rows * msa::kHeadDim * elem, 256);
   void* p = nullptr;
   cudaError_t e = cudaMalloc(&p, obytes + rows * sizeof(float2));

@@ -21,6 +21,23 @@ constexpr int kQSplitMax = 8;
 constexpr int kQSplitMin = 4;
 constexpr int kQSplitMaxUnits = 64;
 
+// Partial outputs of the KV-outer path (bf16 or fp32 rows of 128, one per (CSR position,
+// head of the group)): positions in aligned groups of kPartGroup = 8 -- a tile's 8 entries
+// are 8 consecutive positions -- and inside a group the layout is [16-byte column chunk]
+// [8 positions x 16 heads], so that the attention kernel's warp store of one column chunk
+// of 32 rows (after a 32x32b TMEM load: a thread per row) covers 512 contiguous bytes, and
+// the combine reads 256 contiguous bytes per (position, chunk).  Chunk c of (position p,
+// head h) is the uint4 at part_index(p, h, c, chunks), chunks = 16 (bf16: 8 columns) or
+// 32 (fp32: 4 columns).
+constexpr int kPartGroup = 8;
+__host__ __device__ __forceinline__ int64_t part_index(int64_t p, int h, int c, int chunks) {
+  return ((p / kPartGroup) * chunks + c) * (kPartGroup * kGroup) + (p % kPartGroup) * kGroup + h;
+}
+// rows (of 128 elements) the partial workspace holds for cap positions: whole groups
+__host__ __device__ __forceinline__ int64_t part_rows(int64_t cap) {
+  return (cap + kPartGroup - 1) / kPartGroup * kPartGroup * kGroup;
+}
+
 constexpr int kPathKvOuter = 1;
 constexpr int kPathQOuter = 2;
 

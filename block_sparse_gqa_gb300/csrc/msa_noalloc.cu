@@ -102,7 +102,7 @@ extern "C" msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int 
   std::memset(&s, 0, sizeof(s));
   msa::schedule_dims(&s, N, Hkv, topK, nblocks);
   msa::carve_schedule(&s, nullptr);
-  const size_t rows = static_cast<size_t>(s.cap_entries) * msa::kGroup;
+  const size_t rows = static_cast<size_t>(msa::part_rows(s.cap_entries));
   const size_t sched_bytes = round256(s.dev_bytes);
   const size_t part_bytes = round256(rows * msa::kHeadDim * 2);
   const size_t total = sched_bytes + part_bytes + rows * sizeof(float2);
