@@ -21,7 +21,7 @@
 // lanes 32 * (warp % 4) .. + 31, so a warpgroup covers all 128 rows):
 //   warp 0       scheduler, all 32 lanes: claims chunks, reads the next chunk's
 //                tile info and query ids ahead of time, gathers each tile's Q into Q
-//                stage t % 3 (three stages) once S(t - 3) has read it -- one TMA box per
+//                stage t % 4 (four stages) once S(t - 4) has read it -- one TMA box per
 //                query, the 16 heads of its group (4 KB bf16, 2 KB E4M3), landing in the
 //                128-byte-swizzled MMA layout through a 5-D (bf16) or 3-D (E4M3) view of
 //                Q -- and publishes each tile in a shared-memory ring for the other roles
@@ -29,20 +29,22 @@
 //                buffers and V_b into the V buffer (TMA; E4M3: V as f16, into the next of
 //                two V buffers); a ring slot is reused only after both this warp and
 //                the output warps have released it
-//   warp 1       TMEM allocation (512 columns: S[0], S[1], O[0], O[1]) and issue of
-//                S[s] = Q K^T (tcgen05, smem x smem) for tile t into stage s = t % 2
-//   warp 3       issue of O[s] = P V with P read from TMEM (it overwrites S[s] in
+//   warp 1       TMEM allocation (512 columns = four regions R0..R3 of 128) and issue of
+//                S = Q K^T (tcgen05, smem x smem) for tile t into region t % 4, once the
+//                output warps have read O of tile t - 3 from it
+//   warp 3       issue of O = P V into region (t + 3) % 4 -- where tile t - 1's P was --
+//                with P read from TMEM (it overwrites S of region t % 4 in
 //                place).  Two issuing threads: S of tile t + 1 never waits behind
 //                the P V of tile t (its softmax, or an E4M3 V block being widened)
-//   warps 4-7    softmax of even tiles (TMEM stage 0)
-//   warps 8-11   softmax of odd tiles  (TMEM stage 1)
+//   warps 4-7    softmax of even tiles
+//   warps 8-11   softmax of odd tiles
 //                (The Q gather used to be 16-byte cp.async copies issued by the softmax
 //                warpgroups after each softmax: the load/store unit throttled their
 //                issue to ~1.3 us per 32 KB tile, half of a warpgroup's time, while the
 //                partial stores went through the TMA unit.  The roles are now swapped:
 //                TMA carries the gather, the load/store unit the partial stores,
 //                0.554 -> 0.498 ms at M3.)
-//   warps 12-15  output: O[s] -> registers -> bf16 -> 16-byte global stores, no staging:
+//   warps 12-15  output: O -> registers -> bf16 -> 16-byte global stores, no staging:
 //                the partial workspace is chunk-major inside each aligned group of 8
 //                CSR positions (part_index), so the 32 rows a warp holds after one
 //                TMEM load (32 consecutive columns each) are stored as 512 contiguous
@@ -54,6 +56,16 @@
 // 176 for the softmax warpgroups (a row's 128 scores stay in registers), 88 for the
 // output warpgroup: 128*72 + 256*176 + 128*88 = 65536, the block's launch allocation
 // (512 x 128), so every increase can be granted.
+// TMEM rotation: a region serves tile t as S / P, then tile t + 1 as O, then tile t + 4 as S.
+// S of tile t therefore waits only for the output warps to have read O of tile t - 3, and
+// three tiles are between S and the reuse of its columns (with fixed S[2] / O[2] stages S
+// of tile t waited for P V of tile t - 2: the chain S -> softmax -> P V of one tile set the
+// pace of two).  P V of tile t writes over the P of tile t - 1, so it waits for that P V to
+// complete (the ordering PTX guarantees between pipelined MMAs of one thread covers a shared
+// accumulator, not a later MMA writing its accumulator over an earlier one's A operand, so the
+// wait is explicit; it costs nothing measurable, P of tile t comes much later).  Each barrier of the S / P / O chain has four slots, one
+// per region, so no waiter can fall a whole phase behind.  Measured at M3: 0.494 -> 0.479 ms
+// with four Q stages (three: 0.489).
 // A softmax thread owns one MMA row (TMEM lane): row maximum m (base-2 units,
 // scale folded in), P = 2^(s*scale*log2e - m) written back over S as bf16 pairs,
 // row sum l; (m, l) go to global as one float2 per row.
@@ -92,7 +104,10 @@ static_assert(kThreads == 512 && 128 * (kRegCtl + 2 * kRegSoftmax + kRegOut) <= 
               "setmaxnreg shares exceed the launch allocation");
 constexpr int kChunkTiles = 8;  // tiles per claimed chunk
 constexpr int kRing = 8;        // tile-info ring slots
-constexpr int kQStages = 3;
+constexpr int kQStages = 4;
+// TMEM: four regions of 128 columns.  Tile t computes S (and P over it) in region t % 4
+// and accumulates O in region (t + 3) % 4, the region tile t - 1's P occupied.
+constexpr int kRegions = 4;
 constexpr uint32_t kCtlBytes = 1024;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;  // a 16-bit 128 x 128 tile (two 16 KB halves)
 
@@ -114,9 +129,10 @@ static_assert(Lay<false>::kSmemBytes <= 232448 && Lay<true>::kSmemBytes <= 23244
 
 // barrier slots (8 bytes each) at the start of the control area
 enum {
-  B_QFULL0 = 0, B_KFULL0 = 3, B_KFREE0 = 5, B_VFULL0 = 7, B_VFREE0 = 9,  // slot 11 unused
-  B_SFULL0 = 12, B_PFULL0 = 14, B_PVDONE0 = 16, B_OFREE0 = 18, B_TFULL0 = 20, B_TEMPTY0 = 20 + kRing,
-  B_QFREE0 = 20 + 2 * kRing, B_COUNT = 20 + 2 * kRing + kQStages
+  B_QFULL0 = 0, B_KFULL0 = B_QFULL0 + kQStages, B_KFREE0 = B_KFULL0 + 2, B_VFULL0 = B_KFREE0 + 2,
+  B_VFREE0 = B_VFULL0 + 2, B_SFULL0 = B_VFREE0 + 2, B_PFULL0 = B_SFULL0 + kRegions, B_PVDONE0 = B_PFULL0 + kRegions,
+  B_OFREE0 = B_PVDONE0 + kRegions, B_TFULL0 = B_OFREE0 + kRegions, B_TEMPTY0 = B_TFULL0 + kRing,
+  B_QFREE0 = B_TEMPTY0 + kRing, B_COUNT = B_QFREE0 + kQStages
 };
 constexpr uint32_t kOffTmemSlot = 8 * B_COUNT;  // 4 bytes
 constexpr uint32_t kOffRing = 512;              // kRing entries of 64 bytes
@@ -293,10 +309,12 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_KFULL0 + s), 1);
       mbar_init(bar(B_KFREE0 + s), 1);
-      mbar_init(bar(B_SFULL0 + s), 1);
-      mbar_init(bar(B_PFULL0 + s), 128);
-      mbar_init(bar(B_PVDONE0 + s), 1);
-      mbar_init(bar(B_OFREE0 + s), 128);
+    }
+    for (int r = 0; r < kRegions; ++r) {
+      mbar_init(bar(B_SFULL0 + r), 1);
+      mbar_init(bar(B_PFULL0 + r), 128);
+      mbar_init(bar(B_PVDONE0 + r), 1);
+      mbar_init(bar(B_OFREE0 + r), 128);
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(bar(B_TFULL0 + r), 1);
@@ -391,7 +409,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
             const bool new_row = row != prev_row;
             const int kb = new_row ? (nk & 1) : ((nk - 1) & 1);
             {
-              // Q of this tile into stage it % 3 once S(it - 3) has read that stage: one TMA
+              // Q of this tile into stage it % 4 once S(it - 4) has read that stage: one TMA
               // box per query (its 16 heads, 4 KB bf16 / 2 KB E4M3), issued by lane j for
               // query j after lane 0 has armed the stage's barrier with the byte count
               const int qs = it % kQStages;
@@ -435,14 +453,14 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           if (!(ok = mbar_wait(bar(B_TFULL0 + slot), (it / kRing) & 1))) break;
           const int count = ring[slot].count, flags = ring[slot].flags;
           if (count == 0) break;
-          const int s = it & 1;
+          const int r = it & 3;  // TMEM region of this tile's S and P
           if (flags & 1) {
             // a new row: the previous row's K buffer is read no more once the S MMAs
             // issued so far are done
             if (++seg > 0) mma_commit(bar(B_KFREE0 + ((seg - 1) & 1)));
           }
-          // S[s] / P[s] is reused: P V of tile it-2 must have consumed P
-          if (it >= 2 && !(ok = mbar_wait(bar(B_PVDONE0 + s), ((it - 2) >> 1) & 1))) break;
+          // region r last held O of tile it - 3: the output warps must have read it
+          if (it >= 3 && !(ok = mbar_wait(bar(B_OFREE0 + ((it - 3) & 3)), ((it - 3) >> 2) & 1))) break;
           if ((flags & 1) && !(ok = mbar_wait(bar(B_KFULL0 + (seg & 1)), (seg >> 1) & 1))) break;
           const int qs = it % kQStages;
           if (!(ok = mbar_wait(bar(B_QFULL0 + qs), (it / kQStages) & 1))) break;
@@ -452,18 +470,18 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
             // E4M3: K = 128 bytes = one swizzle span, 32 elements per MMA
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_f8_ss(tmem + s * 128, smem_desc(qa + k * 32, 16, 1024, 2), smem_desc(ka + k * 32, 16, 1024, 2),
+              mma_f8_ss(tmem + r * 128, smem_desc(qa + k * 32, 16, 1024, 2), smem_desc(ka + k * 32, 16, 1024, 2),
                         idesc_qk, k > 0);
           } else {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               // Q: [query][8-head group][D half][8 rows][128 B] (8-row groups 2048 B apart,
               // D halves 1024 B apart); K: [D half][128 rows][128 B]
-              mma_f16_ss(tmem + s * 128, smem_desc(qa + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048, 2),
+              mma_f16_ss(tmem + r * 128, smem_desc(qa + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048, 2),
                          smem_desc(ka + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024, 2), idesc_qk, k > 0);
             }
           }
-          mma_commit(bar(B_SFULL0 + s));
+          mma_commit(bar(B_SFULL0 + r));
           mma_commit(bar(B_QFREE0 + qs));  // the scheduler may load tile it + 3's Q into this stage
         }
         if (!ok) flag_timeout(p.hdr);
@@ -532,22 +550,22 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           if (!(ok = mbar_wait(bar(B_TFULL0 + slot), (u / kRing) & 1))) break;
           const int count = ring[slot].count, flags = ring[slot].flags;
           if (count == 0) break;
-          const int s = u & 1;
+          const int r = u & 3, ro = (u + 3) & 3;  // P in region r, O into region ro
           if (flags & 1) {
             // a new row: the previous row's V buffer is free once the P V MMAs issued so far are done
             if (++vseg > 0) mma_commit(bar(B_VFREE0 + (vseg - 1) % L::kVBuf));
             if (!(ok = mbar_wait(bar(B_VFULL0 + vseg % L::kVBuf), (vseg / L::kVBuf) & 1))) break;
           }
-          if (!(ok = mbar_wait(bar(B_PFULL0 + s), (u >> 1) & 1))) break;
-          // O[s] is reused: the output warps must have read O of tile u-2
-          if (u >= 2 && !(ok = mbar_wait(bar(B_OFREE0 + s), ((u - 2) >> 1) & 1))) break;
+          if (!(ok = mbar_wait(bar(B_PFULL0 + r), (u >> 2) & 1))) break;
+          // O goes over the P of tile u - 1: its P V must have completed
+          if (u >= 1 && !(ok = mbar_wait(bar(B_PVDONE0 + ((u - 1) & 3)), ((u - 1) >> 2) & 1))) break;
           tc_fence_after();
           const uint32_t va = sb + L::kOffV + (vseg % L::kVBuf) * kTileBytes;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_f16_ts(tmem + 256 + s * 128, tmem + s * 128 + k * 8, smem_desc(va + k * 2048, 16384, 1024, 2),
+            mma_f16_ts(tmem + ro * 128, tmem + r * 128 + k * 8, smem_desc(va + k * 2048, 16384, 1024, 2),
                        idesc_pv, k > 0);
-          mma_commit(bar(B_PVDONE0 + s));
+          mma_commit(bar(B_PVDONE0 + r));
         }
         if (!ok) flag_timeout(p.hdr);
       }
@@ -557,7 +575,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
     // ------------------------------------------------------------ softmax
     const int wg = (warp - 4) >> 2;  // 0 or 1: the stage (tile parity) handled
     const int row = 32 * (warp & 3) + lane;
-    const uint32_t tS = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + wg * 128;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const bool neg = p.sl2 < 0.f;  // a negative scale turns the row maximum into a minimum
     // Each warp decides for itself (tcgen05.ld / st are warp-collective, not warpgroup-
     // collective): a bounded wait that expires in one warp ends that warp's loop, and the
@@ -579,9 +597,10 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       // (a row with lim >= 127 is unaffected by the masked path).
       const bool masked = __any_sync(0xffffffffu, lim < kBlock - 1);
 
-      ok = mbar_wait(bar(B_SFULL0 + wg), (it >> 1) & 1);
+      ok = mbar_wait(bar(B_SFULL0 + (it & 3)), (it >> 2) & 1);
       if (!__all_sync(0xffffffffu, ok)) { flag_timeout(p.hdr); break; }
       tc_fence_after();
+      const uint32_t tS = tmem + lane_base + (it & 3) * 128;
       uint32_t v[128];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
@@ -592,7 +611,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       else ml = softmax_row<false, kFp8>(v, lim, p.sl2, tS);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL0 + wg));
+      mbar_arrive(bar(B_PFULL0 + (it & 3)));
       if (valid) p.pstat[static_cast<size_t>(first) * kGroup + row] = ml;
     }
   } else {
@@ -611,12 +630,12 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       if (!named_bar_and(bar_id, 128, ok)) { flag_timeout(p.hdr); break; }
       const int count = ring[slot].count, first = ring[slot].first;
       if (count == 0) break;
-      const int s = it & 1;
-      ok = mbar_wait(bar(B_PVDONE0 + s), (it >> 1) & 1);
+      const int s = it & 3;
+      ok = mbar_wait(bar(B_PVDONE0 + s), (it >> 2) & 1);
       if (!named_bar_and(bar_id, 128, ok)) { flag_timeout(p.hdr); break; }
       if (elected) mbar_arrive(bar(B_TEMPTY0 + slot));
       tc_fence_after();
-      const uint32_t tO = tmem + lane_base + 256 + s * 128;
+      const uint32_t tO = tmem + lane_base + ((it + 3) & 3) * 128;
       const bool store = jr < count;
       uint4* dst = p.partial + part_index(static_cast<int64_t>(first) + jr, h, 0, kChunks);
 #pragma unroll
