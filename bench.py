@@ -31,6 +31,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+WINDOW = 2048  # queries per work-list window of the library
 METRIC = "sparse-attn fwd useful TFLOP/s and % HBM roofline, M3 shape top16, 1 GB300"
 METRIC_BWD = "sparse-attn bwd useful TFLOP/s (dQ, dK, dV; 2.5x the forward's nominal FLOPs), M3 shape top16, 1 GB300"
 
@@ -42,7 +43,7 @@ def kernels_per_step(cfg):
     segments, scatter + tiles in one launch) + kv_outer + combine + q_outer (the two
     attention kernels not chosen exit at once)."""
     rows, words = cfg.Hkv * cfg.nblocks, -(-cfg.N // 32)
-    nseg = -(-cfg.N // 256) * rows
+    nseg = -(-cfg.N // WINDOW) * rows
     if cfg.N * cfg.Hkv * cfg.topK <= 1024 and rows * words <= 8192 and words <= 64 and nseg <= 8192:
         return 1 + 3
     return (4 if nseg <= 32768 else 7) + 3

@@ -11,7 +11,7 @@
 //
 // Work unit (tile): up to 8 consecutive CSR entries of one (group g, block b) row,
 // i.e. 8 queries x 16 heads = 128 MMA rows (the head-packed "box" of one query is
-// 16 rows).  The schedule lists tiles window by window (256 queries per window).
+// 16 rows).  The schedule lists tiles window by window (2048 queries per window).
 // CTAs take chunks of 8 consecutive tiles from that list with one atomicAdd on a
 // per-launch counter: all CTAs move through the windows together (Q and K/V of the
 // current windows stay in L2) and a slow SM simply takes fewer chunks.  Each tile

@@ -13,7 +13,7 @@ constexpr int kHeadDim = 128;    // D
 constexpr int kGroup = 16;       // G = Hq / Hkv handled by the kernels
 constexpr int kTileQ = 8;        // queries per tile: 8 queries x 16 heads = 128 MMA rows
 constexpr int kChunk = 32;       // queries per bitmask word of the schedule
-constexpr int kWindow = 256;     // queries per work-list window (multiple of kChunk)
+constexpr int kWindow = 2048;    // queries per work-list window (multiple of kChunk)
 
 // Q-outer split units: at most this many splits per unit, and only while the units
 // number at most kQSplitMaxUnits (more units fill the GPU without splitting)

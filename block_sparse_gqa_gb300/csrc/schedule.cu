@@ -317,13 +317,16 @@ __global__ void __launch_bounds__(NT) k_seg_down(int32_t* __restrict__ seg, int6
   }
 }
 
-// Work-list tiles of the segments, CTA bid of nbid (256 threads).
+// Work-list tiles of the segments, CTA bid of nbid (256 threads): one warp per (window, row)
+// segment, its lanes writing the segment's tiles (a segment holds up to kWindow / kTileQ tiles)
 __device__ __forceinline__ void tiles_body(const int32_t* __restrict__ segoff, int64_t nseg, int R, int C,
                                            const int32_t* __restrict__ rowbase, const int32_t* __restrict__ offsets,
                                            int4* __restrict__ tiles, int bid, int nbid) {
   constexpr int kCpw = kWindow / kChunk;
-  for (int64_t s = bid * static_cast<int64_t>(kEntThreads) + threadIdx.x; s < nseg;
-       s += static_cast<int64_t>(nbid) * kEntThreads) {
+  constexpr int kWarps = kEntThreads / 32;
+  const int lane = threadIdx.x & 31;
+  for (int64_t s = bid * static_cast<int64_t>(kWarps) + (threadIdx.x >> 5); s < nseg;
+       s += static_cast<int64_t>(nbid) * kWarps) {
     const int t0 = segoff[s], n = segoff[s + 1] - t0;
     if (n == 0) continue;
     const int w = static_cast<int>(s / R), r = static_cast<int>(s % R);
@@ -331,7 +334,7 @@ __device__ __forceinline__ void tiles_body(const int32_t* __restrict__ segoff, i
     const int32_t* rb = rowbase + static_cast<size_t>(r) * (C + 1);
     const int first = offsets[r] + rb[cw0];
     const int cnt = rb[cw1] - rb[cw0];
-    for (int j = 0; j < n; ++j)
+    for (int j = lane; j < n; j += 32)
       tiles[t0 + j] = make_int4(r, first + kTileQ * j, min(kTileQ, cnt - kTileQ * j), w);
   }
 }
@@ -494,7 +497,7 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
     k_seg_top<1024><<<1, 1024, 0, st>>>(d.seg_sums, nb, d.segoff, s->nseg, d.window_tiles, s->nW, d.hdr);
     k_seg_down<256><<<nb, 256, 0, st>>>(d.segoff, s->nseg, d.seg_sums, s->R, d.window_tiles);
   }
-  const int tiles_grid = grid_for(s->nseg, kEntThreads, 1 << 16);
+  const int tiles_grid = grid_for(s->nseg, kEntThreads / 32, 1 << 16);  // a warp per segment
   k_scatter_tiles<<<ent_grid + tiles_grid, kEntThreads, 0, st>>>(
       indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C, lists_per_cta, ent_grid, d.mask, d.rowbase, d.offsets,
       d.qlist, d.slot, d.cmap, d.blist, d.segoff, s->nseg, s->R, d.tiles, d.hdr);

@@ -34,9 +34,9 @@
  *    LSE = -inf;
  *  - schedule rows are r = g * nblocks + b; each row lists its queries ascending,
  *    with the slot (list position) of the first occurrence of b in the query's list;
- *  - the work list cuts each row's entries per window of 256 query ids into tiles of
- *    at most 8 entries, listed window by window (the page's split rule is garbled;
- *    see oracle_worklist);
+ *  - the work list cuts each row's entries per window of query ids (2048 in the library;
+ *    a parameter here) into tiles of at most 8 entries, listed window by window (the
+ *    page's split rule is garbled; see oracle_worklist);
  *  - the dispatch threshold is stated at oracle_dispatch.
  *
  * Pins: every function here is checked by the CPU test suite against results fixed

@@ -104,8 +104,9 @@ def test_schedule_deterministic_and_reusable():
                                             (300, 2048, 1, 3), (1024, 1024, 1, 1)])
 def test_schedule_small_inputs_match_oracle(N, Lkv, Hkv, topK):
     """Tiny inputs (at most 1024 list slots and 8192 bitmask words) are scheduled by one
-    CTA; the shapes here sit on both sides of that limit (the last two: one CTA with 2
-    and 4 query windows), with pads, duplicates, future blocks and one invalid id."""
+    CTA; the shapes here sit on both sides of that limit, with pads, duplicates, future
+    blocks and one invalid id.  (Several query windows are exercised by the workloads of
+    test_schedule_matches_oracle: 4 at M3, 16 on the long workload, 32 at fp8.)"""
     rng = np.random.default_rng(N * 100 + topK)
     nb = Lkv // 128
     idx = rng.integers(-1, nb, size=(N, Hkv, topK)).astype(np.int32)

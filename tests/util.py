@@ -6,7 +6,7 @@ BF16_REL_L2 = 1e-2
 BF16_MAX_ABS = 2e-2
 LSE_MAX_ABS = 1e-3
 FP8_REL_L2 = 5e-2
-WINDOW = 256  # queries per work-list window of the library
+WINDOW = 2048  # queries per work-list window of the library
 TILE = 8      # CSR entries per tile
 
 
