@@ -167,6 +167,38 @@ __global__ void __launch_bounds__(NT) k_rowscan(const uint32_t* __restrict__ mas
   }
 }
 
+// k_rowscan for rows of at most 32 bitmask words (N <= 1024 queries: decode and
+// low-reuse sizes, where rows are many and short): one warp per row instead of a CTA.
+__global__ void __launch_bounds__(256) k_rowscan_warp(const uint32_t* __restrict__ mask, int R, int C, int nW,
+                                                      int32_t* __restrict__ rowbase, int32_t* __restrict__ counts,
+                                                      int32_t* __restrict__ segtiles) {
+  constexpr int kCpw = kWindow / kChunk;
+  const int lane = threadIdx.x & 31;
+  for (int64_t r = blockIdx.x * 8ll + (threadIdx.x >> 5); r < R; r += gridDim.x * 8ll) {
+    const int v = lane < C ? __popc(mask[r * C + lane]) : 0;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, inc, 31);
+    int32_t* rb = rowbase + r * (C + 1);
+    if (lane < C) rb[lane] = inc - v;
+    if (lane == 0) {
+      rb[C] = total;
+      counts[r] = total;
+    }
+    for (int w0 = 0; w0 < nW; w0 += 32) {  // warp-uniform trip count: the shuffles below
+      const int w = w0 + lane;
+      const int cw0 = min(w * kCpw, C), cw1 = min(cw0 + kCpw, C);
+      const int a = __shfl_sync(0xffffffffu, inc - v, cw0 & 31), b = __shfl_sync(0xffffffffu, inc - v, cw1 & 31);
+      const int e0 = cw0 >= C ? total : a, e1 = cw1 >= C ? total : b;
+      if (w < nW) segtiles[static_cast<size_t>(w) * R + r] = (e1 - e0 + kTileQ - 1) / kTileQ;
+    }
+  }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(NT) k_scan_rows(const int32_t* __restrict__ counts, int R, int N,
                                                   int32_t* __restrict__ offsets, SchedHeader* hdr) {
@@ -485,8 +517,12 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
   if ((e = cudaMemsetAsync(d.hdr, 0, sizeof(SchedHeader), st))) return e;
   k_mark<<<ent_grid, kEntThreads, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C, lists_per_cta,
                                             d.mask, d.hdr);
-  k_rowscan<256><<<grid_for(s->R, 1, 1 << 20), 256, 0, st>>>(d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
+  if (s->C <= 32)
+    k_rowscan_warp<<<grid_for(s->R, 8, 1 << 20), 256, 0, st>>>(d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
                                                              d.segoff);
+  else
+    k_rowscan<256><<<grid_for(s->R, 1, 1 << 20), 256, 0, st>>>(d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
+                                                               d.segoff);
   if (s->nseg <= 1024 * kSmallSegPer) {
     k_scan_small<1024><<<1, 1024, 0, st>>>(d.counts, s->R, s->N, d.offsets, d.segoff, static_cast<int>(s->nseg),
                                            d.window_tiles, s->nW, d.hdr);
