@@ -226,6 +226,61 @@ __global__ void __launch_bounds__(NT) k_scan_rows(const int32_t* __restrict__ co
   }
 }
 
+// Exclusive scan of in[0, n) into out (in place allowed) by one CTA of NT threads, in chunks
+// of NT * 8 elements staged in shared memory: coalesced loads and stores, a serial scan of 8
+// consecutive elements per thread (indices padded by one word per 32 against bank conflicts)
+// and one block scan per chunk.  Returns the total; *nz (if given) counts the nonzero inputs;
+// window_tiles (if given) receives out[q] for every q that is a multiple of R.
+constexpr int kScanItems = 8;
+template <int NT>
+__device__ int block_scan_array(const int32_t* in, int32_t* out, int n, int* sm, int* warp_buf, int* nz,
+                                int32_t* window_tiles, int R) {
+  constexpr int kCh = NT * kScanItems;
+  auto pad = [](int i) { return i + (i >> 5); };
+  const int t = threadIdx.x;
+  int carry = 0, nzc = 0;
+  for (int base = 0; base < n; base += kCh) {
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+      const int i = base + k * NT + t;
+      sm[pad(k * NT + t)] = i < n ? in[i] : 0;
+    }
+    __syncthreads();
+    int v[kScanItems], sum = 0;
+#pragma unroll
+    for (int j = 0; j < kScanItems; ++j) {
+      v[j] = sm[pad(t * kScanItems + j)];
+      sum += v[j];
+      nzc += v[j] > 0;
+    }
+    int total;
+    int run = carry + block_exclusive_scan<NT>(sum, &total, warp_buf);  // (its barriers order sm)
+#pragma unroll
+    for (int j = 0; j < kScanItems; ++j) {
+      sm[pad(t * kScanItems + j)] = run;
+      run += v[j];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+      const int i = base + k * NT + t;
+      if (i < n) {
+        const int e = sm[pad(k * NT + t)];
+        out[i] = e;
+        if (window_tiles && i % R == 0) window_tiles[i / R] = e;
+      }
+    }
+    carry += total;
+    __syncthreads();
+  }
+  if (nz) {
+    int nzt;
+    block_exclusive_scan<NT>(nzc, &nzt, warp_buf);
+    *nz = nzt;
+  }
+  return carry;
+}
+
 // Rows (as k_scan_rows) and, in the same CTA, the exclusive scan of the per-(window,
 // row) segment tile counts when there are few segments (at most NT * kSmallSegPer).
 constexpr int kSmallSegPer = 32;
@@ -233,45 +288,21 @@ constexpr int kSmallSegPer = 32;
 template <int NT>
 __device__ void scan_small_body(const int32_t* __restrict__ counts, int R, int N, int32_t* __restrict__ offsets,
                                 int32_t* __restrict__ seg, int nseg, int32_t* __restrict__ window_tiles, int nW,
-                                SchedHeader* hdr, int* warp_buf) {
-  {
-    const int per = (R + NT - 1) / NT;
-    const int r0 = min(static_cast<int>(threadIdx.x) * per, R), r1 = min(r0 + per, R);
-    int sum = 0, nz = 0;
-    for (int r = r0; r < r1; ++r) {
-      sum += counts[r];
-      nz += counts[r] > 0;
-    }
-    int total, nsb;
-    int run = block_exclusive_scan<NT>(sum, &total, warp_buf);
-    block_exclusive_scan<NT>(nz, &nsb, warp_buf);
-    for (int r = r0; r < r1; ++r) {
-      offsets[r] = run;
-      run += counts[r];
-    }
-    if (threadIdx.x == 0) {
-      offsets[R] = total;
-      hdr->entries = total;
-      hdr->nsb = nsb;
-      hdr->path = (static_cast<int64_t>(nsb) * 100 < static_cast<int64_t>(N) * 285) ? kPathKvOuter : kPathQOuter;
-    }
-  }
-  const int per = (nseg + NT - 1) / NT;
-  const int s0 = min(static_cast<int>(threadIdx.x) * per, nseg), s1 = min(s0 + per, nseg);
-  int sum = 0;
-  for (int q = s0; q < s1; ++q) sum += seg[q];
-  int total;
-  int run = block_exclusive_scan<NT>(sum, &total, warp_buf);
-  for (int q = s0; q < s1; ++q) {
-    const int v = seg[q];
-    seg[q] = run;
-    if (q % R == 0) window_tiles[q / R] = run;
-    run += v;
-  }
+                                SchedHeader* hdr, int* warp_buf, int* sm) {
+  int nsb = 0;
+  const int total = block_scan_array<NT>(counts, offsets, R, sm, warp_buf, &nsb, nullptr, R);
   if (threadIdx.x == 0) {
-    seg[nseg] = total;
-    window_tiles[nW] = total;
-    hdr->ntiles = total;
+    offsets[R] = total;
+    hdr->entries = total;
+    hdr->nsb = nsb;
+    // crossover: KV-outer when nsb / N < 2.85, in exact integers
+    hdr->path = (static_cast<int64_t>(nsb) * 100 < static_cast<int64_t>(N) * 285) ? kPathKvOuter : kPathQOuter;
+  }
+  const int tiles = block_scan_array<NT>(seg, seg, nseg, sm, warp_buf, nullptr, window_tiles, R);
+  if (threadIdx.x == 0) {
+    seg[nseg] = tiles;
+    window_tiles[nW] = tiles;
+    hdr->ntiles = tiles;
   }
 }
 
@@ -281,7 +312,8 @@ __global__ void __launch_bounds__(NT) k_scan_small(const int32_t* __restrict__ c
                                                    int nseg, int32_t* __restrict__ window_tiles, int nW,
                                                    SchedHeader* hdr) {
   __shared__ int warp_buf[32];
-  scan_small_body<NT>(counts, R, N, offsets, seg, nseg, window_tiles, nW, hdr, warp_buf);
+  __shared__ int sm[NT * kScanItems + NT * kScanItems / 32];
+  scan_small_body<NT>(counts, R, N, offsets, seg, nseg, window_tiles, nW, hdr, warp_buf, sm);
 }
 
 template <int NT>
@@ -413,6 +445,7 @@ k_schedule_one(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nb
                SchedDev d) {
   __shared__ int warp_buf[32];
   __shared__ int s_bad;
+  __shared__ int sm[kOneThreads * kScanItems + kOneThreads * kScanItems / 32];
   constexpr int kCpw = kWindow / kChunk;
   const int t = threadIdx.x;
   const int64_t nmask = static_cast<int64_t>(R) * C;
@@ -451,7 +484,7 @@ k_schedule_one(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nb
   }
   __syncthreads();
   const int nseg = nW * R;
-  scan_small_body<kOneThreads>(d.counts, R, N, d.offsets, d.segoff, nseg, d.window_tiles, nW, d.hdr, warp_buf);
+  scan_small_body<kOneThreads>(d.counts, R, N, d.offsets, d.segoff, nseg, d.window_tiles, nW, d.hdr, warp_buf, sm);
   __syncthreads();
   for (int64_t e = t; e < nslot; e += kOneThreads) {
     const int64_t L = e / topK;
