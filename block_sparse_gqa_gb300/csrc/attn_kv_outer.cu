@@ -275,6 +275,9 @@ template <bool kFp8, bool kF32P, bool kWithhold = false>
 __global__ void __launch_bounds__(kThreads, 1)
 kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const __grid_constant__ CUtensorMap tmQ, const KvParams p) {
+  griddep_wait();
+  // (no early griddep_launch: a combine grid left pending for the whole persistent run of
+  // this kernel cost 0.09 ms per M3 step; the combine is released when this grid ends)
   using L = Lay<kFp8>;
   const int path = p.force_path ? p.force_path : p.hdr->path;
   if (path != kPathKvOuter) return;
@@ -677,6 +680,8 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
 // per thread and step, read once (streaming), written as two 16-byte f16 chunks in order.
 __global__ void __launch_bounds__(256) widen_e4m3_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                                          int64_t n16) {
+  griddep_wait();
+  griddep_launch();
   for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n16; i += static_cast<int64_t>(gridDim.x) * 256) {
     const uint4 v = __ldcs(src + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -701,7 +706,7 @@ cudaError_t launch_widen_e4m3(const void* src, void* dst, int64_t n, cudaStream_
   int64_t grid = (n16 + 255) / 256;
   if (grid > sms * 8) grid = sms * 8;
   if (grid < 1) grid = 1;
-  widen_e4m3_kernel<<<static_cast<int>(grid), 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+  MSA_LAUNCH(widen_e4m3_kernel, static_cast<int>(grid), 256, 0, st, static_cast<const uint4*>(src), static_cast<uint4*>(dst),
                                                             n16);
   return cudaGetLastError();
 }
@@ -782,14 +787,14 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set[inst] = true;
   }
-  // the chunk counter this launch claims its work from starts at zero
-  cudaError_t e = cudaMemsetAsync(&s->d.hdr->pad[0], 0, sizeof(int32_t), st);
-  if (e != cudaSuccess) return e;
+  // the chunk counter this launch claims its work from is zero: the schedule build clears the
+  // header and the combine kernel that follows every launch of this kernel clears the counter
+  // again (a memset here would break the launch chain's programmatic dependency)
   // no more CTAs than work-list chunks can exist (decode sizes: a few; also makes the
   // launch cheap where the device picks the Q-outer path and this kernel exits at once)
   const int64_t max_chunks = (s->cap_tiles + kChunkTiles - 1) / kChunkTiles;
   const int grid = max_chunks < a.num_ctas ? static_cast<int>(max_chunks) : a.num_ctas;
-  kern<<<grid, kThreads, smem, st>>>(tmK, tmV, tmQ, p);
+  MSA_LAUNCH(kern, grid, kThreads, smem, st, tmK, tmV, tmQ, p);
   return cudaGetLastError();
 }
 

@@ -159,6 +159,8 @@ template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const QoParams p) {
+  griddep_wait();
+  griddep_launch();
   const int path = p.force_path ? p.force_path : p.hdr->path;
   if (path != kPathQOuter) return;
 
@@ -611,9 +613,9 @@ cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, 
   int64_t grid = sms;
   if (grid > units * splits) grid = units * splits;
   if (splits > 1)
-    q_outer_kernel<true><<<static_cast<int>(grid), kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, p);
+    MSA_LAUNCH(q_outer_kernel<true>, static_cast<int>(grid), kThreads, kSmemBytes, st, tmQ, tmK, tmV, p);
   else
-    q_outer_kernel<false><<<static_cast<int>(grid), kThreads, kSmemBytes, st>>>(tmQ, tmK, tmV, p);
+    MSA_LAUNCH(q_outer_kernel<false>, static_cast<int>(grid), kThreads, kSmemBytes, st, tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }
 

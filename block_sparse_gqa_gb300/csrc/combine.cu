@@ -74,7 +74,13 @@ __global__ void __launch_bounds__(kThreads, kF32 ? 3 : 4)
 combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ partial,
                const float2* __restrict__ pstat, int N, int Hkv, int topK, int Hq,
                __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, float v_descale,
-               const SchedHeader* __restrict__ hdr, int force_path) {
+               SchedHeader* __restrict__ hdr, int force_path) {
+  griddep_wait();
+  // (no early griddep_launch here: the Q-outer kernel after this one would then be scheduled
+  // beside running combine CTAs, and its ~210 KB of shared memory takes the L1 this kernel's
+  // gathers rely on -- 0.83 -> 0.92 ms per M3 step)
+  // the KV-outer launch before this one is complete: its chunk counter starts the next launch at zero
+  if (blockIdx.x == 0 && threadIdx.x == 0) hdr->pad[0] = 0;
   constexpr int kKChunk = kF32 ? 4 : 8;  // partial loads in flight per thread
   const int path = force_path ? force_path : hdr->path;
   if (path != kPathKvOuter) return;
@@ -163,11 +169,11 @@ cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, f
   int64_t grid = sms * 64;
   if (grid > units) grid = units;
   if (f32p)
-    combine_kernel<true><<<static_cast<int>(grid), kThreads, 0, st>>>(
+    MSA_LAUNCH(combine_kernel<true>, static_cast<int>(grid), kThreads, 0, st, 
         s->d.cmap, static_cast<const uint4*>(s->partial), s->pstat, s->N, s->Hkv, s->topK, Hq,
         static_cast<__nv_bfloat16*>(O), LSE, v_descale, s->d.hdr, force_path);
   else
-    combine_kernel<false><<<static_cast<int>(grid), kThreads, 0, st>>>(
+    MSA_LAUNCH(combine_kernel<false>, static_cast<int>(grid), kThreads, 0, st, 
         s->d.cmap, static_cast<const uint4*>(s->partial), s->pstat, s->N, s->Hkv, s->topK, Hq,
         static_cast<__nv_bfloat16*>(O), LSE, v_descale, s->d.hdr, force_path);
   return cudaGetLastError();

@@ -1,12 +1,40 @@
 // Internal declarations shared by the libmsa translation units.
 #pragma once
 #include <cstdint>
+#include <utility>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "msa.h"
 
 namespace msa {
+
+// Launch with a programmatic dependency on the previous work in the stream (the kernel
+// must start with griddep_wait(); see ptx.cuh).  After a non-kernel stream operation the
+// launch is simply ordered after it.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// launch_pdl inside a function returning cudaError_t: returns the launch error, if any
+#define MSA_LAUNCH(...)                                               \
+  do {                                                                \
+    const cudaError_t launch_err_ = ::msa::launch_pdl(__VA_ARGS__);   \
+    if (launch_err_ != cudaSuccess) return launch_err_;               \
+  } while (0)
 
 constexpr int kBlock = 128;      // tokens per KV block
 constexpr int kHeadDim = 128;    // D

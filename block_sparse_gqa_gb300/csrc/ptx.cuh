@@ -64,6 +64,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// The forward's kernels are launched with a programmatic dependency on the kernel before them,
+// so a kernel's CTAs can be scheduled while its predecessor still runs.  Every such kernel
+// starts with griddep_wait() -- which returns once the preceding grid has completed and its
+// writes are visible (at once for a launch without the dependency) -- before it reads any
+// input or exits, so completion stays ordered along the whole chain; griddep_launch() then
+// lets the next kernel be scheduled.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");

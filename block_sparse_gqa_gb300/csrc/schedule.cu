@@ -130,6 +130,8 @@ __device__ __forceinline__ void entries_body(const int32_t* __restrict__ idx, in
 __global__ void __launch_bounds__(kEntThreads)
 k_mark(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int C, int lists_per_cta,
        uint32_t* __restrict__ mask, SchedHeader* hdr) {
+  griddep_wait();
+  griddep_launch();
   entries_body<false>(idx, N, Hkv, topK, nblocks, Lkv, C, lists_per_cta, mask, nullptr, nullptr, nullptr, nullptr,
                       nullptr, nullptr, hdr, blockIdx.x, gridDim.x);
 }
@@ -138,6 +140,8 @@ template <int NT>
 __global__ void __launch_bounds__(NT) k_rowscan(const uint32_t* __restrict__ mask, int R, int C, int nW,
                                                 int32_t* __restrict__ rowbase, int32_t* __restrict__ counts,
                                                 int32_t* __restrict__ segtiles) {
+  griddep_wait();
+  griddep_launch();
   __shared__ int warp_buf[32];
   constexpr int kCpw = kWindow / kChunk;
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
@@ -172,6 +176,8 @@ __global__ void __launch_bounds__(NT) k_rowscan(const uint32_t* __restrict__ mas
 __global__ void __launch_bounds__(256) k_rowscan_warp(const uint32_t* __restrict__ mask, int R, int C, int nW,
                                                       int32_t* __restrict__ rowbase, int32_t* __restrict__ counts,
                                                       int32_t* __restrict__ segtiles) {
+  griddep_wait();
+  griddep_launch();
   constexpr int kCpw = kWindow / kChunk;
   const int lane = threadIdx.x & 31;
   for (int64_t r = blockIdx.x * 8ll + (threadIdx.x >> 5); r < R; r += gridDim.x * 8ll) {
@@ -202,6 +208,8 @@ __global__ void __launch_bounds__(256) k_rowscan_warp(const uint32_t* __restrict
 template <int NT>
 __global__ void __launch_bounds__(NT) k_scan_rows(const int32_t* __restrict__ counts, int R, int N,
                                                   int32_t* __restrict__ offsets, SchedHeader* hdr) {
+  griddep_wait();
+  griddep_launch();
   __shared__ int warp_buf[32];
   const int per = (R + NT - 1) / NT;
   const int r0 = min(static_cast<int>(threadIdx.x) * per, R), r1 = min(r0 + per, R);
@@ -311,6 +319,8 @@ __global__ void __launch_bounds__(NT) k_scan_small(const int32_t* __restrict__ c
                                                    int32_t* __restrict__ offsets, int32_t* __restrict__ seg,
                                                    int nseg, int32_t* __restrict__ window_tiles, int nW,
                                                    SchedHeader* hdr) {
+  griddep_wait();
+  griddep_launch();
   __shared__ int warp_buf[32];
   __shared__ int sm[NT * kScanItems + NT * kScanItems / 32];
   scan_small_body<NT>(counts, R, N, offsets, seg, nseg, window_tiles, nW, hdr, warp_buf, sm);
@@ -319,6 +329,8 @@ __global__ void __launch_bounds__(NT) k_scan_small(const int32_t* __restrict__ c
 template <int NT>
 __global__ void __launch_bounds__(NT) k_seg_reduce(const int32_t* __restrict__ seg, int64_t nseg,
                                                    int32_t* __restrict__ sums) {
+  griddep_wait();
+  griddep_launch();
   __shared__ int warp_buf[32];
   constexpr int per = kSegScanBlock / NT;
   const int64_t s0 = static_cast<int64_t>(blockIdx.x) * kSegScanBlock + threadIdx.x * per;
@@ -334,6 +346,8 @@ template <int NT>
 __global__ void __launch_bounds__(NT) k_seg_top(int32_t* __restrict__ sums, int nb, int32_t* __restrict__ segoff,
                                                 int64_t nseg, int32_t* __restrict__ window_tiles, int nW,
                                                 SchedHeader* hdr) {
+  griddep_wait();
+  griddep_launch();
   __shared__ int warp_buf[32];
   const int per = (nb + NT - 1) / NT;
   const int b0 = min(static_cast<int>(threadIdx.x) * per, nb), b1 = min(b0 + per, nb);
@@ -358,6 +372,8 @@ template <int NT>
 __global__ void __launch_bounds__(NT) k_seg_down(int32_t* __restrict__ seg, int64_t nseg,
                                                  const int32_t* __restrict__ sums, int R,
                                                  int32_t* __restrict__ window_tiles) {
+  griddep_wait();
+  griddep_launch();
   __shared__ int warp_buf[32];
   constexpr int per = kSegScanBlock / NT;
   const int64_t s0 = static_cast<int64_t>(blockIdx.x) * kSegScanBlock + threadIdx.x * per;
@@ -412,6 +428,8 @@ k_scatter_tiles(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int n
                 int32_t* __restrict__ qlist, int32_t* __restrict__ slot, int32_t* __restrict__ cmap,
                 int32_t* __restrict__ blist, const int32_t* __restrict__ segoff, int64_t nseg, int R,
                 int4* __restrict__ tiles, SchedHeader* hdr) {
+  griddep_wait();
+  griddep_launch();
   const int b = blockIdx.x;
   if (b < ent_grid)
     entries_body<true>(idx, N, Hkv, topK, nblocks, Lkv, C, lists_per_cta, const_cast<uint32_t*>(mask), rowbase,
@@ -443,6 +461,8 @@ __device__ __forceinline__ bool slot_entry(const int32_t* __restrict__ lst, int 
 __global__ void __launch_bounds__(kOneThreads, 1)
 k_schedule_one(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int R, int C, int nW,
                SchedDev d) {
+  griddep_wait();
+  griddep_launch();
   __shared__ int warp_buf[32];
   __shared__ int s_bad;
   __shared__ int sm[kOneThreads * kScanItems + kOneThreads * kScanItems / 32];
@@ -543,31 +563,31 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
   // tiny inputs: one CTA (limits keep its serial per-thread loops short)
   if (nl * s->topK <= kOneMaxSlots && static_cast<int64_t>(s->R) * s->C <= kOneMaxMaskWords && s->C <= 64 &&
       s->nseg <= kOneMaxSegments) {
-    k_schedule_one<<<1, kOneThreads, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->R, s->C, s->nW, d);
+    MSA_LAUNCH(k_schedule_one, 1, kOneThreads, 0, st, indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->R, s->C, s->nW, d);
     return cudaGetLastError();
   }
   if ((e = cudaMemsetAsync(d.mask, 0, sizeof(uint32_t) * static_cast<size_t>(s->R) * s->C, st))) return e;
   if ((e = cudaMemsetAsync(d.hdr, 0, sizeof(SchedHeader), st))) return e;
-  k_mark<<<ent_grid, kEntThreads, 0, st>>>(indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C, lists_per_cta,
+  MSA_LAUNCH(k_mark, ent_grid, kEntThreads, 0, st, indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C, lists_per_cta,
                                             d.mask, d.hdr);
   if (s->C <= 32)
-    k_rowscan_warp<<<grid_for(s->R, 8, 1 << 20), 256, 0, st>>>(d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
+    MSA_LAUNCH(k_rowscan_warp, grid_for(s->R, 8, 1 << 20), 256, 0, st, d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
                                                              d.segoff);
   else
-    k_rowscan<256><<<grid_for(s->R, 1, 1 << 20), 256, 0, st>>>(d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
+    MSA_LAUNCH(k_rowscan<256>, grid_for(s->R, 1, 1 << 20), 256, 0, st, d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
                                                                d.segoff);
   if (s->nseg <= 1024 * kSmallSegPer) {
-    k_scan_small<1024><<<1, 1024, 0, st>>>(d.counts, s->R, s->N, d.offsets, d.segoff, static_cast<int>(s->nseg),
+    MSA_LAUNCH(k_scan_small<1024>, 1, 1024, 0, st, d.counts, s->R, s->N, d.offsets, d.segoff, static_cast<int>(s->nseg),
                                            d.window_tiles, s->nW, d.hdr);
   } else {
-    k_scan_rows<1024><<<1, 1024, 0, st>>>(d.counts, s->R, s->N, d.offsets, d.hdr);
+    MSA_LAUNCH(k_scan_rows<1024>, 1, 1024, 0, st, d.counts, s->R, s->N, d.offsets, d.hdr);
     const int nb = static_cast<int>(s->nseg_blocks);
-    k_seg_reduce<256><<<nb, 256, 0, st>>>(d.segoff, s->nseg, d.seg_sums);
-    k_seg_top<1024><<<1, 1024, 0, st>>>(d.seg_sums, nb, d.segoff, s->nseg, d.window_tiles, s->nW, d.hdr);
-    k_seg_down<256><<<nb, 256, 0, st>>>(d.segoff, s->nseg, d.seg_sums, s->R, d.window_tiles);
+    MSA_LAUNCH(k_seg_reduce<256>, nb, 256, 0, st, d.segoff, s->nseg, d.seg_sums);
+    MSA_LAUNCH(k_seg_top<1024>, 1, 1024, 0, st, d.seg_sums, nb, d.segoff, s->nseg, d.window_tiles, s->nW, d.hdr);
+    MSA_LAUNCH(k_seg_down<256>, nb, 256, 0, st, d.segoff, s->nseg, d.seg_sums, s->R, d.window_tiles);
   }
   const int tiles_grid = grid_for(s->nseg, kEntThreads / 32, 1 << 16);  // a warp per segment
-  k_scatter_tiles<<<ent_grid + tiles_grid, kEntThreads, 0, st>>>(
+  MSA_LAUNCH(k_scatter_tiles, ent_grid + tiles_grid, kEntThreads, 0, st, 
       indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C, lists_per_cta, ent_grid, d.mask, d.rowbase, d.offsets,
       d.qlist, d.slot, d.cmap, d.blist, d.segoff, s->nseg, s->R, d.tiles, d.hdr);
   return cudaGetLastError();
