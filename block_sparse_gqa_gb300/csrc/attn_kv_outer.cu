@@ -679,9 +679,11 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
 // E4M3 -> f16, elementwise and exact (every E4M3 value is an f16 value): 16 source bytes
 // per thread and step, read once (streaming), written as two 16-byte f16 chunks in order.
 __global__ void __launch_bounds__(256) widen_e4m3_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                                         int64_t n16) {
+                                                         int64_t n16, const SchedHeader* __restrict__ hdr,
+                                                         int force_path) {
   griddep_wait();
   griddep_launch();
+  if ((force_path ? force_path : hdr->path) != kPathKvOuter) return;  // only the KV-outer kernel reads the copy
   for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n16; i += static_cast<int64_t>(gridDim.x) * 256) {
     const uint4 v = __ldcs(src + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -698,7 +700,8 @@ __global__ void __launch_bounds__(256) widen_e4m3_kernel(const uint4* __restrict
 
 }  // namespace
 
-cudaError_t launch_widen_e4m3(const void* src, void* dst, int64_t n, cudaStream_t st) {
+cudaError_t launch_widen_e4m3(const void* src, void* dst, int64_t n, const SchedHeader* hdr, int force_path,
+                              cudaStream_t st) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -707,11 +710,12 @@ cudaError_t launch_widen_e4m3(const void* src, void* dst, int64_t n, cudaStream_
   if (grid > sms * 8) grid = sms * 8;
   if (grid < 1) grid = 1;
   MSA_LAUNCH(widen_e4m3_kernel, static_cast<int>(grid), 256, 0, st, static_cast<const uint4*>(src), static_cast<uint4*>(dst),
-                                                            n16);
+             n16, hdr, force_path);
   return cudaGetLastError();
 }
 
 cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
+  if (a.force_path == kPathQOuter) return cudaSuccess;  // (the kernel would exit at once)
   const msa_schedule* s = a.s;
   const bool fp8 = a.fp8;
   const uint64_t es = fp8 ? 1 : 2;  // bytes per input element

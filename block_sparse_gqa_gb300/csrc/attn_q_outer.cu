@@ -1,4 +1,5 @@
-// Q-outer (query-stationary) attention, bf16, tcgen05 + TMA: the low-reuse fallback.
+// Q-outer (query-stationary) attention, bf16 or fp8 E4M3, tcgen05 + TMA: the low-reuse
+// fallback.
 //
 // "Kernel optimization for MiniMax M3 on NVIDIA Blackwell", Q-outer vs KV-outer
 // section: when nsb / N >= 2.85 (few queries share a block) each query walks its own
@@ -31,6 +32,13 @@
 //                running output o[h] (its column d) rescaled by 2^(m_old - m_new)
 // The causal limit only matters in the query's own block (keys > pos(i) get p = 0).
 //
+// E4M3 inputs (per-tensor descales): S^T on kind::f8f6f4 (K-major, 32 elements per MMA),
+// q and k descales folded into the softmax scale; V arrives as E4M3 and the softmax warps
+// widen it (exact) into one of two f16 buffers in the bf16 V layout at the start of the
+// block, while S is computed; P^T is written as f16 and P V runs on f16; the v descale
+// scales the output.  (A whole-tensor f16 copy of V, as the KV-outer path uses, would
+// double the V bytes of a low-reuse call.)
+//
 // Few units (decode-size N): each unit's list is split into S contiguous chunks of its
 // valid blocks, and a work item is (unit, chunk), so that up to S times more SMs work.
 // An item ends with its unnormalised output o (fp32 [16 heads][128]) and (m, l) per
@@ -40,6 +48,7 @@
 // denominator).  The merge order is fixed, so results do not depend on timing.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "msa_internal.h"
 #include "ptx.cuh"
@@ -49,14 +58,23 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kSlots = 6;                // K/V ring: K of item x in slot 2x % 6, V in slot (2x + 1) % 6
-constexpr uint32_t kSlotBytes = 32768;   // one 128 x 128 bf16 block
-constexpr uint32_t kOffKV = 0;
-constexpr uint32_t kOffQ = kSlots * kSlotBytes;  // 2 x 4 KB
-constexpr uint32_t kOffP = kOffQ + 8192;           // 4 KB
-constexpr uint32_t kOffRed = kOffP + 4096;         // [max, sum][2 blocks][16 heads][4 warps] floats
-constexpr uint32_t kOffCtl = kOffRed + 1024;
-constexpr uint32_t kSmemBytes = kOffCtl + 256 + 1024;
 constexpr uint32_t kTmemCols = 64;
+constexpr uint32_t kVhBytes = 32768;     // one 128 x 128 block of 16-bit V
+
+// Shared-memory layout per input type.  E4M3: 16 KB ring slots (one E4M3 block) and two
+// f16 V blocks, into which the softmax warps widen each block's V for the P V MMA.
+template <bool kFp8>
+struct QoLay {
+  static constexpr uint32_t kSlot = kFp8 ? 16384 : 32768;  // one 128 x 128 K or V block as loaded
+  static constexpr uint32_t kOffKV = 0;
+  static constexpr uint32_t kOffVh = kSlots * kSlot;
+  static constexpr uint32_t kOffQ = kOffVh + (kFp8 ? 2 * kVhBytes : 0);  // 2 x 4 KB
+  static constexpr uint32_t kOffP = kOffQ + 8192;                        // 4 KB
+  static constexpr uint32_t kOffRed = kOffP + 4096;  // [max, sum][2 blocks][16 heads][4 warps] floats
+  static constexpr uint32_t kOffCtl = kOffRed + 1024;
+  static constexpr uint32_t kSmemBytes = kOffCtl + 256 + 1024;
+};
+static_assert(QoLay<false>::kSmemBytes <= 232448 && QoLay<true>::kSmemBytes <= 232448, "shared memory");
 
 enum {
   B_FULL0 = 0, B_EMPTY0 = 6, B_QFULL0 = 12, B_QEMPTY0 = 14, B_SFULL0 = 16, B_SFREE0 = 18, B_PREADY = 20,
@@ -72,7 +90,8 @@ struct QoParams {
   __nv_bfloat16* O;
   float* LSE;
   int N, Lkv, Hq, Hkv, topK, nblocks;
-  float sl2;  // scale * log2(e)
+  float sl2;  // scale * log2(e) (E4M3: * q descale * k descale)
+  float v_descale;  // E4M3: the output's factor (1 for bf16)
   int force_path;
   int splits;       // chunks per unit (1: no splitting)
   float* qs_o;      // [items][16][128] partial outputs (splits > 1)
@@ -153,9 +172,32 @@ __device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
   return op(d, __shfl_xor_sync(0xffffffffu, d, 1));
 }
 
+// E4M3 V block (TMA layout: 128 keys x 128 bytes, 16-byte chunks swizzled by key % 8) -> f16
+// in the layout the bf16 P V MMA reads ([key / 8][d / 64][key % 8][64], 128-byte swizzle).
+// Thread `key` converts its key's row (exact: every E4M3 value is an f16 value).
+__device__ __forceinline__ void widen_v_row(const uint8_t* src, uint8_t* dst, int key) {
+  const uint8_t* row = src + key * 128;
+  uint8_t* base = dst + (key >> 3) * 2048 + (key & 7) * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {  // d = 16 j .. 16 j + 15
+    const uint4 w = *reinterpret_cast<const uint4*>(row + ((j ^ (key & 7)) << 4));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * q]) : "h"(static_cast<uint16_t>(ws[q] & 0xFFFFu)));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * q + 1]) : "h"(static_cast<uint16_t>(ws[q] >> 16)));
+    }
+    uint8_t* half = base + (j >> 2) * 1024;
+    const int c0 = (2 * j) & 7;
+    *reinterpret_cast<uint4*>(half + ((c0 ^ (key & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(half + (((c0 + 1) ^ (key & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
 // kSplit: the instance for split units (p.splits > 1); the other one is the plain
-// per-unit kernel (p.splits is 1 there and never read)
-template <bool kSplit>
+// per-unit kernel (p.splits is 1 there and never read).  kFp8: E4M3 Q / K / V.
+template <bool kSplit, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
 q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const QoParams p) {
@@ -163,15 +205,16 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   griddep_launch();
   const int path = p.force_path ? p.force_path : p.hdr->path;
   if (path != kPathQOuter) return;
+  using L = QoLay<kFp8>;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_u & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   const uint32_t sb = raw_u + pad;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffCtl);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffCtl + 8 * B_COUNT);
-  float* red = reinterpret_cast<float*>(smem + kOffRed);  // [2][4 warps][16 heads]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffCtl);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffCtl + 8 * B_COUNT);
+  float* red = reinterpret_cast<float*>(smem + L::kOffRed);  // [2][4 warps][16 heads]
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -228,10 +271,16 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         // Q buffer qb was last read by the S MMAs of unit nu - 2
         if (nu >= 2) ok = mbar_wait(bar(B_QEMPTY0 + qb), ((nu >> 1) - 1) & 1);
         if (ok) {
-          const uint32_t dq = sb + kOffQ + qb * 4096;
-          mbar_expect_tx(bar(B_QFULL0 + qb), 4096);
-          tma_load_3d(dq, &tmQ, 0, g * kGroup, i, bar(B_QFULL0 + qb), pol);
-          tma_load_3d(dq + 2048, &tmQ, 64, g * kGroup, i, bar(B_QFULL0 + qb), pol);
+          const uint32_t dq = sb + L::kOffQ + qb * 4096;
+          if constexpr (kFp8) {
+            // E4M3: the 16 heads' 128-byte rows in one box
+            mbar_expect_tx(bar(B_QFULL0 + qb), 2048);
+            tma_load_3d(dq, &tmQ, 0, g * kGroup, i, bar(B_QFULL0 + qb), pol);
+          } else {
+            mbar_expect_tx(bar(B_QFULL0 + qb), 4096);
+            tma_load_3d(dq, &tmQ, 0, g * kGroup, i, bar(B_QFULL0 + qb), pol);
+            tma_load_3d(dq + 2048, &tmQ, 64, g * kGroup, i, bar(B_QFULL0 + qb), pol);
+          }
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -248,8 +297,11 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             if (n >= kSlots) ok = mbar_wait(bar(B_EMPTY0 + sl), ((n / kSlots) - 1) & 1);
             if (ok) {
               const uint32_t fb = bar(B_FULL0 + sl);
-              mbar_expect_tx(fb, kSlotBytes);
-              tma_load_5d(sb + kOffKV + sl * kSlotBytes, t ? &tmV : &tmK, 0, 0, 0, g, b * (kBlock / 8), fb, pol_kv);
+              mbar_expect_tx(fb, L::kSlot);
+              if constexpr (kFp8)  // 128 keys x 128 bytes
+                tma_load_3d(sb + L::kOffKV + sl * L::kSlot, t ? &tmV : &tmK, 0, g, b * kBlock, fb, pol_kv);
+              else
+                tma_load_5d(sb + L::kOffKV + sl * L::kSlot, t ? &tmV : &tmK, 0, 0, 0, g, b * (kBlock / 8), fb, pol_kv);
             }
           }
         }
@@ -261,24 +313,26 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     // S^T: M 128 keys, N 16 heads, both operands K-major (128-byte swizzle)
-    constexpr uint32_t idesc_s = idesc_f16(128, 16, 1, 1, 0, 0);
-    // O^T: M 128 (D), N 16 heads; A = V_b read MN-major, B = P^T K-major
-    constexpr uint32_t idesc_o = idesc_f16(128, 16, 1, 1, 1, 0);
+    constexpr uint32_t idesc_s = kFp8 ? idesc_f8(128, 16, 0, 0) : idesc_f16(128, 16, 1, 1, 0, 0);
+    // O^T: M 128 (D), N 16 heads; A = V_b read MN-major, B = P^T K-major (E4M3: both f16)
+    constexpr uint32_t idesc_o = kFp8 ? idesc_f16(128, 16, 0, 0, 1, 0) : idesc_f16(128, 16, 1, 1, 1, 0);
     bool ok = true;
     int item = 0, nu = 0, pending = -1;
     auto issue_pv = [&](int x) -> bool {
       const int vn = 2 * x + 1, vs = vn % kSlots;
-      if (!mbar_wait(bar(B_FULL0 + vs), (vn / kSlots) & 1)) return false;
+      // (E4M3: the softmax warps waited for the slot, widened it, and are done with it)
+      if (!kFp8 && !mbar_wait(bar(B_FULL0 + vs), (vn / kSlots) & 1)) return false;
       if (!mbar_wait(bar(B_PREADY), x & 1)) return false;
       tc_fence_after();
-      const uint32_t va = sb + kOffKV + vs * kSlotBytes;
-      const uint32_t pa = sb + kOffP;
+      if constexpr (kFp8) mbar_arrive(bar(B_EMPTY0 + vs));
+      const uint32_t va = kFp8 ? sb + L::kOffVh + (x & 1) * kVhBytes : sb + L::kOffKV + vs * L::kSlot;
+      const uint32_t pa = sb + L::kOffP;
 #pragma unroll
       for (int k = 0; k < 8; ++k)
         mma_f16_ss(tmem + 32, smem_desc(va + k * 4096, 1024, 2048, 2),
                    smem_desc(pa + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024, 2), idesc_o, k > 0);
       mma_commit(bar(B_PVDONE));
-      mma_commit(bar(B_EMPTY0 + vs));
+      if constexpr (!kFp8) mma_commit(bar(B_EMPTY0 + vs));
       return true;
     };
     for (int64_t x = blockIdx.x; x < nitems && ok; x += gridDim.x) {
@@ -298,11 +352,19 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           // S[s] is reused: the softmax warps must have read S of item - 2
           if (item >= 2 && !(ok = mbar_wait(bar(B_SFREE0 + s), ((item >> 1) - 1) & 1))) break;
           tc_fence_after();
-          const uint32_t ka = sb + kOffKV + ks * kSlotBytes, qa = sb + kOffQ + qb * 4096;
+          const uint32_t ka = sb + L::kOffKV + ks * L::kSlot, qa = sb + L::kOffQ + qb * 4096;
+          if constexpr (kFp8) {
+            // E4M3: a row is one 128-byte swizzle span, 32 elements per MMA
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ss(tmem + s * 16, smem_desc(ka + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048, 2),
-                       smem_desc(qa + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024, 2), idesc_s, kk > 0);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f8_ss(tmem + s * 16, smem_desc(ka + kk * 32, 16, 1024, 2), smem_desc(qa + kk * 32, 16, 1024, 2),
+                        idesc_s, kk > 0);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16_ss(tmem + s * 16, smem_desc(ka + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048, 2),
+                         smem_desc(qa + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024, 2), idesc_s, kk > 0);
+          }
           mma_commit(bar(B_SFULL0 + s));
           mma_commit(bar(B_EMPTY0 + ks));
           if (k == k_hi - 1) mma_commit(bar(B_QEMPTY0 + qb));
@@ -324,8 +386,8 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const float kLn2 = 0.6931471805599453f;
     bool ok = true;
     int item = 0;
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + kOffCtl + 192);
-    float* mscr = reinterpret_cast<float*>(smem + kOffP);  // merge scratch (P is free then)
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::kOffCtl + 192);
+    float* mscr = reinterpret_cast<float*>(smem + L::kOffP);  // merge scratch (P is free then)
     static_assert((3 * kQSplitMax + 2) * kGroup * 4 <= 4096, "merge scratch");
     // split item x of unit u done: store its partial; the last of the unit's chunks merges
     auto finish_split = [&](int64_t x, int64_t u, __nv_bfloat16* Orow, float* lse_out, const float (&m)[kGroup],
@@ -393,13 +455,13 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
           for (int sp = 0; sp < kQSplitMax; ++sp)
             if (sp < S) acc = fmaf(ww[sp * kGroup + h], v[hh][sp], acc);
-          const float L = LL[h];
-          Orow[h * kHeadDim + key] = __float2bfloat16(L > 0.f ? acc / L : 0.f);
+          const float Lh = LL[h];
+          Orow[h * kHeadDim + key] = __float2bfloat16(Lh > 0.f ? p.v_descale * acc / Lh : 0.f);
         }
       }
       if (lse_out && key < kGroup) {
-        const float L = LL[key];
-        lse_out[key] = L > 0.f ? (MM[key] + lg2(L)) * kLn2 : -INFINITY;
+        const float Lk = LL[key];
+        lse_out[key] = Lk > 0.f ? (MM[key] + lg2(Lk)) * kLn2 : -INFINITY;
       }
     };
     for (int64_t x = blockIdx.x; x < nitems; x += gridDim.x) {
@@ -435,6 +497,14 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       for (int k = k_lo; k < k_hi; ++k, ++item) {
         const int b = block_at(mine, k);
         const int s = item & 1;
+        if constexpr (kFp8) {
+          // this block's V (E4M3) -> f16 buffer item % 2, whose last reader, the P V of item - 2,
+          // completed before the P V of item - 1 this warpgroup has already waited for
+          const int vn = 2 * item + 1, vs = vn % kSlots;
+          ok = mbar_wait(bar(B_FULL0 + vs), (vn / kSlots) & 1);
+          if (!named_bar_and(bar_id, 128, ok)) { ok = false; break; }
+          widen_v_row(smem + L::kOffKV + vs * L::kSlot, smem + L::kOffVh + (item & 1) * kVhBytes, key);
+        }
         ok = mbar_wait(bar(B_SFULL0 + s), (item >> 1) & 1);
         if (!named_bar_and(bar_id, 128, ok)) { ok = false; break; }
         tc_fence_after();
@@ -491,10 +561,13 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         // 64-127 in two 2 KB halves of 16 rows
         {
           const int half = key >> 6, kk = key & 63;
-          uint8_t* pb = smem + kOffP + half * 2048 + (kk & 7) * 2;
+          uint8_t* pb = smem + L::kOffP + half * 2048 + (kk & 7) * 2;
 #pragma unroll
           for (int h = 0; h < kGroup; ++h)
-            *reinterpret_cast<__nv_bfloat16*>(pb + h * 128 + (((kk >> 3) ^ (h & 7)) << 4)) = __float2bfloat16(pv[h]);
+            if constexpr (kFp8)  // f16 P for the f16 V
+              *reinterpret_cast<__half*>(pb + h * 128 + (((kk >> 3) ^ (h & 7)) << 4)) = __float2half_rn(pv[h]);
+            else
+              *reinterpret_cast<__nv_bfloat16*>(pb + h * 128 + (((kk >> 3) ^ (h & 7)) << 4)) = __float2bfloat16(pv[h]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -515,7 +588,7 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         finish_split(x, u, Orow, lse_out, m, l, o);
       } else {
 #pragma unroll
-        for (int h = 0; h < kGroup; ++h) Orow[h * kHeadDim + key] = __float2bfloat16(o[h] / l[h]);
+        for (int h = 0; h < kGroup; ++h) Orow[h * kHeadDim + key] = __float2bfloat16(p.v_descale * o[h] / l[h]);
         if (lse_out && key < kGroup) {
           float mk = m[0], lk = l[0];
 #pragma unroll
@@ -540,12 +613,29 @@ q_outer_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 }  // namespace
 
 cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, const void* V, int Hq, float scale,
-                           void* O, float* LSE, int force_path, cudaStream_t st) {
+                           void* O, float* LSE, int force_path, cudaStream_t st, bool fp8, float qk_descale,
+                           float v_descale) {
   if (s->topK > 64) return cudaErrorInvalidValue;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   CUtensorMap tmQ, tmK, tmV;
+  if (fp8) {
+    // E4M3 Q [N][Hq][128]: box = the 128-byte rows of the 16 heads of one group of one query;
+    // K, V [Lkv][Hkv][128]: box = one 128-key block of one group, 128 bytes per key
+    const uint64_t qd[3] = {kHeadDim, static_cast<uint64_t>(Hq), static_cast<uint64_t>(s->N)};
+    const uint64_t qs[2] = {kHeadDim, static_cast<uint64_t>(Hq) * kHeadDim};
+    const uint32_t qbox[3] = {128, kGroup, 1};
+    if (!encode_tmap(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, Q, qd, qs, qbox, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    const uint64_t kd[3] = {kHeadDim, static_cast<uint64_t>(s->Hkv), static_cast<uint64_t>(s->nblocks) * kBlock};
+    const uint64_t ks[2] = {kHeadDim, static_cast<uint64_t>(s->Hkv) * kHeadDim};
+    const uint32_t kbox[3] = {128, 1, kBlock};
+    if (!encode_tmap(&tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, K, kd, ks, kbox, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, V, kd, ks, kbox, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  } else {
   {
     // Q [N][Hq][128] bf16: box = 64 columns of the 16 heads of one group of one query
     const uint64_t dims[3] = {kHeadDim, static_cast<uint64_t>(Hq), static_cast<uint64_t>(s->N)};
@@ -567,11 +657,14 @@ cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, 
     if (!encode_tmap(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, V, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
+  }
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(q_outer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(q_outer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaSuccess;
+    for (auto* k : {q_outer_kernel<false, false>, q_outer_kernel<true, false>})
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QoLay<false>::kSmemBytes);
+    for (auto* k : {q_outer_kernel<false, true>, q_outer_kernel<true, true>})
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QoLay<true>::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -588,7 +681,8 @@ cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, 
   p.Hkv = s->Hkv;
   p.topK = s->topK;
   p.nblocks = s->nblocks;
-  p.sl2 = scale * 1.4426950408889634f;
+  p.sl2 = scale * qk_descale * 1.4426950408889634f;
+  p.v_descale = v_descale;
   p.force_path = force_path;
   const int64_t units = static_cast<int64_t>(s->N) * s->Hkv;
   // split the units' lists while the units fill at most a quarter of the SMs: the
@@ -612,10 +706,11 @@ cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, 
   }
   int64_t grid = sms;
   if (grid > units * splits) grid = units * splits;
-  if (splits > 1)
-    MSA_LAUNCH(q_outer_kernel<true>, static_cast<int>(grid), kThreads, kSmemBytes, st, tmQ, tmK, tmV, p);
-  else
-    MSA_LAUNCH(q_outer_kernel<false>, static_cast<int>(grid), kThreads, kSmemBytes, st, tmQ, tmK, tmV, p);
+  const uint32_t smem = fp8 ? QoLay<true>::kSmemBytes : QoLay<false>::kSmemBytes;
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, QoParams) =
+      fp8 ? (splits > 1 ? q_outer_kernel<true, true> : q_outer_kernel<false, true>)
+          : (splits > 1 ? q_outer_kernel<true, false> : q_outer_kernel<false, false>);
+  MSA_LAUNCH(kern, static_cast<int>(grid), kThreads, smem, st, tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }
 

@@ -217,13 +217,11 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
   if (fp8 && !(std::isfinite(opts->q_descale) && std::isfinite(opts->k_descale) && std::isfinite(opts->v_descale) &&
                opts->q_descale > 0.f && opts->k_descale > 0.f && opts->v_descale > 0.f))
     return MSA_ERR_INVALID_ARG;
-  if (fp8 && opts->path == MSA_PATH_Q_OUTER) return MSA_ERR_UNSUPPORTED;  // the Q-outer kernel is bf16 only
   if (opts->partials_fp32 != 0 && opts->partials_fp32 != 1) return MSA_ERR_INVALID_ARG;
   const bool f32p = opts->partials_fp32 == 1;
   msa_status_t st = ensure_partials(s, msa::kGroup, f32p ? 4 : 2);
   if (st != MSA_OK) return st;
-  // E4M3 inputs always take the KV-outer kernel (the only one with an E4M3 instance)
-  const int force = fp8 ? msa::kPathKvOuter : opts->path == MSA_PATH_AUTO ? 0 : static_cast<int>(opts->path);
+  const int force = opts->path == MSA_PATH_AUTO ? 0 : static_cast<int>(opts->path);
   const float qk_descale = fp8 ? opts->q_descale * opts->k_descale : 1.f;
   const float v_descale = fp8 ? opts->v_descale : 1.f;
   const cudaStream_t stream = opts->stream;
@@ -231,7 +229,7 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
   if (ctas < 1) return MSA_ERR_CUDA;
   const int Hq = static_cast<int>(Q.h);
   const int64_t v_elems = static_cast<int64_t>(K.n) * K.h * K.d;
-  if (fp8 && !s->vf16) {
+  if (fp8 && force != msa::kPathQOuter && !s->vf16) {
     // the f16 copy of E4M3 V (first E4M3 call of this schedule; later calls allocate nothing)
     void* p = nullptr;
     cudaError_t ea = cudaMalloc(&p, static_cast<size_t>(v_elems) * 2);
@@ -240,13 +238,15 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
   }
   cudaError_t e;
   if (opts->stage_events[0] && (e = cudaEventRecord(opts->stage_events[0], stream))) return from_cuda(e);
-  if (fp8 && (e = msa::launch_widen_e4m3(V.ptr, s->vf16, v_elems, stream))) return from_cuda(e);
+  if (fp8 && force != msa::kPathQOuter && (e = msa::launch_widen_e4m3(V.ptr, s->vf16, v_elems, s->d.hdr, force, stream)))
+    return from_cuda(e);
   msa::KvOuterArgs a{s, Q.ptr, K.ptr, V.ptr, Hq, s->nblocks * msa::kBlock, scale, force, ctas, fp8, qk_descale, f32p,
                      opts->debug_flags, s->vf16};
   if ((e = msa::launch_kv_outer(a, stream))) return from_cuda(e);
   if (opts->stage_events[1] && (e = cudaEventRecord(opts->stage_events[1], stream))) return from_cuda(e);
   if ((e = msa::launch_combine(s, Hq, O, LSE, v_descale, force, f32p, stream))) return from_cuda(e);
-  if ((e = msa::launch_q_outer(s, Q.ptr, K.ptr, V.ptr, Hq, scale, O, LSE, force, stream))) return from_cuda(e);
+  if ((e = msa::launch_q_outer(s, Q.ptr, K.ptr, V.ptr, Hq, scale, O, LSE, force, stream, fp8, qk_descale, v_descale)))
+    return from_cuda(e);
   if (opts->stage_events[2] && (e = cudaEventRecord(opts->stage_events[2], stream))) return from_cuda(e);
   s->last_stream = stream;
   return MSA_OK;

@@ -155,7 +155,9 @@ struct KvOuterArgs {
 };
 cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st);
 // E4M3 [n] -> f16 [n], exact; n a multiple of 16
-cudaError_t launch_widen_e4m3(const void* src, void* dst, int64_t n, cudaStream_t st);
+// (exits at once where the device chose the Q-outer path, which widens V in shared memory)
+cudaError_t launch_widen_e4m3(const void* src, void* dst, int64_t n, const SchedHeader* hdr, int force_path,
+                              cudaStream_t st);
 
 // combine.cu
 cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, float v_descale, int force_path,
@@ -163,7 +165,8 @@ cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, f
 
 // attn_q_outer.cu
 cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, const void* V, int Hq,
-                           float scale, void* O, float* LSE, int force_path, cudaStream_t st);
+                           float scale, void* O, float* LSE, int force_path, cudaStream_t st, bool fp8 = false,
+                           float qk_descale = 1.f, float v_descale = 1.f);
 
 // select.cu: block selector R1
 size_t select_workspace_bytes(int N, int Hq, int Hkv, int nblocks);

@@ -136,20 +136,22 @@ msa_status_t msa_build_schedule(const int32_t* indices, int N, int Hkv, int topK
  * element, real value = stored value * the tensor's descale in opts; descales must be
  * finite and > 0).  O: bf16 [N, Hq, D] device; LSE: fp32 [N, Hq] device (may be NULL).
  * scale multiplies q.k (typically 1/sqrt(D)).  opts may be NULL (defaults).
- * E4M3 inputs always run the KV-outer path (AUTO included): S = Q K^T on E4M3
- * tensor cores, V widened to f16 (exact) by a pass before the attention kernel, P V in
- * f16, output bf16.
+ * E4M3 inputs take either path (AUTO: the device's choice, as for bf16): S = Q K^T on
+ * E4M3 tensor cores, V widened to f16 (exact) and P V in f16, output bf16.  The KV-outer
+ * path widens the whole V tensor by a pass before the attention kernel; the Q-outer path
+ * widens each selected block in shared memory, so the pass exits at once there.
  *
  * The first call for a given head count and partial format allocates the partial-output
  * workspace of the schedule (cudaMalloc, synchronous): N*Hkv*topK*G*(2*D + 8) bytes at most
  * for bf16 rows + float2 (m, l), N*Hkv*topK*G*(4*D + 8) with opts->partials_fp32.  A fp32
- * workspace also serves bf16 calls; the first E4M3 call also allocates Lkv*Hkv*D*2 bytes
- * for an f16 copy of V (each call widens V into it, exactly, before the attention kernel);
- * later calls allocate nothing.
+ * workspace also serves bf16 calls; the first E4M3 call that may take the KV-outer path
+ * (any but a forced Q-outer) also allocates Lkv*Hkv*D*2 bytes for an f16 copy of V (each
+ * such call widens V into it, exactly, when the device takes that path); later calls
+ * allocate nothing.
  *
  * Returns MSA_ERR_INVALID_ARG on null pointers or shapes inconsistent with the
- * schedule or non-positive E4M3 descales; MSA_ERR_UNSUPPORTED for D != 128, G != 16,
- * mixed dtypes, or E4M3 with MSA_PATH_Q_OUTER forced; MSA_ERR_CUDA on launch failure.
+ * schedule or non-positive E4M3 descales; MSA_ERR_UNSUPPORTED for D != 128, G != 16 or
+ * mixed dtypes; MSA_ERR_CUDA on launch failure.
  */
 msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V, msa_schedule_t s,
                                  void* O, float* LSE, float scale, const msa_fwd_opts_t* opts);

@@ -67,7 +67,7 @@ def assert_parity(Og, Lg, Or, Lr):
 
 @pytest.mark.parametrize("N,Lkv,Hkv,topK", [(2048, 2048, 2, 8), (333, 2048, 1, 5), (1, 1024, 2, 4)])
 def test_fp8_random_lists(N, Lkv, Hkv, topK):
-    """Pads, duplicates, future blocks, ragged N; E4M3 always runs the KV-outer kernel."""
+    """Pads, duplicates, future blocks, ragged N (high reuse: the KV-outer kernel)."""
     Q, K, V, ds, idx = fp8_case(7 * N + Lkv, N, Lkv, Hkv, topK)
     scale = 1 / math.sqrt(128)
     Og, Lg = run_gpu(Q, K, V, ds, idx, Lkv // 128, scale)
@@ -101,15 +101,41 @@ def test_fp8_deterministic():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def test_fp8_rejects_q_outer_and_bad_descales():
+@pytest.mark.parametrize("N,Lkv,Hkv,topK", [(64, 65536, 4, 16), (37, 131072, 2, 9), (1, 16384, 4, 16)])
+def test_fp8_low_reuse_q_outer(N, Lkv, Hkv, topK):
+    """E4M3 at low reuse (nsb / N far above the crossover): AUTO takes the Q-outer kernel's
+    E4M3 instance; forced Q-outer and forced KV-outer give the same answer within the
+    E4M3 tolerance, with pads and duplicates in the lists."""
+    msa = _msa()
+    Q, K, V, ds, idx = fp8_case(13 * N + Lkv, N, Lkv, Hkv, topK)
+    scale = 1 / math.sqrt(128)
+    dev = torch.device("cuda")
+    s = msa.build_schedule(torch.from_numpy(np.ascontiguousarray(idx, np.int32)).to(dev), Lkv // 128)
+    assert s.query()["path"] == 2  # the device chose Q-outer
+    s.close()
+    Or, Lr = run_oracle(Q, K, V, ds, idx, Lkv, scale)
+    for path in ("auto", "q_outer", "kv_outer"):
+        Og, Lg = run_gpu(Q, K, V, ds, idx, Lkv // 128, scale, path=path)
+        assert_parity(Og, Lg, Or, Lr)
+
+
+def test_fp8_q_outer_sharp_and_empty():
+    """Forced Q-outer on E4M3: a sharp softmax with descales far from 1, and empty lists
+    (O = 0, LSE = -inf)."""
+    Q, K, V, ds, idx = fp8_case(17, 512, 4096, 2, 12, sigma=(4.0, 3.0, 0.01))
+    idx[5::7] = -1
+    Og, Lg = run_gpu(Q, K, V, ds, idx, 32, 0.5, path="q_outer")
+    assert np.all(Og[5::7] == 0) and np.all(np.isneginf(Lg[5::7]))
+    Or, Lr = run_oracle(Q, K, V, ds, idx, 4096, 0.5)
+    assert_parity(Og, Lg, Or, Lr)
+
+
+def test_fp8_rejects_bad_descales():
     msa = _msa()
     Q, K, V, ds, idx = fp8_case(1, 256, 1024, 1, 4)
     dev = torch.device("cuda")
     s = msa.build_schedule(torch.from_numpy(idx).to(dev), 8)
     Qd, Kd, Vd = Q.to(dev), K.to(dev), V.to(dev)
-    with pytest.raises(msa.MsaError) as e:
-        msa.sparse_attn_fwd(Qd, Kd, Vd, s, path="q_outer", descales=ds)
-    assert e.value.status == 2  # MSA_ERR_UNSUPPORTED
     for bad in ((0.0, 1.0, 1.0), (1.0, -1.0, 1.0), (1.0, 1.0, float("nan"))):
         with pytest.raises(msa.MsaError) as e:
             msa.sparse_attn_fwd(Qd, Kd, Vd, s, descales=bad)
