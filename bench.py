@@ -65,6 +65,9 @@ def parse_args():
     ap.add_argument("--partials", default="bf16", choices=["bf16", "fp32"],
                     help="format of the KV-outer partial outputs (the pages' bf16 vs fp32 study)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--dispatch-sweep", action="store_true",
+                    help="time the step with each path forced over a grid of (dtype, Lkv, N) with uniform "
+                         "picks; one JSON line per point (the measurement the AUTO crossover is derived from)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return ap.parse_args()
@@ -606,8 +609,80 @@ def run_ours(args, world, rank, local, pg):
     print(json.dumps(line), flush=True)
 
 
+# (dtype, Lkv, Hkv, topK, query counts)
+SWEEP_GRID = [("bf16", 16384, 4, 16, (1, 16, 64, 128, 256, 512, 1024, 2048, 4096)),
+              ("bf16", 131072, 4, 16, (1, 16, 64, 128, 256, 512, 1024, 2048, 4096)),
+              ("bf16", 524288, 4, 16, (1, 16, 64, 128, 256, 512, 1024, 2048)),
+              ("e4m3", 131072, 4, 16, (1, 16, 64, 128, 256, 512, 1024, 2048, 4096)),
+              ("bf16", 131072, 2, 8, (16, 64, 128, 256, 512, 1024)),
+              ("bf16", 131072, 8, 32, (4, 16, 32, 64, 128, 256)),
+              ("bf16", 32768, 1, 4, (64, 256, 512, 1024, 2048))]
+
+
+def run_dispatch_sweep(args):
+    """Step time (schedule + forward, L2 flushed before each step) with the path forced to
+    KV-outer and to Q-outer, over queries at the tail of contexts of several lengths
+    (Hq = 16 Hkv, D 128, own block + topK - 1 uniform earlier blocks).  Q / K / V are
+    drawn on the device (seeded): only the timing is used, and the lists are the seeded
+    uniform ones of the workloads module.  One JSON line per (dtype, Lkv, N)."""
+    import torch
+
+    import block_sparse_gqa_gb300 as msa
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    gen = torch.Generator(device=dev)
+    for dtype, Lkv, Hkv, topK, Ns in SWEEP_GRID:
+        gen.manual_seed(Lkv)
+        K = torch.randn((Lkv, Hkv, 128), generator=gen, device=dev)
+        V = torch.randn((Lkv, Hkv, 128), generator=gen, device=dev)
+        if dtype == "e4m3":
+            K, V = (x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8) for x in (K, V))
+        else:
+            K, V = K.to(torch.bfloat16), V.to(torch.bfloat16)
+        for N in Ns:
+            cfg = workloads.Config("sweep", N, Lkv, 16 * Hkv, Hkv, 128, topK, "uniform", 2000 + N, dtype=dtype)
+            idx = torch.from_numpy(workloads.make_indices(cfg)).to(dev)
+            Q = torch.randn((N, 16 * Hkv, 128), generator=gen, device=dev)
+            Q = Q.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8) if dtype == "e4m3" else Q.to(torch.bfloat16)
+            O = torch.empty((N, 16 * Hkv, 128), dtype=torch.bfloat16, device=dev)
+            LSE = torch.empty((N, 16 * Hkv), dtype=torch.float32, device=dev)
+            sched = msa.build_schedule(idx, cfg.nblocks)
+            desc = (1.0, 1.0, 1.0)
+            row = {"dtype": dtype, "Lkv": Lkv, "Hkv": Hkv, "topK": topK, "N": N}
+            for path in ("kv_outer", "q_outer"):
+                def step():
+                    msa.build_schedule(idx, cfg.nblocks, schedule=sched)
+                    msa.sparse_attn_fwd(Q, K, V, sched, scale=cfg.scale, O=O, LSE=LSE, path=path, descales=desc)
+                for _ in range(args.warmup):
+                    step()
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(args.steps)]
+                torch.cuda.synchronize()
+                for a, b in evs:
+                    flush.zero_()
+                    a.record(stream)
+                    step()
+                    b.record(stream)
+                torch.cuda.synchronize()
+                row[path + "_us"] = 1e3 * statistics.median(a.elapsed_time(b) for a, b in evs)
+            info = sched.query()
+            assert info["status"] == 0, info
+            sched.close()
+            row.update(nsb=info["nsb"], entries=info["entries"], nsb_per_N=info["nsb"] / N,
+                       auto=("kv_outer" if info["path"] == 1 else "q_outer"),
+                       faster=("kv_outer" if row["kv_outer_us"] <= row["q_outer_us"] else "q_outer"))
+            print(json.dumps(row), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.dispatch_sweep:
+        run_dispatch_sweep(args)
+        return
     if args.impl == "reference":
         # rank 0 alone times the oracle; other ranks exit without work or collectives
         rank = int(os.environ.get("RANK", "0"))

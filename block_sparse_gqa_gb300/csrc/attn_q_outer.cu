@@ -2,8 +2,9 @@
 // fallback.
 //
 // "Kernel optimization for MiniMax M3 on NVIDIA Blackwell", Q-outer vs KV-outer
-// section: when nsb / N >= 2.85 (few queries share a block) each query walks its own
-// selected blocks; no partial outputs and no combine are needed.
+// section: at low reuse (few queries share a block; the dispatch rule is dispatch_path in
+// msa_internal.h) each query walks its own selected blocks; no partial outputs and no
+// combine are needed.
 //
 // Unit = (query i, group g): the 16 heads of the group against each selected block
 // of the (deduplicated, causally filtered) list, with an online softmax across the

@@ -69,6 +69,21 @@ __host__ __device__ __forceinline__ int64_t part_rows(int64_t cap) {
 constexpr int kPathKvOuter = 1;
 constexpr int kPathQOuter = 2;
 
+// The AUTO dispatch: KV-outer when 10 E - 13 nsb > 35000, in exact integers (E = CSR entries,
+// i.e. distinct (query, KV head, block) triples; nsb = distinct (KV head, block) pairs).
+// "Kernel optimization for MiniMax M3", Q-outer vs KV-outer section and its appendix, derives
+// KV-outer when nsb / N < 2.85 from a bandwidth model of its B200 kernels and asks for the
+// constant to be re-derived from the machine's own numbers.  Re-derived on GB300 from
+// measurement: the step time with each path forced over 36 (dtype, context, N) points
+// (bench.py --dispatch-sweep) fits T_kv - T_q = 24.3 us - 6.96 ns * E + 9.04 ns * nsb --
+// the KV-outer path's fixed cost (launches, pipeline fill, the combine), the Q-outer kernel's
+// per-entry cost, the KV-outer kernel's per-block cost -- and the rule picks the faster path
+// at all 52 measured points (16 more shapes with Hkv 1-8, topK 4-32), where nsb / N < 2.85
+// picks the slower one at 12.
+__host__ __device__ constexpr int dispatch_path(int64_t entries, int64_t nsb) {
+  return 10 * entries - 13 * nsb > 35000 ? kPathKvOuter : kPathQOuter;
+}
+
 constexpr int kStatusBadIndex = 1;
 constexpr int kStatusTimeout = 2;
 

@@ -229,8 +229,7 @@ __global__ void __launch_bounds__(NT) k_scan_rows(const int32_t* __restrict__ co
     offsets[R] = total;
     hdr->entries = total;
     hdr->nsb = nsb;
-    // crossover: KV-outer when nsb / N < 2.85, in exact integers
-    hdr->path = (static_cast<int64_t>(nsb) * 100 < static_cast<int64_t>(N) * 285) ? kPathKvOuter : kPathQOuter;
+    hdr->path = dispatch_path(total, nsb);  // (msa_internal.h)
   }
 }
 
@@ -303,8 +302,7 @@ __device__ void scan_small_body(const int32_t* __restrict__ counts, int R, int N
     offsets[R] = total;
     hdr->entries = total;
     hdr->nsb = nsb;
-    // crossover: KV-outer when nsb / N < 2.85, in exact integers
-    hdr->path = (static_cast<int64_t>(nsb) * 100 < static_cast<int64_t>(N) * 285) ? kPathKvOuter : kPathQOuter;
+    hdr->path = dispatch_path(total, nsb);  // (msa_internal.h)
   }
   const int tiles = block_scan_array<NT>(seg, seg, nseg, sm, warp_buf, nullptr, window_tiles, R);
   if (threadIdx.x == 0) {

@@ -57,7 +57,7 @@ def _load():
         lib.oracle_e4m3_decode.restype = f64
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
         lib.oracle_dispatch.restype = i32
-        lib.oracle_dispatch.argtypes = [ctypes.c_int32, i32]
+        lib.oracle_dispatch.argtypes = [ctypes.c_int64, ctypes.c_int32]
         lib.oracle_attn_bwd.restype = i32
         lib.oracle_attn_bwd.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i32, f64,
                                         P, i32, P, P, i32, P, P, i32]
@@ -220,9 +220,10 @@ def e4m3_decode(byte: int) -> float:
     return _load().oracle_e4m3_decode(int(byte))
 
 
-def dispatch(nsb: int, N: int) -> int:
-    """1 = KV-outer, 2 = Q-outer (crossover nsb/N < 2.85)."""
-    return _load().oracle_dispatch(int(nsb), int(N))
+def dispatch(E: int, nsb: int) -> int:
+    """1 = KV-outer, 2 = Q-outer: KV-outer when 10 E - 13 nsb > 35000 (E CSR entries, nsb
+    distinct (group, block) pairs; the GB300 re-derivation of the pages' crossover)."""
+    return _load().oracle_dispatch(int(E), int(nsb))
 
 
 def select_r4(Q, K, *, Lkv, topK, block=128, tile=128):

@@ -331,11 +331,18 @@ void oracle_lse_merge(int n, int D, const double* O_parts, const double* lse_par
   *lse_out = LSE;
 }
 
-/* Crossover ("Kernel optimization for MiniMax M3", Q-outer vs KV-outer section):
- * KV-outer when nsb / N < 2.85, i.e. 100*nsb < 285*N in exact integers.
- * Returns 1 for KV-outer, 2 for Q-outer. */
-int oracle_dispatch(int32_t nsb, int N) {
-  return ((int64_t)nsb * 100 < (int64_t)N * 285) ? 1 : 2;
+/* Crossover ("Kernel optimization for MiniMax M3", Q-outer vs KV-outer section and its
+ * appendix).  The page derives "KV-outer when nsb / N < 2.85" from a bandwidth model of
+ * its B200 kernels and says the constant is to be re-derived from the target machine's own
+ * measurements.  The reading taken here is that re-derivation for this library on GB300:
+ * the step-time difference of the two paths, measured over queries at the tail of contexts
+ * of several lengths, is fitted by a constant (the KV-outer path's fixed launch and pipeline
+ * cost), a term per CSR entry E (the Q-outer kernel's per-entry cost) and a term per
+ * distinct (group, block) pair nsb (the KV-outer kernel's per-block cost), which gives:
+ * KV-outer when 10*E - 13*nsb > 35000, in exact integers.  Returns 1 for KV-outer, 2 for
+ * Q-outer. */
+int oracle_dispatch(int64_t E, int32_t nsb) {
+  return (10 * E - 13 * (int64_t)nsb > 35000) ? 1 : 2;
 }
 
 /* Block selector R1 ("Sparse Attention" (dinara-dl), Chapter 4, "R1: One

@@ -56,10 +56,12 @@ def assert_parity(Og, Lg, Or, Lr, rel_tol=BF16_REL_L2):
 def test_tiny_all_queries():
     wl = workloads.make_workload("tiny")
     cfg = wl.cfg
-    Og, Lg, st = run_gpu(wl.Q, wl.K, wl.V, wl.indices.numpy(), cfg.nblocks, cfg.scale)
-    assert st["path"] == 1
     Or, Lr = run_oracle(wl.Q, wl.K, wl.V, wl.indices.numpy(), cfg.Lkv, cfg.scale)
-    assert_parity(Og, Lg, Or, Lr)
+    ref = oracle.schedule(wl.indices.numpy(), Lkv=cfg.Lkv)
+    for path in ("auto", "kv_outer", "q_outer"):
+        Og, Lg, st = run_gpu(wl.Q, wl.K, wl.V, wl.indices.numpy(), cfg.nblocks, cfg.scale, path=path)
+        assert st["path"] == oracle.dispatch(ref["E"], ref["nsb"])  # the device's AUTO choice
+        assert_parity(Og, Lg, Or, Lr)
 
 
 def random_case(seed, N, Lkv, Hkv, topK, pad_dup=True):

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads
-from tests.util import TILE, WINDOW, check_worklist
+from tests.util import BF16_MAX_ABS, BF16_REL_L2, LSE_MAX_ABS, TILE, WINDOW, check_worklist, compare_outputs
 
 pytestmark = pytest.mark.gpu
 
@@ -30,7 +30,7 @@ def assert_same(exp, ref, N, Lkv):
     for k in ("counts", "offsets", "qlist", "slot", "cmap"):
         np.testing.assert_array_equal(exp[k], ref[k], err_msg=k)
     assert exp["E"] == ref["E"] and exp["nsb"] == ref["nsb"]
-    assert exp["path"] == oracle.dispatch(ref["nsb"], N)
+    assert exp["path"] == oracle.dispatch(ref["E"], ref["nsb"])
     check_worklist(exp, ref, N)
     tiles, wt = oracle.worklist(ref["offsets"], ref["qlist"], N, window=WINDOW, tile_rows=TILE)
     np.testing.assert_array_equal(np.asarray(exp["window_tiles"]), wt, err_msg="window_tiles")
@@ -119,3 +119,29 @@ def test_schedule_small_inputs_match_oracle(N, Lkv, Hkv, topK):
     assert exp["status"] & 1 and ref["status"] == 1
     assert_same(exp, ref, N, Lkv)
     s.close()
+
+
+@pytest.mark.parametrize("N,expected", [(3536, 2), (3537, 1)])
+def test_dispatch_at_the_boundary(N, expected):
+    """Own-block lists at the tail of 3584 tokens (28 blocks, one KV head): E = N and
+    nsb = 28, so 10 E - 13 nsb is 34996 (Q-outer) or 35006 (KV-outer).  The device's AUTO
+    choice equals the oracle's on both sides, and the forward it runs matches the oracle."""
+    Lkv, nb = 3584, 28
+    idx = ((Lkv - N + np.arange(N)) // 128).astype(np.int32).reshape(N, 1, 1)
+    ref = oracle.schedule(idx, Lkv=Lkv)
+    assert (ref["E"], ref["nsb"]) == (N, nb)
+    s, exp = gpu_schedule(idx, nb)
+    assert exp["path"] == oracle.dispatch(ref["E"], ref["nsb"]) == expected
+    gen = torch.Generator().manual_seed(N)
+    Q = torch.randn((N, 16, 128), generator=gen).to(torch.bfloat16)
+    K = torch.randn((Lkv, 1, 128), generator=gen).to(torch.bfloat16)
+    V = torch.randn((Lkv, 1, 128), generator=gen).to(torch.bfloat16)
+    msa = _msa()
+    O, LSE = msa.sparse_attn_fwd(Q.cuda(), K.cuda(), V.cuda(), s, scale=0.09)
+    torch.cuda.synchronize()
+    s.close()
+    qids = np.array([0, 1, 127, 128, N // 2, N - 2, N - 1], np.int32)
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    Or, Lr, _ = oracle.attn_fwd(bits(Q), bits(K), bits(V), idx, Lkv=Lkv, scale=0.09, qids=qids)
+    rel, mabs, lerr = compare_outputs(O.float().cpu().numpy()[qids], LSE.cpu().numpy()[qids], Or, Lr)
+    assert rel <= BF16_REL_L2 and mabs <= BF16_MAX_ABS and lerr <= LSE_MAX_ABS, (rel, mabs, lerr)

@@ -327,8 +327,14 @@ def test_worklist_invariants(seed, N, Lkv, Hkv, window):
 
 
 def test_dispatch_threshold():
-    assert oracle.dispatch(56, 20) == 1 and oracle.dispatch(57, 20) == 2  # 57/20 = 2.85 exactly
-    assert oracle.dispatch(256, 8192) == 1 and oracle.dispatch(9980, 256) == 2
+    """KV-outer when 10 E - 13 nsb > 35000, evaluated by hand at and around the boundary."""
+    assert oracle.dispatch(3500, 0) == 2 and oracle.dispatch(3501, 0) == 1  # 35000 is not above
+    assert oracle.dispatch(3536, 28) == 2 and oracle.dispatch(3537, 28) == 1  # 34996 / 35006
+    assert oracle.dispatch(4600, 1000) == 2 and oracle.dispatch(4600, 846) == 1  # 33000 / 35002
+    # the workloads: M3 (E 462848, nsb 256) and the low-reuse one (E 16384, nsb 9980: 34100)
+    assert oracle.dispatch(462848, 256) == 1 and oracle.dispatch(16384, 9980) == 2
+    # a larger nsb favours Q-outer, a larger E KV-outer (the signs of the two terms)
+    assert oracle.dispatch(10_000, 4999) == 1 and oracle.dispatch(10_000, 4999 + 3848) == 2  # 35013 / -11
 
 
 def test_e4m3_decoder_matches_library_cast():

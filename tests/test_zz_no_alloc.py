@@ -60,13 +60,15 @@ def bits(t):
 def test_noalloc_matches_allocating_path_on_two_calls_in_a_row():
     import block_sparse_gqa_gb300 as msa
     dev = torch.device("cuda")
-    for seed, sparser in ((1000, False), (4242, True)):
+    # the KV-outer path keeps its partial outputs in the shared array; the tiny workload's
+    # own choice (AUTO) is the Q-outer kernel, which needs no partials
+    for (seed, sparser), path in (((1000, False), "kv_outer"), ((4242, True), "kv_outer"), ((1000, False), "auto")):
         cfg, idx_h, Qh, Kh, Vh = inputs(seed, sparser)
         idx, Q, K, V = idx_h.to(dev), Qh.to(dev), Kh.to(dev), Vh.to(dev)
         sched = msa.build_schedule(idx, cfg.nblocks)
-        O_ref, L_ref = msa.sparse_attn_fwd(Q, K, V, sched, scale=cfg.scale)
+        O_ref, L_ref = msa.sparse_attn_fwd(Q, K, V, sched, scale=cfg.scale, path=path)
         status = torch.full((1,), -1, dtype=torch.int32, device=dev)
-        st, O, LSE = noalloc_fwd(msa, idx, cfg.nblocks, Q, K, V, cfg.scale, status=status)
+        st, O, LSE = noalloc_fwd(msa, idx, cfg.nblocks, Q, K, V, cfg.scale, status=status, path=msa.PATHS[path])
         torch.cuda.synchronize()
         sched.close()
         assert st == 0, msa.lib().msa_status_string(st)
@@ -90,11 +92,11 @@ def test_noalloc_reports_bad_block_ids_through_status():
     idx_h[5, 0, 1] = cfg.nblocks + 7  # out of range: ignored like a pad, and reported
     idx, Q, K, V = idx_h.to(dev), Qh.to(dev), Kh.to(dev), Vh.to(dev)
     status = torch.zeros((1,), dtype=torch.int32, device=dev)
-    st, O, LSE = noalloc_fwd(msa, idx, cfg.nblocks, Q, K, V, cfg.scale, status=status)
+    st, O, LSE = noalloc_fwd(msa, idx, cfg.nblocks, Q, K, V, cfg.scale, status=status, path=1)
     torch.cuda.synchronize()
     assert st == 0 and int(status.item()) & 1
     sched = msa.build_schedule(idx, cfg.nblocks)
-    O_ref, _ = msa.sparse_attn_fwd(Q, K, V, sched, scale=cfg.scale)
+    O_ref, _ = msa.sparse_attn_fwd(Q, K, V, sched, scale=cfg.scale, path="kv_outer")
     torch.cuda.synchronize()
     assert sched.status() == 5  # MSA_ERR_BAD_INDEX on the allocating pair too
     sched.close()
