@@ -79,7 +79,7 @@ constexpr int kPathQOuter = 2;
 // the KV-outer path's fixed cost (launches, pipeline fill, the combine), the Q-outer kernel's
 // per-entry cost, the KV-outer kernel's per-block cost -- and the rule picks the faster path
 // at all 52 measured points (16 more shapes with Hkv 1-8, topK 4-32), where nsb / N < 2.85
-// picks the slower one at 12.
+// picks the slower one at 19.
 __host__ __device__ constexpr int dispatch_path(int64_t entries, int64_t nsb) {
   return 10 * entries - 13 * nsb > 35000 ? kPathKvOuter : kPathQOuter;
 }

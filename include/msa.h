@@ -55,7 +55,7 @@ typedef enum { MSA_BF16 = 0, MSA_FP8_E4M3 = 1 } msa_dtype_t;
  * optimization for MiniMax M3" (Q-outer vs KV-outer section and appendix), re-derived from
  * measurements on GB300 as the page asks: KV-outer when 10 E - 13 nsb > 35000, where E is
  * the number of distinct (query, KV head, block) entries and nsb the number of distinct
- * (KV head, block) pairs (the page's B200 rule, nsb / N < 2.85, picked the slower path at 12
+ * (KV head, block) pairs (the page's B200 rule, nsb / N < 2.85, picked the slower path at 19
  * of 52 measured GB300 points).  The choice is made on the device by msa_build_schedule;
  * no device-to-host copy is needed. */
 typedef enum { MSA_PATH_AUTO = 0, MSA_PATH_KV_OUTER = 1, MSA_PATH_Q_OUTER = 2 } msa_path_t;
