@@ -14,16 +14,18 @@ from dataclasses import dataclass
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmsa.so")
+# MSA_LIBRARY=debug selects the bounds-checked build (same entry points; see msa_debug_build)
+LIB_PATH = os.path.join(_HERE, "libmsa_debug.so" if os.environ.get("MSA_LIBRARY") == "debug" else "libmsa.so")
 
 MSA_OK = 0
 STATUS_NAMES = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_CUDA",
-                4: "MSA_ERR_OOM", 5: "MSA_ERR_BAD_INDEX", 6: "MSA_ERR_TIMEOUT", 7: "MSA_ERR_CAPACITY"}
+                4: "MSA_ERR_OOM", 5: "MSA_ERR_BAD_INDEX", 6: "MSA_ERR_TIMEOUT", 7: "MSA_ERR_CAPACITY",
+                8: "MSA_ERR_BOUNDS"}
 DTYPE_BF16, DTYPE_FP8_E4M3 = 0, 1
 PATHS = {"auto": 0, "kv_outer": 1, "q_outer": 2}
 EXPORTED = ["msa_fwd_opts_init", "msa_build_schedule", "msa_sparse_attn_fwd", "msa_schedule_destroy",
             "msa_schedule_query", "msa_schedule_export", "msa_status_string", "msa_last_cuda_error",
-            "msa_version"]
+            "msa_version", "msa_debug_build"]
 
 
 class MsaError(RuntimeError):

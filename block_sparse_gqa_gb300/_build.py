@@ -11,6 +11,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmsa.so")
+LIB_DEBUG = os.path.join(HERE, "libmsa_debug.so")  # bounds-checked build (MSA_DEBUG=1)
 SOURCES = ["msa_api.cu", "schedule.cu", "attn_kv_outer.cu", "combine.cu", "attn_q_outer.cu", "msa_noalloc.cu",
            "select.cu", "attn_tiles.cu", "attn_bwd.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("ptx.cuh", "msa_internal.h")] + [os.path.join(ROOT, "include", "msa.h")]
@@ -33,16 +34,25 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def _build_one(lib: str, objdir: str, defines, force: bool, verbose: bool, extra_flags) -> str:
+    os.makedirs(objdir, exist_ok=True)
     nvcc = _nvcc()
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(objdir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + HEADERS):
-            jobs.append([nvcc, *FLAGS, *extra_flags, "-c", s, "-o", o])
+            jobs.append([nvcc, *FLAGS, *defines, *extra_flags, "-c", s, "-o", o])
+    return lib, objs, jobs
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    """Compile libmsa.so and its bounds-checked twin libmsa_debug.so (MSA_DEBUG=1), all
+    translation units of both in parallel."""
+    targets = [_build_one(LIB, BUILD, [], force, verbose, extra_flags),
+               _build_one(LIB_DEBUG, BUILD + "_debug", ["-DMSA_DEBUG=1"], force, verbose, extra_flags)]
+    jobs = [j for _, _, js in targets for j in js]
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
             futs = [ex.submit(subprocess.run, j, capture_output=True, text=True) for j in jobs]
@@ -52,12 +62,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                     print(r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError(f"nvcc failed: {' '.join(j)}\n{r.stdout}\n{r.stderr}")
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
-        r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"link failed\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
+    for lib, objs, js in targets:
+        if force or js or _stale(lib, objs):
+            tmp = lib + f".tmp{os.getpid()}"
+            r = subprocess.run([_nvcc(), *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"link failed\n{r.stdout}\n{r.stderr}")
+            os.replace(tmp, lib)
     return LIB
 
 

@@ -93,6 +93,8 @@ struct BwdParams {
   float* dkv;              // [units][2][128][128]: dK then dV
   SchedHeader* hdr;
   int N, Lkv, Hq, nblocks;
+  int R;          // schedule rows (Hkv * nblocks)
+  int64_t cap_e;  // CSR positions the schedule holds
   float sl2;  // scale * log2(e)
 };
 
@@ -182,7 +184,10 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           }
           break;
         }
-        const int4 un = p.units[u];
+        int4 un = p.units[u];
+        // (bounds-checked build: a unit record out of range becomes one entry of row 0)
+        if (!dbg_ok(un.x >= 0 && un.x < p.R && un.y >= 0 && un.z >= 1 && un.y + un.z <= p.cap_e, &p.hdr->status))
+          un = make_int4(0, 0, 1, un.w);
         const int g = un.x / p.nblocks, b = un.x - g * p.nblocks;
         const int ntile = (un.z + kTileQ - 1) / kTileQ;
         for (int t = 0; t < ntile && ok; ++t, ++it) {
@@ -202,7 +207,8 @@ bwd_kv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
           for (int j = 0; j < cnt; ++j) {
             // one 4 KB box per query and tensor: its 16 heads as two 8-row groups, each
             // with both D halves ([group][D half][8 rows][128 B])
-            const int q = __ldg(p.qlist + e0 + j);
+            int q = __ldg(p.qlist + e0 + j);
+            if (!dbg_ok(q >= 0 && q < p.N, &p.hdr->status)) q = 0;
             tl.q[j] = q;
             tma_load_5d(dq + j * 4096, &tmQ, 0, 0, 0, 2 * g, q, bq, pol_q);
             tma_load_5d(ddo + j * 4096, &tmDO, 0, 0, 0, 2 * g, q, bq, pol_q);
@@ -710,6 +716,8 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
   p.Lkv = a.Lkv;
   p.Hq = a.Hq;
   p.nblocks = s->nblocks;
+  p.R = s->R;
+  p.cap_e = s->cap_entries;
   p.sl2 = a.scale * 1.4426950408889634f;
   static bool attr_set = false;
   if (!attr_set) {

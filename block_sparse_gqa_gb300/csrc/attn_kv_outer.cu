@@ -156,6 +156,8 @@ struct KvParams {
   SchedHeader* hdr;
   float2* pstat;
   int N, Lkv, nblocks;
+  int R;          // Hkv * nblocks schedule rows
+  int64_t cap_e;  // CSR positions the schedule's arrays and the partial workspace hold
   float sl2;  // scale * log2(e) (* q descale * k descale for E4M3)
   int force_path;
 };
@@ -362,8 +364,10 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           const int t0 = lane >> 3, j = lane & 7;
           const int f0 = __shfl_sync(full, m.tile.y, t0), n0 = __shfl_sync(full, m.tile.z, t0);
           const int f1 = __shfl_sync(full, m.tile.y, t0 + 4), n1 = __shfl_sync(full, m.tile.z, t0 + 4);
-          m.qa = j < n0 ? p.qlist[f0 + j] : 0;
-          m.qb = j < n1 ? p.qlist[f1 + j] : 0;
+          const bool in0 = j < n0 && dbg_ok(f0 + j >= 0 && f0 + j < p.cap_e, &p.hdr->status);
+          const bool in1 = j < n1 && dbg_ok(f1 + j >= 0 && f1 + j < p.cap_e, &p.hdr->status);
+          m.qa = in0 ? p.qlist[f0 + j] : 0;
+          m.qb = in1 ? p.qlist[f1 + j] : 0;
         };
         int c_cur = 0, c_next = 0, c_claim = 0;
         if (lane == 0) {
@@ -405,10 +409,21 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           bool ids_next = false;
           for (int t = 0; t < cur.n; ++t, ++it) {
             if (t == 3) { load_ids(nxt); ids_next = true; }  // the next chunk's tiles have arrived by now
-            const int row = __shfl_sync(full, cur.tile.x, t);
-            const int first = __shfl_sync(full, cur.tile.y, t);
-            const int count = __shfl_sync(full, cur.tile.z, t);
-            const int qv = __shfl_sync(full, t < 4 ? cur.qa : cur.qb, ((t & 3) << 3) | (lane & 7));
+            int row = __shfl_sync(full, cur.tile.x, t);
+            int first = __shfl_sync(full, cur.tile.y, t);
+            int count = __shfl_sync(full, cur.tile.z, t);
+            int qv = __shfl_sync(full, t < 4 ? cur.qa : cur.qb, ((t & 3) << 3) | (lane & 7));
+            if (MSA_DEBUG) {
+              // a tile record or query id out of range: the tile becomes one entry of row 0 at
+              // position 0 (valid addresses; the status reports the fault)
+              if (!dbg_ok(row >= 0 && row < p.R && count >= 1 && count <= kTileQ && first >= 0 &&
+                              first + count <= p.cap_e, &p.hdr->status)) {
+                row = 0;
+                first = 0;
+                count = 1;
+              }
+              if (lane < count && !dbg_ok(qv >= 0 && qv < p.N, &p.hdr->status)) qv = 0;
+            }
             const bool new_row = row != prev_row;
             const int kb = new_row ? (nk & 1) : ((nk - 1) & 1);
             {
@@ -768,6 +783,8 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   p.N = s->N;
   p.Lkv = a.Lkv;
   p.nblocks = s->nblocks;
+  p.R = s->R;
+  p.cap_e = s->cap_entries;
   p.sl2 = a.scale * a.qk_descale * 1.4426950408889634f;
   p.force_path = a.force_path;
   static bool attr_set[4] = {false, false, false, false};

@@ -120,7 +120,8 @@ __device__ __forceinline__ int unit_blocks(const QoParams& p, int64_t u, int lan
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     const int k = 32 * c + lane;
-    const int b = k < p.topK ? lst[k] : -1;
+    int b = k < p.topK ? lst[k] : -1;
+    if (!dbg_ok(b >= -1 && b < p.nblocks, &p.hdr_w->status)) b = -1;  // (bounds-checked build)
     const unsigned m = __ballot_sync(0xffffffffu, b >= 0);
     // compaction: the valid id of lane src goes to slot cnt + (valid lanes below src)
     for (int src = 0; src < 32; ++src) {

@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(kThreads, kF32 ? 3 : 4)
 combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ partial,
                const float2* __restrict__ pstat, int N, int Hkv, int topK, int Hq,
                __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, float v_descale,
-               SchedHeader* __restrict__ hdr, int force_path) {
+               SchedHeader* __restrict__ hdr, int force_path, int64_t cap_e) {
   griddep_wait();
   // (no early griddep_launch here: the Q-outer kernel after this one would then be scheduled
   // beside running combine CTAs, and its ~210 KB of shared memory takes the L1 this kernel's
@@ -108,6 +108,9 @@ combine_kernel(const int32_t* __restrict__ cmap, const uint4* __restrict__ parti
       int pos[kKChunk];
 #pragma unroll
       for (int k = 0; k < kKChunk; ++k) pos[k] = k0 == 0 ? first[k] : (k0 + k < topK) ? __ldg(cm + k0 + k) : -1;
+#pragma unroll
+      for (int k = 0; k < kKChunk; ++k)  // (bounds-checked build: a map entry out of range is dropped)
+        if (!dbg_ok(pos[k] >= -1 && pos[k] < cap_e, &hdr->status)) pos[k] = -1;
       float2 st[kKChunk];
       Part8<kF32> v[kKChunk];
 #pragma unroll
@@ -171,11 +174,11 @@ cudaError_t launch_combine(const msa_schedule* s, int Hq, void* O, float* LSE, f
   if (f32p)
     MSA_LAUNCH(combine_kernel<true>, static_cast<int>(grid), kThreads, 0, st, 
         s->d.cmap, static_cast<const uint4*>(s->partial), s->pstat, s->N, s->Hkv, s->topK, Hq,
-        static_cast<__nv_bfloat16*>(O), LSE, v_descale, s->d.hdr, force_path);
+        static_cast<__nv_bfloat16*>(O), LSE, v_descale, s->d.hdr, force_path, s->cap_entries);
   else
     MSA_LAUNCH(combine_kernel<false>, static_cast<int>(grid), kThreads, 0, st, 
         s->d.cmap, static_cast<const uint4*>(s->partial), s->pstat, s->N, s->Hkv, s->topK, Hq,
-        static_cast<__nv_bfloat16*>(O), LSE, v_descale, s->d.hdr, force_path);
+        static_cast<__nv_bfloat16*>(O), LSE, v_descale, s->d.hdr, force_path, s->cap_entries);
   return cudaGetLastError();
 }
 

@@ -322,6 +322,7 @@ msa_status_t msa_schedule_query(msa_schedule_t s, msa_schedule_info_t* info) {
   info->rows = s->R;
   info->windows = s->nW;
   if (h.status & msa::kStatusTimeout) return MSA_ERR_TIMEOUT;
+  if (h.status & msa::kStatusBounds) return MSA_ERR_BOUNDS;
   if (h.status & msa::kStatusBadIndex) return MSA_ERR_BAD_INDEX;
   return MSA_OK;
 }
@@ -423,11 +424,14 @@ const char* msa_status_string(msa_status_t st) {
     case MSA_ERR_BAD_INDEX: return "block id out of range in indices (ignored)";
     case MSA_ERR_TIMEOUT: return "bounded device wait expired";
     case MSA_ERR_CAPACITY: return "size exceeds a fixed capacity";
+    case MSA_ERR_BOUNDS: return "an index or TMA coordinate was out of range (bounds-checked build)";
   }
   return "unknown status";
 }
 
 int msa_last_cuda_error(void) { return g_last_cuda; }
+
+int msa_debug_build(void) { return MSA_DEBUG; }
 
 int msa_version(void) { return 100; }
 

@@ -86,6 +86,26 @@ __host__ __device__ constexpr int dispatch_path(int64_t entries, int64_t nsb) {
 
 constexpr int kStatusBadIndex = 1;
 constexpr int kStatusTimeout = 2;
+constexpr int kStatusBounds = 4;  // bounds-checked builds only
+
+// Bounds-checked build (compiled with -DMSA_DEBUG=1 into libmsa_debug.so): every gather index
+// and TMA coordinate a kernel reads from device memory (schedule arrays, tile records, query
+// and block ids, combine map entries) is checked against its tensor's extent before use.  A
+// value out of range sets kStatusBounds in the schedule header and the access is skipped
+// (stores) or redirected to element 0 (loads, so that barrier byte counts still match); no
+// trap or assert.  The release build compiles the checks away.
+#ifndef MSA_DEBUG
+#define MSA_DEBUG 0
+#endif
+#ifdef __CUDACC__
+__device__ __forceinline__ bool dbg_ok(bool in_range, int32_t* status) {
+  if (MSA_DEBUG && !in_range) {
+    atomicOr(status, kStatusBounds);
+    return false;
+  }
+  return true;
+}
+#endif
 
 // Device-resident header written by the schedule kernels and read by the attention
 // kernels (the dispatch decision never leaves the device).

@@ -115,8 +115,12 @@ __device__ __forceinline__ void entries_body(const int32_t* __restrict__ idx, in
         if (entry) {
           const uint32_t word = mask[r * C + (i >> 5)];
           p = offsets[r] + rowbase[r * (C + 1) + (i >> 5)] + __popc(word & ((1u << (i & 31)) - 1u));
-          qlist[p] = i;
-          slot[p] = k;
+          if (dbg_ok(p >= 0 && static_cast<int64_t>(p) < static_cast<int64_t>(N) * Hkv * topK, &hdr->status)) {
+            qlist[p] = i;
+            slot[p] = k;
+          } else {
+            p = -1;
+          }
         }
         cmap[e0 + t] = p;
         blist[e0 + t] = entry ? b : -1;
@@ -399,7 +403,8 @@ __global__ void __launch_bounds__(NT) k_seg_down(int32_t* __restrict__ seg, int6
 // segment, its lanes writing the segment's tiles (a segment holds up to kWindow / kTileQ tiles)
 __device__ __forceinline__ void tiles_body(const int32_t* __restrict__ segoff, int64_t nseg, int R, int C,
                                            const int32_t* __restrict__ rowbase, const int32_t* __restrict__ offsets,
-                                           int4* __restrict__ tiles, int bid, int nbid) {
+                                           int4* __restrict__ tiles, int64_t cap_tiles, int32_t* status,
+                                           int bid, int nbid) {
   constexpr int kCpw = kWindow / kChunk;
   constexpr int kWarps = kEntThreads / 32;
   const int lane = threadIdx.x & 31;
@@ -413,7 +418,8 @@ __device__ __forceinline__ void tiles_body(const int32_t* __restrict__ segoff, i
     const int first = offsets[r] + rb[cw0];
     const int cnt = rb[cw1] - rb[cw0];
     for (int j = lane; j < n; j += 32)
-      tiles[t0 + j] = make_int4(r, first + kTileQ * j, min(kTileQ, cnt - kTileQ * j), w);
+      if (dbg_ok(t0 + j >= 0 && t0 + j < cap_tiles, status))
+        tiles[t0 + j] = make_int4(r, first + kTileQ * j, min(kTileQ, cnt - kTileQ * j), w);
   }
 }
 
@@ -425,7 +431,7 @@ k_scatter_tiles(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int n
                 const int32_t* __restrict__ rowbase, const int32_t* __restrict__ offsets,
                 int32_t* __restrict__ qlist, int32_t* __restrict__ slot, int32_t* __restrict__ cmap,
                 int32_t* __restrict__ blist, const int32_t* __restrict__ segoff, int64_t nseg, int R,
-                int4* __restrict__ tiles, SchedHeader* hdr) {
+                int4* __restrict__ tiles, int64_t cap_tiles, SchedHeader* hdr) {
   griddep_wait();
   griddep_launch();
   const int b = blockIdx.x;
@@ -433,7 +439,8 @@ k_scatter_tiles(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int n
     entries_body<true>(idx, N, Hkv, topK, nblocks, Lkv, C, lists_per_cta, const_cast<uint32_t*>(mask), rowbase,
                        offsets, qlist, slot, cmap, blist, hdr, b, ent_grid);
   else
-    tiles_body(segoff, nseg, R, C, rowbase, offsets, tiles, b - ent_grid, static_cast<int>(gridDim.x) - ent_grid);
+    tiles_body(segoff, nseg, R, C, rowbase, offsets, tiles, cap_tiles, &hdr->status, b - ent_grid,
+               static_cast<int>(gridDim.x) - ent_grid);
 }
 
 // The whole schedule in one CTA (small inputs).  Phases, separated by CTA barriers:
@@ -458,7 +465,7 @@ __device__ __forceinline__ bool slot_entry(const int32_t* __restrict__ lst, int 
 
 __global__ void __launch_bounds__(kOneThreads, 1)
 k_schedule_one(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int R, int C, int nW,
-               SchedDev d) {
+               SchedDev d, int64_t cap_tiles) {
   griddep_wait();
   griddep_launch();
   __shared__ int warp_buf[32];
@@ -517,8 +524,12 @@ k_schedule_one(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nb
       const size_t r = static_cast<size_t>(g) * nblocks + b;
       const uint32_t word = __ldcg(d.mask + r * C + (i >> 5));
       p = d.offsets[r] + d.rowbase[r * (C + 1) + (i >> 5)] + __popc(word & ((1u << (i & 31)) - 1u));
-      d.qlist[p] = i;
-      d.slot[p] = k;
+      if (dbg_ok(p >= 0 && p < nslot, &d.hdr->status)) {
+        d.qlist[p] = i;
+        d.slot[p] = k;
+      } else {
+        p = -1;
+      }
     }
     d.cmap[e] = p;
     d.blist[e] = entry ? b : -1;
@@ -531,7 +542,9 @@ k_schedule_one(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nb
     const int32_t* rb = d.rowbase + static_cast<size_t>(r) * (C + 1);
     const int first = d.offsets[r] + rb[cw0];
     const int cnt = rb[cw1] - rb[cw0];
-    for (int j = 0; j < n; ++j) d.tiles[t0 + j] = make_int4(r, first + kTileQ * j, min(kTileQ, cnt - kTileQ * j), w);
+    for (int j = 0; j < n; ++j)
+      if (dbg_ok(t0 + j >= 0 && t0 + j < cap_tiles, &d.hdr->status))
+        d.tiles[t0 + j] = make_int4(r, first + kTileQ * j, min(kTileQ, cnt - kTileQ * j), w);
   }
   if (t == 0 && s_bad) atomicOr(&d.hdr->status, kStatusBadIndex);
 }
@@ -561,7 +574,8 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
   // tiny inputs: one CTA (limits keep its serial per-thread loops short)
   if (nl * s->topK <= kOneMaxSlots && static_cast<int64_t>(s->R) * s->C <= kOneMaxMaskWords && s->C <= 64 &&
       s->nseg <= kOneMaxSegments) {
-    MSA_LAUNCH(k_schedule_one, 1, kOneThreads, 0, st, indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->R, s->C, s->nW, d);
+    MSA_LAUNCH(k_schedule_one, 1, kOneThreads, 0, st, indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->R, s->C, s->nW, d,
+               s->cap_tiles);
     return cudaGetLastError();
   }
   if ((e = cudaMemsetAsync(d.mask, 0, sizeof(uint32_t) * static_cast<size_t>(s->R) * s->C, st))) return e;
@@ -587,7 +601,7 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
   const int tiles_grid = grid_for(s->nseg, kEntThreads / 32, 1 << 16);  // a warp per segment
   MSA_LAUNCH(k_scatter_tiles, ent_grid + tiles_grid, kEntThreads, 0, st, 
       indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C, lists_per_cta, ent_grid, d.mask, d.rowbase, d.offsets,
-      d.qlist, d.slot, d.cmap, d.blist, d.segoff, s->nseg, s->R, d.tiles, d.hdr);
+      d.qlist, d.slot, d.cmap, d.blist, d.segoff, s->nseg, s->R, d.tiles, s->cap_tiles, d.hdr);
   return cudaGetLastError();
 }
 

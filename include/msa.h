@@ -46,7 +46,10 @@ typedef enum {
   MSA_ERR_OOM = 4,          /* device allocation failed */
   MSA_ERR_BAD_INDEX = 5,    /* device saw block ids >= nblocks or < -1 (ignored) */
   MSA_ERR_TIMEOUT = 6,      /* a bounded device wait expired; outputs undefined */
-  MSA_ERR_CAPACITY = 7      /* a size exceeds a fixed capacity */
+  MSA_ERR_CAPACITY = 7,     /* a size exceeds a fixed capacity */
+  MSA_ERR_BOUNDS = 8        /* bounds-checked build only (libmsa_debug.so, MSA_DEBUG): an index
+                               or TMA coordinate read from device memory was out of range; the
+                               access was skipped or redirected to element 0; outputs undefined */
 } msa_status_t;
 
 typedef enum { MSA_BF16 = 0, MSA_FP8_E4M3 = 1 } msa_dtype_t;
@@ -358,6 +361,12 @@ int msa_last_cuda_error(void);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int msa_version(void);
+
+/* 1 in the bounds-checked build (libmsa_debug.so, compiled with MSA_DEBUG=1; same entry
+ * points, every device-side gather index and TMA coordinate checked, violations reported as
+ * MSA_ERR_BOUNDS by msa_schedule_status / msa_schedule_query), 0 in the release build.  A
+ * development aid with no counterpart in the pages. */
+int msa_debug_build(void);
 
 #ifdef __cplusplus
 }
