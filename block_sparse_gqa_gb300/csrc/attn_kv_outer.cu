@@ -84,6 +84,12 @@
 // block in shared memory with the loader warp instead cost 45% more kernel time on the
 // 65536-query E4M3 workload: one warp's conversion, once per row change, was on the
 // critical path.)
+//
+// Optional E4M3 P V (kP8, msa_fwd_opts_t.debug_flags bit 1): P rounded to E4M3 (scaled so
+// that its largest value is 256) into a shared-memory tile per tile parity, V transposed per
+// block to E4M3 V^T by transpose_e4m3_kernel, and P V as 4 kind::f8f6f4 MMAs with both
+// operands K-major.  Measured on the 65536-query E4M3 workload: 3.84 against 3.85 ms, relative
+// L2 error 9.3e-3 against 1.9e-3 with f16 P V, so f16 P V is the default.
 #include <cfloat>
 
 #include <cuda_bf16.h>
@@ -112,7 +118,9 @@ constexpr uint32_t kCtlBytes = 1024;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;  // a 16-bit 128 x 128 tile (two 16 KB halves)
 
 // Shared-memory layout per input type (offsets from the 1024-aligned base).
-template <bool kFp8>
+// kP8 (E4M3 inputs only): P V on kind::f8f6f4 from an E4M3 V^T copy and an E4M3 P staged in
+// shared memory, instead of f16 V and f16 P in tensor memory
+template <bool kFp8, bool kP8 = false>
 struct Lay {
   static constexpr uint32_t kInTile = kFp8 ? 16384 : 32768;  // Q or K tile in the input type
   static constexpr uint32_t kOffQ = 0;                       // + kInTile * stage
@@ -121,11 +129,14 @@ struct Lay {
   // 16-bit V (bf16, or f16 widened from E4M3): one buffer for bf16 (shared memory is full),
   // two for E4M3 so that the next row's V loads while this row's P V runs
   static constexpr int kVBuf = kFp8 ? 2 : 1;
+  static constexpr uint32_t kVTile = kP8 ? 16384 : kTileBytes;  // one V block (kP8: E4M3 V^T)
   static constexpr uint32_t kOffV = kOffK1 + kInTile;
-  static constexpr uint32_t kOffCtl = kOffV + kVBuf * kTileBytes;
+  static constexpr uint32_t kOffP = kOffV + kVBuf * kVTile;  // kP8: two E4M3 P tiles (128 x 128 bytes)
+  static constexpr uint32_t kOffCtl = kOffP + (kP8 ? 2 * 16384 : 0);
   static constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + alignment slack
 };
-static_assert(Lay<false>::kSmemBytes <= 232448 && Lay<true>::kSmemBytes <= 232448, "shared memory");
+static_assert(Lay<false>::kSmemBytes <= 232448 && Lay<true>::kSmemBytes <= 232448 &&
+                  Lay<true, true>::kSmemBytes <= 232448, "shared memory");
 
 // barrier slots (8 bytes each) at the start of the control area
 enum {
@@ -250,6 +261,55 @@ __device__ __forceinline__ float2 softmax_row(uint32_t (&v)[128], int lim, float
   return make_float2(m2, (l0 + l1) + (l2 + l3));
 }
 
+// E4M3 P for the kind::f8f6f4 P V (positive scales): P = 2^(v * sl2 - mb) with mb = m2 - 8,
+// so P <= 256 (E4M3's largest value is 448) and values down to 2^-14 of the row maximum
+// stay in E4M3's normal range; (mb, l) are returned, l summed from the unrounded P, and
+// the combine merges them like any other base.  The row's 128 keys go to shared memory as
+// one 128-byte K-major row (16-byte chunks swizzled by row % 8).
+template <bool kMasked>
+__device__ __forceinline__ float2 softmax_row_p8(uint32_t (&v)[128], int lim, float sl2, uint8_t* prow, int sw) {
+  float a0 = -FLT_MAX, a1 = -FLT_MAX, a2 = -FLT_MAX, a3 = -FLT_MAX;
+#pragma unroll
+  for (int e = 0; e < 128; e += 8) {
+    float x[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) x[q] = (kMasked && e + q > lim) ? -FLT_MAX : __uint_as_float(v[e + q]);
+    a0 = max3(a0, x[0], x[1]);
+    a1 = max3(a1, x[2], x[3]);
+    a2 = max3(a2, x[4], x[5]);
+    a3 = max3(a3, x[6], x[7]);
+  }
+  const float mb = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2 - 8.f;
+  const uint64_t sl2x2 = pack2(sl2, sl2), negm = pack2(-mb, -mb);
+  uint64_t s0 = 0, s1 = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {  // keys 16 j .. 16 j + 15: one 16-byte chunk
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      const int col = 16 * j + e;
+      float x0, x1;
+      unpack2(ffma2(pack2(__uint_as_float(v[col]), __uint_as_float(v[col + 1])), sl2x2, negm), x0, x1);
+      float p0 = ex2(x0), p1 = ex2(x1);
+      if (kMasked) {
+        if (col > lim) p0 = 0.f;
+        if (col + 1 > lim) p1 = 0.f;
+      }
+      if ((e >> 1) & 1) s1 = fadd2(s1, pack2(p0, p1));
+      else s0 = fadd2(s0, pack2(p0, p1));
+      uint16_t h;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(p1), "f"(p0));
+      if ((e >> 1) & 1) w[e >> 2] |= static_cast<uint32_t>(h) << 16;
+      else w[e >> 2] = h;
+    }
+    *reinterpret_cast<uint4*>(prow + ((j ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  float l0, l1, l2, l3;
+  unpack2(s0, l0, l1);
+  unpack2(s1, l2, l3);
+  return make_float2(mb, (l0 + l1) + (l2 + l3));
+}
+
 // Any finite scale: the row extremum of v * sl2 taken directly (slower, rare).
 template <bool kF16>
 __device__ __forceinline__ float2 softmax_row_any_scale(uint32_t (&v)[128], int lim, float sl2, uint32_t tS) {
@@ -273,14 +333,14 @@ __device__ __forceinline__ float2 softmax_row_any_scale(uint32_t (&v)[128], int 
 
 // kWithhold (a separate instance, test use only): the scheduler warp publishes no work,
 // so every other role's bounded wait expires
-template <bool kFp8, bool kF32P, bool kWithhold = false>
+template <bool kFp8, bool kF32P, bool kWithhold = false, bool kP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
 kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const __grid_constant__ CUtensorMap tmQ, const KvParams p) {
   griddep_wait();
   // (no early griddep_launch: a combine grid left pending for the whole persistent run of
   // this kernel cost 0.09 ms per M3 step; the combine is released when this grid ends)
-  using L = Lay<kFp8>;
+  using L = Lay<kFp8, kP8>;
   const int path = p.force_path ? p.force_path : p.hdr->path;
   if (path != kPathKvOuter) return;
 
@@ -545,10 +605,14 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           }
           if (ok) {
             // V (bf16, or the f16 copy of E4M3 V): two 64-column boxes of 128-byte rows
-            const uint32_t dv = sb + L::kOffV + vb * kTileBytes;
-            mbar_expect_tx(bar(B_VFULL0 + vb), kTileBytes);
-            tma_load_3d(dv, &tmV, 0, g, b * kBlock, bar(B_VFULL0 + vb), pol_kv);
-            tma_load_3d(dv + 16384, &tmV, 64, g, b * kBlock, bar(B_VFULL0 + vb), pol_kv);
+            const uint32_t dv = sb + L::kOffV + vb * L::kVTile;
+            mbar_expect_tx(bar(B_VFULL0 + vb), L::kVTile);
+            if constexpr (kP8) {  // the block's E4M3 V^T: 128 rows (d) of 128 keys, one box
+              tma_load_3d(dv, &tmV, 0, 0, row, bar(B_VFULL0 + vb), pol_kv);
+            } else {
+              tma_load_3d(dv, &tmV, 0, g, b * kBlock, bar(B_VFULL0 + vb), pol_kv);
+              tma_load_3d(dv + 16384, &tmV, 64, g, b * kBlock, bar(B_VFULL0 + vb), pol_kv);
+            }
           }
         }
         ok = __shfl_sync(full, ok, 0);
@@ -578,11 +642,20 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           // O goes over the P of tile u - 1: its P V must have completed
           if (u >= 1 && !(ok = mbar_wait(bar(B_PVDONE0 + ((u - 1) & 3)), ((u - 1) >> 2) & 1))) break;
           tc_fence_after();
-          const uint32_t va = sb + L::kOffV + (vseg % L::kVBuf) * kTileBytes;
+          const uint32_t va = sb + L::kOffV + (vseg % L::kVBuf) * L::kVTile;
+          if constexpr (kP8) {
+            // E4M3 P (shared memory, buffer u % 2) x E4M3 V^T, both K-major: 32 keys per MMA
+            const uint32_t pa = sb + L::kOffP + (u & 1) * 16384;
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_f16_ts(tmem + ro * 128, tmem + r * 128 + k * 8, smem_desc(va + k * 2048, 16384, 1024, 2),
-                       idesc_pv, k > 0);
+            for (int k = 0; k < 4; ++k)
+              mma_f8_ss(tmem + ro * 128, smem_desc(pa + k * 32, 16, 1024, 2), smem_desc(va + k * 32, 16, 1024, 2),
+                        idesc_f8(128, 128, 0, 0), k > 0);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_f16_ts(tmem + ro * 128, tmem + r * 128 + k * 8, smem_desc(va + k * 2048, 16384, 1024, 2),
+                         idesc_pv, k > 0);
+          }
           mma_commit(bar(B_PVDONE0 + r));
         }
         if (!ok) flag_timeout(p.hdr);
@@ -624,10 +697,22 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
       tmem_ld_wait();
       float2 ml;
-      if (neg) ml = softmax_row_any_scale<kFp8>(v, lim, p.sl2, tS);
-      else if (masked) ml = softmax_row<true, kFp8>(v, lim, p.sl2, tS);
-      else ml = softmax_row<false, kFp8>(v, lim, p.sl2, tS);
-      tmem_st_wait();
+      if constexpr (kP8) {
+        // P buffer it % 2 was last read by the P V of tile it - 2 (the host runs this instance
+        // for positive scales only)
+        if (it >= 2) {
+          ok = mbar_wait(bar(B_PVDONE0 + ((it - 2) & 3)), ((it - 2) >> 2) & 1);
+          if (!__all_sync(0xffffffffu, ok)) { flag_timeout(p.hdr); break; }
+        }
+        uint8_t* prow = smem + L::kOffP + (it & 1) * 16384 + (row >> 3) * 1024 + (row & 7) * 128;
+        ml = masked ? softmax_row_p8<true>(v, lim, p.sl2, prow, row & 7) : softmax_row_p8<false>(v, lim, p.sl2, prow, row & 7);
+        fence_proxy_async_smem();  // generic-proxy writes of P before the MMA reads them
+      } else {
+        if (neg) ml = softmax_row_any_scale<kFp8>(v, lim, p.sl2, tS);
+        else if (masked) ml = softmax_row<true, kFp8>(v, lim, p.sl2, tS);
+        else ml = softmax_row<false, kFp8>(v, lim, p.sl2, tS);
+        tmem_st_wait();
+      }
       tc_fence_before();
       mbar_arrive(bar(B_PFULL0 + (it & 3)));
       if (valid) p.pstat[static_cast<size_t>(first) * kGroup + row] = ml;
@@ -729,6 +814,50 @@ cudaError_t launch_widen_e4m3(const void* src, void* dst, int64_t n, const Sched
   return cudaGetLastError();
 }
 
+namespace {
+
+// E4M3 V [Lkv][Hkv][128] -> V^T per (group, block): vt[(g * nblocks + b) * 128 + d][key], 128
+// keys of one d in 128 contiguous bytes (16 KB per block), so that P V can read V as a
+// K-major E4M3 operand.  One CTA per (group, block): the block goes through shared memory
+// (rows padded to 129 bytes), 16-byte loads and stores.
+__global__ void __launch_bounds__(256) transpose_e4m3_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
+                                                             int Hkv, int nblocks, const SchedHeader* __restrict__ hdr,
+                                                             int force_path) {
+  griddep_wait();
+  griddep_launch();
+  if ((force_path ? force_path : hdr->path) != kPathKvOuter) return;
+  __shared__ uint8_t tile[128 * 129];
+  const int gb = blockIdx.x, g = gb / nblocks, b = gb - g * nblocks;
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // key = q / 8, 16-byte chunk q % 8 of its row
+    const int q = t + 256 * i, key = q >> 3, c = q & 7;
+    const uint4 w = __ldcs(reinterpret_cast<const uint4*>(v + ((static_cast<size_t>(b) * kBlock + key) * Hkv + g) * kHeadDim) + c);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) tile[key * 129 + 16 * c + j] = static_cast<uint8_t>(ws[j >> 2] >> (8 * (j & 3)));
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // d = q / 8, keys 16 (q % 8) .. + 15
+    const int q = t + 256 * i, d = q >> 3, k0 = 16 * (q & 7);
+    uint32_t ws[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) ws[j >> 2] |= static_cast<uint32_t>(tile[(k0 + j) * 129 + d]) << (8 * (j & 3));
+    reinterpret_cast<uint4*>(vt + (static_cast<size_t>(gb) * kHeadDim + d) * kBlock)[q & 7] =
+        make_uint4(ws[0], ws[1], ws[2], ws[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_transpose_e4m3(const void* v, void* vt, int Hkv, int nblocks, const SchedHeader* hdr, int force_path,
+                                  cudaStream_t st) {
+  MSA_LAUNCH(transpose_e4m3_kernel, Hkv * nblocks, 256, 0, st, static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt),
+             Hkv, nblocks, hdr, force_path);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   if (a.force_path == kPathQOuter) return cudaSuccess;  // (the kernel would exit at once)
   const msa_schedule* s = a.s;
@@ -768,9 +897,17 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
     // V: bf16, or (E4M3 inputs) the f16 copy made by launch_widen_e4m3, 64 elements per box row
     const uint64_t vstrides[2] = {kHeadDim * 2, static_cast<uint64_t>(s->Hkv) * kHeadDim * 2};
     const uint32_t vbox[3] = {64u, 1, kBlock};
-    if (!encode_tmap(&tmV, fp8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                     fp8 ? a.Vf16 : a.V, dims, vstrides, vbox, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (a.p8) {
+      // E4M3 P V: V^T [Hkv * nblocks][128 d][128 keys] (launch_transpose_e4m3), one block per box
+      const uint64_t tdims[3] = {kBlock, kHeadDim, static_cast<uint64_t>(s->Hkv) * s->nblocks};
+      const uint64_t tstrides[2] = {kBlock, static_cast<uint64_t>(kBlock) * kHeadDim};
+      const uint32_t tbox[3] = {kBlock, kHeadDim, 1};
+      if (!encode_tmap(&tmV, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.Vf16, tdims, tstrides, tbox, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    } else if (!encode_tmap(&tmV, fp8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                            fp8 ? a.Vf16 : a.V, dims, vstrides, vbox, CU_TENSOR_MAP_SWIZZLE_128B)) {
       return cudaErrorInvalidValue;
+    }
   }
   KvParams p;
   p.Q = static_cast<const uint8_t*>(a.Q);
@@ -787,19 +924,20 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   p.cap_e = s->cap_entries;
   p.sl2 = a.scale * a.qk_descale * 1.4426950408889634f;
   p.force_path = a.force_path;
-  static bool attr_set[4] = {false, false, false, false};
-  const int inst = (fp8 ? 1 : 0) | (a.f32p ? 2 : 0);
+  static bool attr_set[5] = {false, false, false, false, false};
+  const int inst = a.p8 ? 4 : (fp8 ? 1 : 0) | (a.f32p ? 2 : 0);
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, KvParams);
   switch (inst) {
     case 0: kern = kv_outer_kernel<false, false>; break;
     case 1: kern = kv_outer_kernel<true, false>; break;
     case 2: kern = kv_outer_kernel<false, true>; break;
-    default: kern = kv_outer_kernel<true, true>; break;
+    case 3: kern = kv_outer_kernel<true, true>; break;
+    default: kern = kv_outer_kernel<true, false, false, true>; break;  // E4M3 P V
   }
   // test use: the bf16 instance whose scheduler publishes no work
   const bool withhold = (a.debug_flags & 1) != 0 && inst == 0;
   if (withhold) kern = kv_outer_kernel<false, false, true>;
-  const uint32_t smem = fp8 ? Lay<true>::kSmemBytes : Lay<false>::kSmemBytes;
+  const uint32_t smem = a.p8 ? Lay<true, true>::kSmemBytes : fp8 ? Lay<true>::kSmemBytes : Lay<false>::kSmemBytes;
   if (withhold) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

@@ -238,10 +238,15 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
   }
   cudaError_t e;
   if (opts->stage_events[0] && (e = cudaEventRecord(opts->stage_events[0], stream))) return from_cuda(e);
-  if (fp8 && force != msa::kPathQOuter && (e = msa::launch_widen_e4m3(V.ptr, s->vf16, v_elems, s->d.hdr, force, stream)))
-    return from_cuda(e);
+  const bool p8 = msa::kv_outer_p8(fp8, f32p, scale, opts->debug_flags);
+  if (fp8 && force != msa::kPathQOuter) {
+    // the KV-outer kernel's V: widened to f16, or (E4M3 P V) transposed per block
+    e = p8 ? msa::launch_transpose_e4m3(V.ptr, s->vf16, s->Hkv, s->nblocks, s->d.hdr, force, stream)
+           : msa::launch_widen_e4m3(V.ptr, s->vf16, v_elems, s->d.hdr, force, stream);
+    if (e) return from_cuda(e);
+  }
   msa::KvOuterArgs a{s, Q.ptr, K.ptr, V.ptr, Hq, s->nblocks * msa::kBlock, scale, force, ctas, fp8, qk_descale, f32p,
-                     opts->debug_flags, s->vf16};
+                     opts->debug_flags, s->vf16, p8};
   if ((e = msa::launch_kv_outer(a, stream))) return from_cuda(e);
   if (opts->stage_events[1] && (e = cudaEventRecord(opts->stage_events[1], stream))) return from_cuda(e);
   if ((e = msa::launch_combine(s, Hq, O, LSE, v_descale, force, f32p, stream))) return from_cuda(e);

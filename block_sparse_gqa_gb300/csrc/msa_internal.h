@@ -186,11 +186,20 @@ struct KvOuterArgs {
   float qk_descale;  // q descale * k descale (1 for bf16)
   bool f32p;         // fp32 partial outputs
   int debug_flags;   // msa_fwd_opts_t.debug_flags
-  const void* Vf16;  // E4M3 inputs: V widened to f16 (launch_widen_e4m3)
+  const void* Vf16;  // E4M3 inputs: V widened to f16 (launch_widen_e4m3), or (p8) V^T
+  bool p8;           // E4M3 P V: P in E4M3 and V^T (launch_transpose_e4m3) instead of f16
 };
+// Whether an E4M3 call runs the E4M3 P V (kind::f8f6f4) instance of the KV-outer kernel:
+// positive scales with bf16 partials, selected by msa_fwd_opts_t.debug_flags bit 1.
+inline bool kv_outer_p8(bool fp8, bool f32p, float scale, int debug_flags) {
+  return fp8 && !f32p && scale > 0.f && (debug_flags & 2) != 0;
+}
 cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st);
 // E4M3 [n] -> f16 [n], exact; n a multiple of 16
 // (exits at once where the device chose the Q-outer path, which widens V in shared memory)
+// E4M3 V [Lkv][Hkv][128] -> V^T [Hkv * nblocks][128 d][128 keys] (exits at once on the Q-outer path)
+cudaError_t launch_transpose_e4m3(const void* v, void* vt, int Hkv, int nblocks, const SchedHeader* hdr, int force_path,
+                                  cudaStream_t st);
 cudaError_t launch_widen_e4m3(const void* src, void* dst, int64_t n, const SchedHeader* hdr, int force_path,
                               cudaStream_t st);
 

@@ -94,7 +94,12 @@ typedef struct {
    * work runs instead, so every other role's bounded wait (2 s) expires: the call then
    * leaves O undefined, sets the schedule's timeout bit (msa_schedule_query returns
    * MSA_ERR_TIMEOUT until the schedule is rebuilt) and the device stays usable.  It
-   * exercises the timeout path without faulting anything. */
+   * exercises the timeout path without faulting anything.  Bit 1 (E4M3 inputs, positive
+   * scale, bf16 partials, KV-outer path): P V on E4M3 tensor cores, with P rounded to E4M3
+   * in shared memory and V transposed per block (E4M3) by a pass before the kernel, in
+   * place of f16 V and f16 P.  Measured on the 65536-query E4M3 workload: 0.3% faster
+   * (3.84 vs 3.85 ms), relative L2 error 9.3e-3 instead of 1.9e-3, so it is not the
+   * default. */
   int debug_flags;
 } msa_fwd_opts_t;
 

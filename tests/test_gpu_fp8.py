@@ -75,6 +75,26 @@ def test_fp8_random_lists(N, Lkv, Hkv, topK):
     assert_parity(Og, Lg, Or, Lr)
 
 
+@pytest.mark.parametrize("N,Lkv,Hkv,topK,sigma,scale", [(2048, 2048, 2, 8, (1.0, 1.0, 1.0), 1 / math.sqrt(128)),
+                                                        (333, 2048, 1, 5, (1.0, 1.0, 1.0), 1 / math.sqrt(128)),
+                                                        (1024, 4096, 2, 12, (4.0, 3.0, 0.01), 0.5)])
+def test_fp8_e4m3_pv_option(N, Lkv, Hkv, topK, sigma, scale):
+    """The optional E4M3 P V of the KV-outer kernel (debug_flags bit 1: P rounded to E4M3 in
+    shared memory, V transposed per block): within the E4M3 tolerance, with pads,
+    duplicates, masked tiles and a sharp softmax."""
+    msa = _msa()
+    Q, K, V, ds, idx = fp8_case(7 * N + Lkv, N, Lkv, Hkv, topK, sigma=sigma)
+    dev = torch.device("cuda")
+    s = msa.build_schedule(torch.from_numpy(np.ascontiguousarray(idx, np.int32)).to(dev), Lkv // 128)
+    O, LSE = msa.sparse_attn_fwd(Q.to(dev), K.to(dev), V.to(dev), s, scale=scale, path="kv_outer", descales=ds,
+                                 debug_flags=2)
+    torch.cuda.synchronize()
+    assert s.status() == 0
+    s.close()
+    Or, Lr = run_oracle(Q, K, V, ds, idx, Lkv, scale)
+    assert_parity(O.float().cpu().numpy(), LSE.cpu().numpy(), Or, Lr)
+
+
 def test_fp8_peaked_scores_and_descales():
     """Large score range (sharp softmax) and descales far from 1."""
     Q, K, V, ds, idx = fp8_case(3, 1024, 4096, 2, 12, sigma=(4.0, 3.0, 0.01))
