@@ -108,7 +108,10 @@ constexpr int kThreads = 512;
 constexpr uint32_t kRegCtl = 72, kRegSoftmax = 176, kRegOut = 88;
 static_assert(kThreads == 512 && 128 * (kRegCtl + 2 * kRegSoftmax + kRegOut) <= 512 * 128,
               "setmaxnreg shares exceed the launch allocation");
-constexpr int kChunkTiles = 8;  // tiles per claimed chunk
+constexpr int kChunkTiles = 8;  // tiles per chunk of tile metadata the scheduler warp reads at once
+// chunks per claim: a CTA takes kClaimChunks * 8 consecutive tiles of the work list at once,
+// so it changes row (a 64 KB K + V load) about once per claim
+constexpr int kClaimChunks = 2;
 constexpr int kRing = 8;        // tile-info ring slots
 constexpr int kQStages = 4;
 // TMEM: four regions of 128 columns.  Tile t computes S (and P over it) in region t % 4
@@ -429,11 +432,21 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           m.qa = in0 ? p.qlist[f0 + j] : 0;
           m.qb = in1 ? p.qlist[f1 + j] : 0;
         };
+        // lane 0 hands out chunk ids: one atomicAdd claims kClaimChunks consecutive chunks
+        int claim_next = 0, claim_left = 0;
+        auto claim = [&]() -> int {
+          if (claim_left == 0) {
+            claim_next = atomicAdd(counter, 1) * kClaimChunks;
+            claim_left = kClaimChunks;
+          }
+          --claim_left;
+          return claim_next++;
+        };
         int c_cur = 0, c_next = 0, c_claim = 0;
         if (lane == 0) {
-          c_cur = atomicAdd(counter, 1);
-          c_next = atomicAdd(counter, 1);
-          c_claim = atomicAdd(counter, 1);
+          c_cur = claim();
+          c_next = claim();
+          c_claim = claim();
         }
         c_cur = __shfl_sync(full, c_cur, 0);
         c_next = __shfl_sync(full, c_next, 0);
@@ -515,7 +528,7 @@ kv_outer_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__
           cur = nxt;
           // claim the chunk after next; the claim made a chunk ago becomes the next one
           const int claimed = __shfl_sync(full, c_claim, 0);
-          if (lane == 0 && claimed * kChunkTiles < T) c_claim = atomicAdd(counter, 1);
+          if (lane == 0 && claimed * kChunkTiles < T) c_claim = claim();
           load_tiles(claimed, nxt);
         }
         if (!ok && lane == 0) flag_timeout(p.hdr);
@@ -951,8 +964,8 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   // again (a memset here would break the launch chain's programmatic dependency)
   // no more CTAs than work-list chunks can exist (decode sizes: a few; also makes the
   // launch cheap where the device picks the Q-outer path and this kernel exits at once)
-  const int64_t max_chunks = (s->cap_tiles + kChunkTiles - 1) / kChunkTiles;
-  const int grid = max_chunks < a.num_ctas ? static_cast<int>(max_chunks) : a.num_ctas;
+  const int64_t max_claims = (s->cap_tiles + kChunkTiles * kClaimChunks - 1) / (kChunkTiles * kClaimChunks);
+  const int grid = max_claims < a.num_ctas ? static_cast<int>(max_claims) : a.num_ctas;
   MSA_LAUNCH(kern, grid, kThreads, smem, st, tmK, tmV, tmQ, p);
   return cudaGetLastError();
 }
