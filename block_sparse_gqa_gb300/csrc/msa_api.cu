@@ -100,6 +100,7 @@ void carve_schedule(msa_schedule* s, char* base) {
   c.base = base;
   msa::SchedDev& d = s->d;
   d.mask = c.take<uint32_t>(static_cast<size_t>(s->R) * s->C);
+  d.mcopy = c.take<uint32_t>(static_cast<size_t>(s->R) * s->C);
   d.rowbase = c.take<int32_t>(static_cast<size_t>(s->R) * (s->C + 1));
   d.counts = c.take<int32_t>(s->R);
   d.offsets = c.take<int32_t>(static_cast<size_t>(s->R) + 1);

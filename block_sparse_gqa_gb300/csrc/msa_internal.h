@@ -115,11 +115,14 @@ struct SchedHeader {
   int32_t ntiles;
   int32_t path;     // AUTO choice: kPathKvOuter or kPathQOuter
   int32_t status;   // sticky kStatus* bits
+  // pad[0]: the KV-outer kernel's chunk counter (cleared by the combine); pad[1]: the mark
+  // pass's bad-index bit, moved into status by the row scan
   int32_t pad[3];
 };
 
 struct SchedDev {
   uint32_t* mask;        // [R][C] bit (i % 32) of word (r, i / 32): query i has an entry in row r
+  uint32_t* mcopy;       // [R][C] the bitmask words as the row scan read them (it clears the bitmask)
   int32_t* rowbase;      // [R][C + 1] exclusive prefix of popcounts along each row
   int32_t* counts;       // [R]
   int32_t* offsets;      // [R + 1]
@@ -145,6 +148,9 @@ struct msa_schedule {
   int N, Hkv, topK, nblocks;
   int R, C, nW;
   int qs_items;  // capacity of the Q-outer split workspace in work items (0: no splitting)
+  // the bitmask and the header's pad words are zero (the last multi-kernel build cleared them),
+  // so the next build needs no memset
+  bool mask_clean;
   int64_t cap_entries, cap_tiles, nseg, nseg_blocks;
   void* dev_base;
   size_t dev_bytes;

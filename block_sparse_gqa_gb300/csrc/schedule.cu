@@ -15,9 +15,14 @@
 //
 // Kernels, in stream order:
 //   mark              (entries<mark>) one thread per list slot: bits for every valid
-//                     entry; bad ids -> sticky status bit
+//                     entry; bad ids -> a bit in the header's pad[1]
 //   rowscan           per row: exclusive popcount prefix over words, row count, tiles
-//                     per (window, row) segment
+//                     per (window, row) segment; each bitmask word is copied to mcopy
+//                     (what the scatter reads) and cleared, and pad[1] becomes the
+//                     header's status, so the next build of the same schedule starts
+//                     from a zero bitmask and header without a memset (the first build,
+//                     and every build into the no-allocation scratch, zero them with two
+//                     memsets, which also break the launches' programmatic dependencies)
 //   scan_small        one CTA: offsets, E, nsb, the Q-outer / KV-outer decision and the
 //                     exclusive scan of the segment tile counts (at most 32768 segments);
 //                     more segments: scan_rows + seg_reduce / seg_top / seg_down
@@ -128,7 +133,7 @@ __device__ __forceinline__ void entries_body(const int32_t* __restrict__ idx, in
     }
     __syncthreads();
   }
-  if (!kScatter && bad) atomicOr(&hdr->status, kStatusBadIndex);
+  if (!kScatter && bad) atomicOr(&hdr->pad[1], kStatusBadIndex);  // the row scan moves it into status
 }
 
 __global__ void __launch_bounds__(kEntThreads)
@@ -140,16 +145,28 @@ k_mark(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, i
                       nullptr, nullptr, hdr, blockIdx.x, gridDim.x);
 }
 
+// The mark pass's bad-index bit becomes the status of this build (status and pad[1] are
+// read and written by one thread of the row scan only).
+__device__ __forceinline__ void take_mark_status(SchedHeader* hdr) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    hdr->status = hdr->pad[1];
+    hdr->pad[1] = 0;
+  }
+}
+
 template <int NT>
-__global__ void __launch_bounds__(NT) k_rowscan(const uint32_t* __restrict__ mask, int R, int C, int nW,
+__global__ void __launch_bounds__(NT) k_rowscan(uint32_t* __restrict__ mask, int R, int C, int nW,
                                                 int32_t* __restrict__ rowbase, int32_t* __restrict__ counts,
-                                                int32_t* __restrict__ segtiles) {
+                                                int32_t* __restrict__ segtiles, uint32_t* __restrict__ mcopy,
+                                                SchedHeader* hdr) {
   griddep_wait();
   griddep_launch();
+  take_mark_status(hdr);
   __shared__ int warp_buf[32];
   constexpr int kCpw = kWindow / kChunk;
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
-    const uint32_t* m = mask + static_cast<size_t>(r) * C;
+    uint32_t* m = mask + static_cast<size_t>(r) * C;
+    uint32_t* mc = mcopy + static_cast<size_t>(r) * C;
     int32_t* rb = rowbase + static_cast<size_t>(r) * (C + 1);
     const int per = (C + NT - 1) / NT;
     const int c0 = min(static_cast<int>(threadIdx.x) * per, C), c1 = min(c0 + per, C);
@@ -158,8 +175,11 @@ __global__ void __launch_bounds__(NT) k_rowscan(const uint32_t* __restrict__ mas
     int total;
     int run = block_exclusive_scan<NT>(sum, &total, warp_buf);
     for (int c = c0; c < c1; ++c) {
+      const uint32_t w = m[c];
       rb[c] = run;
-      run += __popc(m[c]);
+      run += __popc(w);
+      mc[c] = w;
+      m[c] = 0u;
     }
     if (threadIdx.x == 0) {
       rb[C] = total;
@@ -177,15 +197,22 @@ __global__ void __launch_bounds__(NT) k_rowscan(const uint32_t* __restrict__ mas
 
 // k_rowscan for rows of at most 32 bitmask words (N <= 1024 queries: decode and
 // low-reuse sizes, where rows are many and short): one warp per row instead of a CTA.
-__global__ void __launch_bounds__(256) k_rowscan_warp(const uint32_t* __restrict__ mask, int R, int C, int nW,
+__global__ void __launch_bounds__(256) k_rowscan_warp(uint32_t* __restrict__ mask, int R, int C, int nW,
                                                       int32_t* __restrict__ rowbase, int32_t* __restrict__ counts,
-                                                      int32_t* __restrict__ segtiles) {
+                                                      int32_t* __restrict__ segtiles, uint32_t* __restrict__ mcopy,
+                                                      SchedHeader* hdr) {
   griddep_wait();
   griddep_launch();
+  take_mark_status(hdr);
   constexpr int kCpw = kWindow / kChunk;
   const int lane = threadIdx.x & 31;
   for (int64_t r = blockIdx.x * 8ll + (threadIdx.x >> 5); r < R; r += gridDim.x * 8ll) {
-    const int v = lane < C ? __popc(mask[r * C + lane]) : 0;
+    const uint32_t w = lane < C ? mask[r * C + lane] : 0u;
+    const int v = __popc(w);
+    if (lane < C) {
+      mcopy[r * C + lane] = w;
+      mask[r * C + lane] = 0u;
+    }
     int inc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -571,23 +598,31 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
   const int lists_per_cta = kEntThreads / s->topK;  // topK <= 64
   const int ent_grid = grid_for(nl, lists_per_cta, 1 << 20);
   cudaError_t e;
-  // tiny inputs: one CTA (limits keep its serial per-thread loops short)
+  // tiny inputs: one CTA (limits keep its serial per-thread loops short); it zeroes the
+  // bitmask itself and leaves it set
   if (nl * s->topK <= kOneMaxSlots && static_cast<int64_t>(s->R) * s->C <= kOneMaxMaskWords && s->C <= 64 &&
       s->nseg <= kOneMaxSegments) {
+    s->mask_clean = false;
     MSA_LAUNCH(k_schedule_one, 1, kOneThreads, 0, st, indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->R, s->C, s->nW, d,
                s->cap_tiles);
     return cudaGetLastError();
   }
-  if ((e = cudaMemsetAsync(d.mask, 0, sizeof(uint32_t) * static_cast<size_t>(s->R) * s->C, st))) return e;
-  if ((e = cudaMemsetAsync(d.hdr, 0, sizeof(SchedHeader), st))) return e;
+  // the bitmask and the header start at zero: left so by the previous build's row scan, or
+  // zeroed here (first build, or after a build whose launches did not all go through)
+  const bool clean = s->mask_clean;
+  s->mask_clean = false;
+  if (!clean) {
+    if ((e = cudaMemsetAsync(d.mask, 0, sizeof(uint32_t) * static_cast<size_t>(s->R) * s->C, st))) return e;
+    if ((e = cudaMemsetAsync(d.hdr, 0, sizeof(SchedHeader), st))) return e;
+  }
   MSA_LAUNCH(k_mark, ent_grid, kEntThreads, 0, st, indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C, lists_per_cta,
                                             d.mask, d.hdr);
   if (s->C <= 32)
     MSA_LAUNCH(k_rowscan_warp, grid_for(s->R, 8, 1 << 20), 256, 0, st, d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
-                                                             d.segoff);
+               d.segoff, d.mcopy, d.hdr);
   else
     MSA_LAUNCH(k_rowscan<256>, grid_for(s->R, 1, 1 << 20), 256, 0, st, d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
-                                                               d.segoff);
+               d.segoff, d.mcopy, d.hdr);
   if (s->nseg <= 1024 * kSmallSegPer) {
     MSA_LAUNCH(k_scan_small<1024>, 1, 1024, 0, st, d.counts, s->R, s->N, d.offsets, d.segoff, static_cast<int>(s->nseg),
                                            d.window_tiles, s->nW, d.hdr);
@@ -600,9 +635,12 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
   }
   const int tiles_grid = grid_for(s->nseg, kEntThreads / 32, 1 << 16);  // a warp per segment
   MSA_LAUNCH(k_scatter_tiles, ent_grid + tiles_grid, kEntThreads, 0, st, 
-      indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C, lists_per_cta, ent_grid, d.mask, d.rowbase, d.offsets,
+      indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C, lists_per_cta, ent_grid, d.mcopy, d.rowbase, d.offsets,
       d.qlist, d.slot, d.cmap, d.blist, d.segoff, s->nseg, s->R, d.tiles, s->cap_tiles, d.hdr);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  // every launch went through: the row scan has cleared what the next build needs at zero
+  s->mask_clean = e == cudaSuccess;
+  return e;
 }
 
 }  // namespace msa

@@ -99,6 +99,31 @@ def test_schedule_deterministic_and_reusable():
     s.close()
 
 
+@pytest.mark.parametrize("name", ["m3", "lowreuse"])
+def test_schedule_rebuilds_start_clean(name):
+    """A rebuild of the same schedule starts from the bitmask and status the previous
+    build's row scan cleared (no memset after the first build): other lists, a bad id
+    (flagged), then clean lists again (the flag is gone).  m3 takes the CTA-per-row scan,
+    lowreuse (8 bitmask words per row) the warp-per-row one."""
+    msa = _msa()
+    cfg = workloads.CONFIGS[name]
+    idx = workloads.make_indices(cfg)
+    s, _ = gpu_schedule(idx, cfg.nblocks)
+    bad = workloads.make_indices(cfg, seed=5)
+    bad[3, 1, 2] = cfg.nblocks + 7  # invalid: ignored and flagged
+    _, b = gpu_schedule(bad, cfg.nblocks, schedule=s)
+    ref_b = oracle.schedule(bad, Lkv=cfg.Lkv)
+    assert b["status"] & 1 and ref_b["status"] == 1
+    assert_same(b, ref_b, cfg.N, cfg.Lkv)
+    assert msa.lib().msa_schedule_status(s.handle) == 5
+    for seed in (6, None):
+        idx2 = workloads.make_indices(cfg, seed=seed)
+        _, c = gpu_schedule(idx2, cfg.nblocks, schedule=s)
+        assert c["status"] == 0 and msa.lib().msa_schedule_status(s.handle) == 0
+        assert_same(c, oracle.schedule(idx2, Lkv=cfg.Lkv), cfg.N, cfg.Lkv)
+    s.close()
+
+
 @pytest.mark.parametrize("N,Lkv,Hkv,topK", [(1, 131072, 4, 16), (5, 2048, 1, 3), (31, 65536, 4, 8), (33, 8192, 2, 15),
                                             (64, 4096, 1, 16), (64, 4096, 4, 4), (65, 4096, 4, 4), (16, 65536, 4, 17),
                                             (300, 2048, 1, 3), (1024, 1024, 1, 1)])
