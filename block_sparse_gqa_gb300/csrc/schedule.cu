@@ -319,6 +319,8 @@ __device__ int block_scan_array(const int32_t* in, int32_t* out, int n, int* sm,
   return carry;
 }
 
+constexpr int kRegItems = 16;  // values per thread of the one-pass scan of both small arrays
+
 // Rows (as k_scan_rows) and, in the same CTA, the exclusive scan of the per-(window,
 // row) segment tile counts when there are few segments (at most NT * kSmallSegPer).
 constexpr int kSmallSegPer = 32;
@@ -327,6 +329,84 @@ template <int NT>
 __device__ void scan_small_body(const int32_t* __restrict__ counts, int R, int N, int32_t* __restrict__ offsets,
                                 int32_t* __restrict__ seg, int nseg, int32_t* __restrict__ window_tiles, int nW,
                                 SchedHeader* hdr, int* warp_buf, int* sm) {
+  // The one-pass scan pays where the chunked one needs more than two passes (measured on
+  // GB300: 16,384 rows and segments, 0.1877 -> 0.1852 ms per low-reuse step; at 256 rows and
+  // 1,024 segments, one chunk each, it was 1.5 us slower than the chunked scan)
+  constexpr int kCh = NT * kScanItems;
+  if (R <= NT * kRegItems && nseg <= NT * kRegItems && (R + kCh - 1) / kCh + (nseg + kCh - 1) / kCh > 2) {
+    // both arrays held in registers, their loads issued together: warp w owns the
+    // 32 * kRegItems consecutive values from w * 32 * kRegItems, lane l the ones at
+    // offsets 32 j + l (coalesced), scanned per j across the lanes with a running carry;
+    // one cross-warp scan of the warp totals (row entries, segment tiles, nonempty rows)
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int base = w * 32 * kRegItems;
+    int c[kRegItems], g[kRegItems];
+#pragma unroll
+    for (int j = 0; j < kRegItems; ++j) {
+      const int i = base + 32 * j + lane;
+      c[j] = i < R ? counts[i] : 0;
+      g[j] = i < nseg ? seg[i] : 0;
+    }
+    int cx = 0, cy = 0, cz = 0;  // warp carries
+    const bool has = base < R || base < nseg;  // warp-uniform: warps past both arrays skip the scan
+#pragma unroll
+    for (int j = 0; j < kRegItems && has; ++j) {
+      int x = c[j], y = g[j];
+      cz += __popc(__ballot_sync(0xffffffffu, c[j] > 0));
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, x, o), b = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) {
+          x += a;
+          y += b;
+        }
+      }
+      c[j] = cx + x - c[j];  // exclusive, within the warp
+      g[j] = cy + y - g[j];
+      cx += __shfl_sync(0xffffffffu, x, 31);
+      cy += __shfl_sync(0xffffffffu, y, 31);
+    }
+    if (lane == 0) {
+      warp_buf[w] = cx;
+      warp_buf[32 + w] = cy;
+      warp_buf[64 + w] = cz;
+    }
+    __syncthreads();
+    if (w < 3) {  // warp k: exclusive scan of the k-th total over the warps
+      const int v = lane < NT / 32 ? warp_buf[32 * w + lane] : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += a;
+      }
+      if (lane < NT / 32) warp_buf[32 * w + lane] = x - v;
+      if (lane == 31) warp_buf[96 + w] = x;  // the CTA total
+    }
+    __syncthreads();
+    const int ox = warp_buf[w], oy = warp_buf[32 + w];
+#pragma unroll
+    for (int j = 0; j < kRegItems; ++j) {
+      const int i = base + 32 * j + lane;
+      if (i < R) offsets[i] = ox + c[j];
+      if (i < nseg) {
+        const int e = oy + g[j];
+        seg[i] = e;
+        if (i % R == 0) window_tiles[i / R] = e;
+      }
+    }
+    if (threadIdx.x == 0) {
+      const int E = warp_buf[96], tiles = warp_buf[97], nsb = warp_buf[98];
+      offsets[R] = E;
+      hdr->entries = E;
+      hdr->nsb = nsb;
+      hdr->path = dispatch_path(E, nsb);  // (msa_internal.h)
+      seg[nseg] = tiles;
+      window_tiles[nW] = tiles;
+      hdr->ntiles = tiles;
+    }
+    return;
+  }
   int nsb = 0;
   const int total = block_scan_array<NT>(counts, offsets, R, sm, warp_buf, &nsb, nullptr, R);
   if (threadIdx.x == 0) {
@@ -350,7 +430,7 @@ __global__ void __launch_bounds__(NT) k_scan_small(const int32_t* __restrict__ c
                                                    SchedHeader* hdr) {
   griddep_wait();
   griddep_launch();
-  __shared__ int warp_buf[32];
+  __shared__ int warp_buf[4 * 32];
   __shared__ int sm[NT * kScanItems + NT * kScanItems / 32];
   scan_small_body<NT>(counts, R, N, offsets, seg, nseg, window_tiles, nW, hdr, warp_buf, sm);
 }
@@ -495,7 +575,7 @@ k_schedule_one(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nb
                SchedDev d, int64_t cap_tiles) {
   griddep_wait();
   griddep_launch();
-  __shared__ int warp_buf[32];
+  __shared__ int warp_buf[4 * 32];
   __shared__ int s_bad;
   __shared__ int sm[kOneThreads * kScanItems + kOneThreads * kScanItems / 32];
   constexpr int kCpw = kWindow / kChunk;

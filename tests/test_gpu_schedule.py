@@ -170,3 +170,20 @@ def test_dispatch_at_the_boundary(N, expected):
     Or, Lr, _ = oracle.attn_fwd(bits(Q), bits(K), bits(V), idx, Lkv=Lkv, scale=0.09, qids=qids)
     rel, mabs, lerr = compare_outputs(O.float().cpu().numpy()[qids], LSE.cpu().numpy()[qids], Or, Lr)
     assert rel <= BF16_REL_L2 and mabs <= BF16_MAX_ABS and lerr <= LSE_MAX_ABS, (rel, mabs, lerr)
+
+
+def test_schedule_one_pass_scan_ragged():
+    """Rows and segments that the chunked scan would take in more than two passes go through
+    the one-pass scan (values held in registers, 512 per warp): 3 heads x 3000 blocks =
+    9000 rows and 9000 segments, the last warp's share partly filled."""
+    rng = np.random.default_rng(11)
+    N, Hkv, topK, nb = 300, 3, 5, 3000
+    Lkv = nb * 128
+    idx = rng.integers(-1, nb, size=(N, Hkv, topK)).astype(np.int32)
+    idx[:, :, 0] = ((Lkv - N + np.arange(N)) // 128)[:, None]
+    idx[::3, :, 3] = idx[::3, :, 1]
+    ref = oracle.schedule(idx, Lkv=Lkv)
+    s, exp = gpu_schedule(idx, nb)
+    assert exp["status"] == 0
+    assert_same(exp, ref, N, Lkv)
+    s.close()
