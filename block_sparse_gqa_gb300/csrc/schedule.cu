@@ -14,8 +14,11 @@
 // that follows is a pure function of the input and rows come out sorted by query.
 //
 // Kernels, in stream order:
-//   mark              (entries<mark>) one thread per list slot: bits for every valid
-//                     entry; bad ids -> a bit in the header's pad[1]
+//   mark              bits for every valid entry; bad ids -> a bit in the header's pad[1].
+//                     k_mark_cols: a CTA per (32-query bitmask column, KV head) ORs its
+//                     queries' bits per block in shared memory and stores each nonzero word
+//                     once; k_mark (entries<mark>, one thread per list slot, global atomics)
+//                     where the blocks are many and the columns few
 //   rowscan           per row: exclusive popcount prefix over words, row count, tiles
 //                     per (window, row) segment; each bitmask word is copied to mcopy
 //                     (what the scatter reads) and cleared, and pad[1] becomes the
@@ -154,6 +157,55 @@ __device__ __forceinline__ void take_mark_status(SchedHeader* hdr) {
   }
 }
 
+// Mark by bitmask columns: CTA (w, g) takes the lists of queries 32 w .. 32 w + 31 in KV
+// head g, ORs each entry's query bit into a shared-memory word per block, and stores each
+// nonzero word once, with no global atomics (this CTA is the only writer of word w of the
+// head's rows; the bitmask is zero beforehand: cleared by the previous build's row scan, or
+// by a memset).  The entry rule is entries<>'s.  Shared memory: nblocks words, then the
+// 32 * topK list slots.
+constexpr int kMarkThreads = 256;
+constexpr size_t kMarkColsMaxSmem = 96 * 1024;
+__global__ void __launch_bounds__(kMarkThreads)
+k_mark_cols(const int32_t* __restrict__ idx, int N, int Hkv, int topK, int nblocks, int Lkv, int C,
+            uint32_t* __restrict__ mask, SchedHeader* hdr) {
+  griddep_wait();
+  griddep_launch();
+  extern __shared__ uint32_t s_bits[];
+  int32_t* s_idx = reinterpret_cast<int32_t*>(s_bits + nblocks);
+  const int w = blockIdx.x / Hkv, g = blockIdx.x - (blockIdx.x / Hkv) * Hkv;
+  const int t = threadIdx.x, nsl = 32 * topK;
+  for (int b = t; b < nblocks; b += kMarkThreads) s_bits[b] = 0u;
+  for (int e = t; e < nsl; e += kMarkThreads) {
+    const int qi = e / topK, k = e - qi * topK, i = 32 * w + qi;
+    s_idx[e] = i < N ? idx[(static_cast<int64_t>(i) * Hkv + g) * topK + k] : -1;
+  }
+  __syncthreads();
+  bool bad = false;
+  for (int e = t; e < nsl; e += kMarkThreads) {
+    const int qi = e / topK, k = e - qi * topK, i = 32 * w + qi;
+    if (i >= N) continue;
+    const int b = s_idx[e];
+    if (b < -1 || b >= nblocks) {
+      bad = true;
+      continue;
+    }
+    if (b < 0 || b > (Lkv - N + i) / kBlock) continue;
+    bool first = true;
+    for (int k2 = 0; k2 < k; ++k2)
+      if (s_idx[qi * topK + k2] == b) {
+        first = false;
+        break;
+      }
+    if (first) atomicOr(&s_bits[b], 1u << qi);
+  }
+  if (bad) atomicOr(&hdr->pad[1], kStatusBadIndex);  // the row scan moves it into status
+  __syncthreads();
+  for (int b = t; b < nblocks; b += kMarkThreads) {
+    const uint32_t v = s_bits[b];
+    if (v) mask[(static_cast<size_t>(g) * nblocks + b) * C + w] = v;
+  }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(NT) k_rowscan(uint32_t* __restrict__ mask, int R, int C, int nW,
                                                 int32_t* __restrict__ rowbase, int32_t* __restrict__ counts,
@@ -164,22 +216,44 @@ __global__ void __launch_bounds__(NT) k_rowscan(uint32_t* __restrict__ mask, int
   take_mark_status(hdr);
   __shared__ int warp_buf[32];
   constexpr int kCpw = kWindow / kChunk;
+  constexpr int kWarps = NT / 32;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  // warp wid scans the words [s0, s1) of the row, lane l taking words s0 + 32 j + l (coalesced)
+  const int seg = ((C + kWarps - 1) / kWarps + 31) & ~31;
+  const int s0 = min(wid * seg, C), s1 = min(s0 + seg, C);
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
     uint32_t* m = mask + static_cast<size_t>(r) * C;
     uint32_t* mc = mcopy + static_cast<size_t>(r) * C;
     int32_t* rb = rowbase + static_cast<size_t>(r) * (C + 1);
-    const int per = (C + NT - 1) / NT;
-    const int c0 = min(static_cast<int>(threadIdx.x) * per, C), c1 = min(c0 + per, C);
     int sum = 0;
-    for (int c = c0; c < c1; ++c) sum += __popc(m[c]);
-    int total;
-    int run = block_exclusive_scan<NT>(sum, &total, warp_buf);
-    for (int c = c0; c < c1; ++c) {
-      const uint32_t w = m[c];
-      rb[c] = run;
-      run += __popc(w);
-      mc[c] = w;
-      m[c] = 0u;
+    for (int c = s0 + lane; c < s1; c += 32) sum += __popc(m[c]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) warp_buf[wid] = sum;
+    __syncthreads();
+    int run = 0, total = 0;  // this warp's prefix and the row total
+#pragma unroll
+    for (int q = 0; q < kWarps; ++q) {
+      const int v = warp_buf[q];
+      run += q < wid ? v : 0;
+      total += v;
+    }
+    for (int c0 = s0; c0 < s1; c0 += 32) {  // warp-uniform trip count (the shuffles below)
+      const int c = c0 + lane;
+      const uint32_t w = c < s1 ? m[c] : 0u;
+      const int v = __popc(w);
+      int inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (c < s1) {
+        rb[c] = run + inc - v;
+        mc[c] = w;
+        m[c] = 0u;
+      }
+      run += __shfl_sync(0xffffffffu, inc, 31);
     }
     if (threadIdx.x == 0) {
       rb[C] = total;
@@ -695,8 +769,25 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
     if ((e = cudaMemsetAsync(d.mask, 0, sizeof(uint32_t) * static_cast<size_t>(s->R) * s->C, st))) return e;
     if ((e = cudaMemsetAsync(d.hdr, 0, sizeof(SchedHeader), st))) return e;
   }
-  MSA_LAUNCH(k_mark, ent_grid, kEntThreads, 0, st, indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C, lists_per_cta,
-                                            d.mask, d.hdr);
+  // the column mark clears and scans nblocks shared words per CTA: where that is more than four
+  // times the CTA's 32 * topK list slots (few, wide columns: 256 queries over 4096 blocks took
+  // 1.8 us longer per step than with the atomic mark), the atomic mark stays.  Measured per
+  // step on GB300 against the atomic mark: M3 -1.3 us, the long workload -11 us, fp8 -37 us.
+  const size_t mark_smem = sizeof(uint32_t) * (static_cast<size_t>(s->nblocks) + 32 * static_cast<size_t>(s->topK));
+  if (mark_smem <= kMarkColsMaxSmem && s->nblocks <= 4 * 32 * s->topK) {
+    static bool mark_attr = false;  // (a per-function attribute: set once per process)
+    if (!mark_attr) {
+      if ((e = cudaFuncSetAttribute(k_mark_cols, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kMarkColsMaxSmem))))
+        return e;
+      mark_attr = true;
+    }
+    MSA_LAUNCH(k_mark_cols, s->C * s->Hkv, kMarkThreads, mark_smem, st, indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv,
+               s->C, d.mask, d.hdr);
+  } else {
+    MSA_LAUNCH(k_mark, ent_grid, kEntThreads, 0, st, indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv, s->C,
+               lists_per_cta, d.mask, d.hdr);
+  }
   if (s->C <= 32)
     MSA_LAUNCH(k_rowscan_warp, grid_for(s->R, 8, 1 << 20), 256, 0, st, d.mask, s->R, s->C, s->nW, d.rowbase, d.counts,
                d.segoff, d.mcopy, d.hdr);
