@@ -719,11 +719,8 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t st) {
   p.R = s->R;
   p.cap_e = s->cap_entries;
   p.sl2 = a.scale * 1.4426950408889634f;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if ((e = cudaFuncSetAttribute(bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes))) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if ((e = set_smem_limit(bwd_kv_kernel, kSmemBytes, attr_done))) return e;
   if (a.ev[0] && (e = cudaEventRecord(a.ev[0], st))) return e;
   bwd_kv_kernel<<<a.num_ctas, kThreads, kSmemBytes, st>>>(tmK, tmV, tmQ, tmDO, tmP128, tmP16, p);
   if ((e = cudaGetLastError())) return e;

@@ -937,7 +937,7 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   p.cap_e = s->cap_entries;
   p.sl2 = a.scale * a.qk_descale * 1.4426950408889634f;
   p.force_path = a.force_path;
-  static bool attr_set[5] = {false, false, false, false, false};
+  static std::atomic<uint64_t> attr_done[5];
   const int inst = a.p8 ? 4 : (fp8 ? 1 : 0) | (a.f32p ? 2 : 0);
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, KvParams);
   switch (inst) {
@@ -954,10 +954,9 @@ cudaError_t launch_kv_outer(const KvOuterArgs& a, cudaStream_t st) {
   if (withhold) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-  } else if (!attr_set[inst]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  } else {
+    cudaError_t e = set_smem_limit(kern, static_cast<int>(smem), attr_done[inst]);
     if (e != cudaSuccess) return e;
-    attr_set[inst] = true;
   }
   // the chunk counter this launch claims its work from is zero: the schedule build clears the
   // header and the combine kernel that follows every launch of this kernel clears the counter

@@ -660,15 +660,15 @@ cudaError_t launch_q_outer(const msa_schedule* s, const void* Q, const void* K, 
       return cudaErrorInvalidValue;
   }
   }
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<uint64_t> attr_done[4];
+  {
     cudaError_t e = cudaSuccess;
+    int i = 0;
     for (auto* k : {q_outer_kernel<false, false>, q_outer_kernel<true, false>})
-      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QoLay<false>::kSmemBytes);
+      if (e == cudaSuccess) e = set_smem_limit(k, static_cast<int>(QoLay<false>::kSmemBytes), attr_done[i++]);
     for (auto* k : {q_outer_kernel<false, true>, q_outer_kernel<true, true>})
-      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QoLay<true>::kSmemBytes);
+      if (e == cudaSuccess) e = set_smem_limit(k, static_cast<int>(QoLay<true>::kSmemBytes), attr_done[i++]);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   QoParams p;
   p.blist = s->d.blist;

@@ -472,11 +472,10 @@ cudaError_t launch_tiles(const void* Q, const void* K, const void* V, int N, int
     if (!encode_tmap(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, V, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static std::atomic<uint64_t> attr_done{0};
+  {
+    cudaError_t e = set_smem_limit(tiles_kernel, static_cast<int>(kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   TlParams p;
   p.lists = lists;

@@ -1,5 +1,6 @@
 // Internal declarations shared by the libmsa translation units.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <utility>
 
@@ -27,6 +28,22 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Raises kernel `kern`'s dynamic shared-memory limit to `bytes` on the current device.
+// Function attributes belong to each device's context, so every device a process launches
+// on gets its own call; `done` (one per call site, one bit per device ordinal below 64)
+// skips it afterwards.  Two threads racing on a first call both set the same value.
+template <class K>
+inline cudaError_t set_smem_limit(K kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
 }
 
 // launch_pdl inside a function returning cudaError_t: returns the launch error, if any

@@ -775,13 +775,8 @@ cudaError_t enqueue_schedule(msa_schedule* s, const int32_t* indices, cudaStream
   // step on GB300 against the atomic mark: M3 -1.3 us, the long workload -11 us, fp8 -37 us.
   const size_t mark_smem = sizeof(uint32_t) * (static_cast<size_t>(s->nblocks) + 32 * static_cast<size_t>(s->topK));
   if (mark_smem <= kMarkColsMaxSmem && s->nblocks <= 4 * 32 * s->topK) {
-    static bool mark_attr = false;  // (a per-function attribute: set once per process)
-    if (!mark_attr) {
-      if ((e = cudaFuncSetAttribute(k_mark_cols, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(kMarkColsMaxSmem))))
-        return e;
-      mark_attr = true;
-    }
+    static std::atomic<uint64_t> mark_attr{0};
+    if ((e = set_smem_limit(k_mark_cols, static_cast<int>(kMarkColsMaxSmem), mark_attr))) return e;
     MSA_LAUNCH(k_mark_cols, s->C * s->Hkv, kMarkThreads, mark_smem, st, indices, s->N, s->Hkv, s->topK, s->nblocks, Lkv,
                s->C, d.mask, d.hdr);
   } else {

@@ -347,11 +347,9 @@ cudaError_t launch_select_r1(const void* Q, const void* K, int N, int Lkv, int H
   float* qbar = static_cast<float*>(workspace);
   float* kbar = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((q + 255) / 256) * 256);
   const uint32_t smem = select_smem_bytes(nblocks, 1);
-  static uint32_t smem_set = 0;
-  if (smem > 48 * 1024 && smem > smem_set) {
+  if (smem > 48 * 1024) {  // (a per-device attribute, set on every call: the selector is not on the timed path)
     cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    smem_set = smem;
   }
   k_pool_keys<<<dim3(nblocks, Hkv), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(K), Hkv, nblocks, kbar);
   k_pool_queries<<<dim3(ntiles, Hkv), 1024, 0, st>>>(static_cast<const __nv_bfloat16*>(Q), N, Hq, qbar);
@@ -367,11 +365,9 @@ cudaError_t launch_select_r4(const void* Q, const void* K, int N, int Lkv, int H
   float* qrep = static_cast<float*>(workspace);
   float* krep = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((q + 255) / 256) * 256);
   const uint32_t smem = select_smem_bytes(nblocks, 4);
-  static uint32_t smem_set = 0;
-  if (smem > 48 * 1024 && smem > smem_set) {
+  if (smem > 48 * 1024) {  // (a per-device attribute, set on every call: the selector is not on the timed path)
     cudaError_t e = cudaFuncSetAttribute(k_select4, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    smem_set = smem;
   }
   k_pool_keys4<<<dim3(nblocks, Hkv), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(K), Hkv, nblocks, krep);
   k_pool_queries4<<<dim3(ntiles, Hkv), 1024, 0, st>>>(static_cast<const __nv_bfloat16*>(Q), N, Hq, qrep);
