@@ -222,7 +222,9 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
   const bool f32p = opts->partials_fp32 == 1;
   msa_status_t st = ensure_partials(s, msa::kGroup, f32p ? 4 : 2);
   if (st != MSA_OK) return st;
-  const int force = opts->path == MSA_PATH_AUTO ? 0 : static_cast<int>(opts->path);
+  // AUTO where the sizes alone fix the device's choice (decode sizes): the Q-outer kernel only
+  const int force = opts->path != MSA_PATH_AUTO ? static_cast<int>(opts->path)
+                    : msa::q_outer_certain(s->N, s->Hkv, s->topK) ? msa::kPathQOuter : 0;
   const float qk_descale = fp8 ? opts->q_descale * opts->k_descale : 1.f;
   const float v_descale = fp8 ? opts->v_descale : 1.f;
   const cudaStream_t stream = opts->stream;
@@ -250,7 +252,8 @@ msa_status_t msa_sparse_attn_fwd(msa_tensor_t Q, msa_tensor_t K, msa_tensor_t V,
                      opts->debug_flags, s->vf16, p8};
   if ((e = msa::launch_kv_outer(a, stream))) return from_cuda(e);
   if (opts->stage_events[1] && (e = cudaEventRecord(opts->stage_events[1], stream))) return from_cuda(e);
-  if ((e = msa::launch_combine(s, Hq, O, LSE, v_descale, force, f32p, stream))) return from_cuda(e);
+  if (force != msa::kPathQOuter && (e = msa::launch_combine(s, Hq, O, LSE, v_descale, force, f32p, stream)))
+    return from_cuda(e);
   if ((e = msa::launch_q_outer(s, Q.ptr, K.ptr, V.ptr, Hq, scale, O, LSE, force, stream, fp8, qk_descale, v_descale)))
     return from_cuda(e);
   if (opts->stage_events[2] && (e = cudaEventRecord(opts->stage_events[2], stream))) return from_cuda(e);

@@ -100,6 +100,14 @@ constexpr int kPathQOuter = 2;
 __host__ __device__ constexpr int dispatch_path(int64_t entries, int64_t nsb) {
   return 10 * entries - 13 * nsb > 35000 ? kPathKvOuter : kPathQOuter;
 }
+// True when dispatch_path picks Q-outer for every schedule of these sizes, so the host can
+// launch the Q-outer kernel alone (no KV-outer or combine launch that would only exit).
+// E <= E_max = N * Hkv * topK, and a (KV head, block) row holds at most N entries, so
+// nsb >= E / N and 10 E - 13 nsb <= E (10 - 13 / N) <= E_max (10 - 13 / N).  Every N = 1
+// call qualifies, and at Hkv 4, topK 16 every N up to 55.
+constexpr bool q_outer_certain(int64_t N, int64_t Hkv, int64_t topK) {
+  return N * Hkv * topK * (10 * N - 13) <= 35000 * N;
+}
 
 constexpr int kStatusBadIndex = 1;
 constexpr int kStatusTimeout = 2;

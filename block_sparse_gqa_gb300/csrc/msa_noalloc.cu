@@ -122,7 +122,8 @@ extern "C" msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int 
   s.last_stream = stream;
   const int ctas = opts->num_ctas > 0 ? opts->num_ctas : device_sms();
   if (ctas < 1) return MSA_ERR_CUDA;
-  const int force = opts->path == MSA_PATH_AUTO ? 0 : static_cast<int>(opts->path);
+  const int force = opts->path != MSA_PATH_AUTO ? static_cast<int>(opts->path)
+                    : msa::q_outer_certain(N, Hkv, topK) ? msa::kPathQOuter : 0;
   const int Hq = static_cast<int>(Q.h);
   cudaError_t e;
   if ((e = msa::enqueue_schedule(&s, indices, stream))) return msa::status_from_cuda(e);
@@ -130,7 +131,8 @@ extern "C" msa_status_t msa_sparse_attn_fwd_noalloc(const int32_t* indices, int 
   msa::KvOuterArgs a{&s, Q.ptr, K.ptr, V.ptr, Hq, nblocks * msa::kBlock, scale, force, ctas, false, 1.f, false, 0};
   if ((e = msa::launch_kv_outer(a, stream))) return msa::status_from_cuda(e);
   if (opts->stage_events[1] && (e = cudaEventRecord(opts->stage_events[1], stream))) return msa::status_from_cuda(e);
-  if ((e = msa::launch_combine(&s, Hq, O, LSE, 1.f, force, false, stream))) return msa::status_from_cuda(e);
+  if (force != msa::kPathQOuter && (e = msa::launch_combine(&s, Hq, O, LSE, 1.f, force, false, stream)))
+    return msa::status_from_cuda(e);
   if ((e = msa::launch_q_outer(&s, Q.ptr, K.ptr, V.ptr, Hq, scale, O, LSE, force, stream)))
     return msa::status_from_cuda(e);
   if (opts->stage_events[2] && (e = cudaEventRecord(opts->stage_events[2], stream))) return msa::status_from_cuda(e);
