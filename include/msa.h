@@ -60,7 +60,9 @@ typedef enum { MSA_BF16 = 0, MSA_FP8_E4M3 = 1 } msa_dtype_t;
  * the number of distinct (query, KV head, block) entries and nsb the number of distinct
  * (KV head, block) pairs (the page's B200 rule, nsb / N < 2.85, picked the slower path at 19
  * of 52 measured GB300 points).  The choice is made on the device by msa_build_schedule;
- * no device-to-host copy is needed. */
+ * no device-to-host copy is needed.  Where the sizes alone decide it (E <= N * Hkv * topK
+ * and nsb >= E / N, so N * Hkv * topK * (10 N - 13) <= 35000 N means Q-outer for any lists:
+ * every N = 1 call), the forward launches only the Q-outer kernel; the result is the same. */
 typedef enum { MSA_PATH_AUTO = 0, MSA_PATH_KV_OUTER = 1, MSA_PATH_Q_OUTER = 2 } msa_path_t;
 
 /* Opaque schedule: the reverse index of one indices tensor plus its device
