@@ -41,12 +41,17 @@ def kernels_per_step(cfg):
     most 1024 list slots, 8192 bitmask words and 8192 segments; else mark, rowscan, one
     fused scan or four scan kernels when there are more than 32768 (window, row)
     segments, scatter + tiles in one launch) + kv_outer + combine + q_outer (the two
-    attention kernels not chosen exit at once)."""
+    attention kernels not chosen exit at once), plus the E4M3 V widening; where the sizes
+    alone fix AUTO's choice (N * Hkv * topK * (10 N - 13) <= 35000 N) only q_outer."""
     rows, words = cfg.Hkv * cfg.nblocks, -(-cfg.N // 32)
     nseg = -(-cfg.N // WINDOW) * rows
     if cfg.N * cfg.Hkv * cfg.topK <= 1024 and rows * words <= 8192 and words <= 64 and nseg <= 8192:
-        return 1 + 3
-    return (4 if nseg <= 32768 else 7) + 3
+        sched = 1
+    else:
+        sched = 4 if nseg <= 32768 else 7
+    if cfg.N * cfg.Hkv * cfg.topK * (10 * cfg.N - 13) <= 35000 * cfg.N:
+        return sched + 1
+    return sched + 3 + (1 if cfg.dtype == "e4m3" else 0)
 
 
 def parse_args():
