@@ -187,3 +187,32 @@ def test_schedule_one_pass_scan_ragged():
     assert exp["status"] == 0
     assert_same(exp, ref, N, Lkv)
     s.close()
+
+
+@pytest.mark.parametrize("N,expected", [(55, 2), (56, 1)])
+def test_host_decided_auto_at_its_bound(N, expected):
+    """Where N * Hkv * topK * (10 N - 13) <= 35000 N the sizes alone fix AUTO's choice and the
+    forward launches the Q-outer kernel only; at Hkv 4, topK 16 that holds up to N = 55.
+    Lists in which every query picks the same 16 blocks make 10 E - 13 nsb as large as it
+    can be: 34368 at N = 55 (Q-outer, decided on the host) and 35008 at N = 56 (KV-outer,
+    decided on the device).  The device's choice equals the oracle's on both sides, and the
+    AUTO forward matches the oracle."""
+    Lkv, Hkv, topK = 16384, 4, 16
+    idx = np.ascontiguousarray(np.broadcast_to(np.arange(topK, dtype=np.int32), (N, Hkv, topK)))
+    ref = oracle.schedule(idx, Lkv=Lkv)
+    assert 10 * ref["E"] - 13 * ref["nsb"] == (34368 if N == 55 else 35008)
+    s, exp = gpu_schedule(idx, Lkv // 128)
+    assert exp["path"] == oracle.dispatch(ref["E"], ref["nsb"]) == expected
+    gen = torch.Generator().manual_seed(N)
+    Q = torch.randn((N, 16 * Hkv, 128), generator=gen).to(torch.bfloat16)
+    K = torch.randn((Lkv, Hkv, 128), generator=gen).to(torch.bfloat16)
+    V = torch.randn((Lkv, Hkv, 128), generator=gen).to(torch.bfloat16)
+    msa = _msa()
+    O, LSE = msa.sparse_attn_fwd(Q.cuda(), K.cuda(), V.cuda(), s, scale=0.09)
+    torch.cuda.synchronize()
+    assert s.query()["status"] == 0
+    s.close()
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    Or, Lr, _ = oracle.attn_fwd(bits(Q), bits(K), bits(V), idx, Lkv=Lkv, scale=0.09)
+    rel, mabs, lerr = compare_outputs(O.float().cpu().numpy(), LSE.cpu().numpy(), Or, Lr)
+    assert rel <= BF16_REL_L2 and mabs <= BF16_MAX_ABS and lerr <= LSE_MAX_ABS, (rel, mabs, lerr)
