@@ -1,7 +1,7 @@
 """Long lists: the largest list length the library takes (topK = 64, which fills both
 32-slot words of a Q-outer unit's list) and 33 (one id in the second word), through AUTO,
 both forced paths, the split Q-outer units of a single query, and (one case) the
-backward, against the fp64 oracle.
+backward, against the fp64 oracle; with bf16 and with E4M3 inputs.
 
 Lists hold up to topK distinct visible blocks in random order, so most queries attend
 many blocks; some lists also carry a duplicate, a future block or pads.  Tolerances as in
@@ -72,3 +72,31 @@ def test_long_lists_match_oracle(N, Lkv, Hkv, topK, bwd):
     rQ, rK, rV, _ = oracle.attn_bwd(bits(Q), bits(K), bits(V), bits(dO), idx, Lkv=Lkv, scale=scale)
     for got, ref in ((dQ, rQ), (dK, rK), (dV, rV)):
         assert rel_l2(got.float().cpu().numpy(), ref) <= BWD_REL_L2
+
+
+@pytest.mark.parametrize("N,Lkv,Hkv,topK", [(96, 16384, 2, 64), (1, 16384, 4, 64)])
+def test_long_lists_e4m3_match_oracle(N, Lkv, Hkv, topK):
+    """The same long lists with E4M3 inputs (per-tensor descales): the KV-outer path (V
+    widened to f16 once per call) and the Q-outer path (V widened per block in shared
+    memory), against the oracle on the decoded E4M3 values; relative L2 over O <= 5e-2,
+    |dLSE| <= 1e-3."""
+    import block_sparse_gqa_gb300 as msa
+    import workloads
+    from tests.util import FP8_REL_L2
+    rng = np.random.default_rng(N * 1000 + topK + 7)
+    shapes = [(N, 16 * Hkv, 128), (Lkv, Hkv, 128), (Lkv, Hkv, 128)]
+    (Q, dq), (K, dk), (V, dv) = (workloads.quantize_e4m3(torch.from_numpy(rng.standard_normal(sh).astype(np.float32)))
+                                 for sh in shapes)
+    idx = lists(rng, N, Lkv, Hkv, topK)
+    scale = 0.088
+    dev = torch.device("cuda")
+    s = msa.build_schedule(torch.from_numpy(idx).to(dev), Lkv // 128)
+    Or, Lr, _ = oracle.attn_fwd(Q.numpy(), K.numpy(), V.numpy(), idx, Lkv=Lkv, scale=scale, q_descale=dq,
+                                k_descale=dk, v_descale=dv)
+    for path in ("auto", "kv_outer", "q_outer"):
+        O, LSE = msa.sparse_attn_fwd(Q.to(dev), K.to(dev), V.to(dev), s, scale=scale, path=path, descales=(dq, dk, dv))
+        torch.cuda.synchronize()
+        rel, mabs, lerr = compare_outputs(O.float().cpu().numpy(), LSE.cpu().numpy(), Or, Lr)
+        assert rel <= FP8_REL_L2 and lerr <= LSE_MAX_ABS, (path, rel, mabs, lerr)
+    assert s.query()["status"] == 0
+    s.close()
