@@ -84,6 +84,32 @@ def test_noalloc_matches_allocating_path_on_two_calls_in_a_row():
         assert rel <= BF16_REL_L2 and mabs <= BF16_MAX_ABS and lerr <= LSE_MAX_ABS, (seed, rel, mabs, lerr)
 
 
+def test_noalloc_decode_step_matches_allocating_path():
+    """A decode-size call (one query at the tail of a 128K-token context): AUTO is decided by
+    the sizes alone, so both entry points launch only the Q-outer kernel, with the query's
+    list split over several CTAs whose workspace the scratch array holds.  Bit-identical to
+    the allocating pair, and equal to the oracle."""
+    import block_sparse_gqa_gb300 as msa
+    dev = torch.device("cuda")
+    wl = workloads.make_workload("decode")
+    cfg = wl.cfg
+    idx, Q, K, V = wl.indices.to(dev), wl.Q.to(dev), wl.K.to(dev), wl.V.to(dev)
+    sched = msa.build_schedule(idx, cfg.nblocks)
+    O_ref, L_ref = msa.sparse_attn_fwd(Q, K, V, sched, scale=cfg.scale)
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    st, O, LSE = noalloc_fwd(msa, idx, cfg.nblocks, Q, K, V, cfg.scale, status=status)
+    torch.cuda.synchronize()
+    assert sched.query()["path"] == 2  # the device's own choice agrees: Q-outer
+    sched.close()
+    assert st == 0, msa.lib().msa_status_string(st)
+    assert int(status.item()) == 0
+    assert torch.equal(O.view(torch.int16), O_ref.view(torch.int16))
+    assert torch.equal(LSE.view(torch.int32), L_ref.view(torch.int32))
+    Or, Lr, _ = oracle.attn_fwd(bits(wl.Q), bits(wl.K), bits(wl.V), wl.indices.numpy(), Lkv=cfg.Lkv, scale=cfg.scale)
+    rel, mabs, lerr = compare_outputs(O.float().cpu().numpy(), LSE.cpu().numpy(), Or, Lr)
+    assert rel <= BF16_REL_L2 and mabs <= BF16_MAX_ABS and lerr <= LSE_MAX_ABS, (rel, mabs, lerr)
+
+
 def test_noalloc_reports_bad_block_ids_through_status():
     import block_sparse_gqa_gb300 as msa
     dev = torch.device("cuda")
